@@ -1,0 +1,173 @@
+/*
+ * tg_gemm.h -- C ABI of a tiled dense matrix multiply for NVIDIA GB300 (sm_103a).
+ *
+ * Operation.  Every GEMM entry point computes
+ *
+ *     C[m,n] = sum_{k=0}^{K-1} A[m,k] * B[k,n]      0 <= m < M, 0 <= n < N
+ *
+ * with A of shape [M,K], B of shape [K,N] and C of shape [M,N]: "Matrix
+ * multiplication: reuse the inputs" (triton-cuda-lab lesson 6), section "The
+ * three dimensions have different jobs".  The work is split into output tiles,
+ * each accumulated over K in chunks with the accumulator kept on chip until it
+ * is written once ("Matrix Multiplication", teenygrad docs, section "Tiles";
+ * "Triton tiled matmul", llm-systems-cookbook, section "What").  Products are
+ * accumulated in FP32 whatever the input type, the choice all of those pages
+ * make, and the FP32 sum is rounded to nearest-even once into the output type.
+ *
+ * Layout.  All matrices are row-major with unit column stride and an explicit
+ * leading dimension counted in ELEMENTS: A[m,k] is at a[m*lda + k], B[k,n] at
+ * b[k*ldb + n], C[m,n] at c[m*ldc + n].  Requires lda >= K, ldb >= N, ldc >= N.
+ * Elements outside the logical [rows, cols] block (the padding up to the
+ * leading dimension) are never read and never written.
+ *
+ * Types (dtype_in, dtype_out):
+ *     (TG_F16,  TG_F16)  (TG_F16,  TG_F32)
+ *     (TG_BF16, TG_BF16) (TG_BF16, TG_F32)
+ *     (TG_F32,  TG_F32)  -- FP32 operands contracted at TF32 precision (10
+ *                           fraction bits), FP32 accumulate; the "TF32" input
+ *                           precision of the teenygrad page, section "T::dot".
+ * Any other pair returns TG_ERR_UNSUPPORTED.
+ *
+ * Ownership.  a, b and c are DEVICE pointers owned by the caller and must stay
+ * valid until the work enqueued on `stream` has finished.  The library owns only
+ * temporary device workspace (stream-ordered, freed on the same stream) and
+ * internal caches.  `stream` is a cudaStream_t passed as void*; NULL is the
+ * legacy default stream.
+ *
+ * Asynchrony and errors.  The GEMM calls validate their arguments on the host,
+ * enqueue kernels on `stream` and return without synchronising.  Argument
+ * errors are returned before anything is enqueued and leave C untouched.  A CUDA
+ * error while enqueueing returns TG_ERR_CUDA.  Every wait inside the kernels is
+ * bounded (default 2 s); a kernel whose wait runs out records TG_ERR_TIMEOUT in
+ * a per-device status word, releases what it holds and exits, which
+ * tg_last_device_error() reports.
+ *
+ * Special sizes.  M == 0 or N == 0: nothing to do, TG_OK.  K == 0: C is set to
+ * zero (the empty sum).
+ *
+ * Threading.  Calls may be made from several host threads; a device's lazily
+ * built state is created under a lock.
+ */
+#ifndef TG_GEMM_H
+#define TG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TG_ABI_VERSION 1
+
+typedef enum tg_dtype {
+    TG_F16 = 0,   /* IEEE 754 binary16 */
+    TG_BF16 = 1,  /* bfloat16 */
+    TG_F32 = 2    /* IEEE 754 binary32 */
+} tg_dtype;
+
+typedef enum tg_status {
+    TG_OK = 0,
+    TG_ERR_INVALID_VALUE = 1,    /* bad size, leading dimension, pointer or overlap */
+    TG_ERR_UNSUPPORTED = 2,      /* dtype pair or option not supported */
+    TG_ERR_OUT_OF_MEMORY = 3,    /* workspace allocation failed */
+    TG_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+    TG_ERR_ARCH = 5,             /* current device is not an sm_103 GPU */
+    TG_ERR_TIMEOUT = 6,          /* a kernel's bounded wait ran out */
+    TG_ERR_NOT_IMPLEMENTED = 7
+} tg_status;
+
+/* Execution paths the planner chooses between. */
+typedef enum tg_path {
+    TG_PATH_AUTO = 0,
+    TG_PATH_TC = 1,        /* tcgen05 tensor-core kernel, one CTA per 128-row tile */
+    TG_PATH_TC_PAIR = 2,   /* tcgen05 kernel with CTA pairs (cta_group::2), 256-row tiles */
+    TG_PATH_SKINNY = 3     /* memory-streaming kernel for small M */
+} tg_path;
+
+/* Optional overrides for tg_gemm_ex.  Zero in any field means "let the planner
+ * choose".  Values the compiled kernels cannot honour return
+ * TG_ERR_UNSUPPORTED. */
+typedef struct tg_options {
+    int32_t path;         /* tg_path */
+    int32_t splits;       /* number of K splits (>= 1) */
+    int32_t block_n;      /* output tile width: 64, 128 or 256 */
+    int32_t group_m;      /* grouped raster height in tiles (default 8) */
+    int32_t max_ctas;     /* cap on the persistent grid (default: one per SM) */
+    int32_t timeout_ms;   /* bound on every device-side wait (default 2000) */
+    int32_t reserved[2];  /* must be zero */
+} tg_options;
+
+/* What a call would launch (see tg_plan_gemm). */
+typedef struct tg_plan {
+    int32_t path;          /* tg_path actually used */
+    int32_t block_m, block_n, block_k;
+    int32_t stages;        /* shared-memory ring depth */
+    int32_t splits;        /* K splits (1 = none) */
+    int32_t group_m;
+    int32_t ctas;          /* persistent grid size */
+    int32_t pack_a;        /* 1 if A is first copied to an aligned workspace */
+    int32_t pack_b;        /* 1 if B is first copied to an aligned workspace */
+    int32_t c_vector;      /* 1 if C gets 16-byte vector stores */
+    int32_t kernels;       /* kernel launches per call */
+    int64_t tiles;         /* output tiles */
+    int64_t workspace_bytes;
+} tg_plan;
+
+/*
+ * tg_gemm -- C = A * B (see the top of this file for layout, types and errors).
+ *   M, N, K   sizes (>= 0)
+ *   a, lda    device pointer to A and its leading dimension (elements, >= K)
+ *   b, ldb    device pointer to B and its leading dimension (elements, >= N)
+ *   c, ldc    device pointer to C and its leading dimension (elements, >= N);
+ *             C must not overlap A or B
+ *   dtype_in  type of A and B; dtype_out type of C
+ *   stream    cudaStream_t (as void*) the work is enqueued on
+ */
+tg_status tg_gemm(int64_t M, int64_t N, int64_t K,
+                  const void *a, int64_t lda,
+                  const void *b, int64_t ldb,
+                  void *c, int64_t ldc,
+                  tg_dtype dtype_in, tg_dtype dtype_out,
+                  void *stream);
+
+/* tg_gemm with planner overrides (`opt` may be NULL). */
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K,
+                     const void *a, int64_t lda,
+                     const void *b, int64_t ldb,
+                     void *c, int64_t ldc,
+                     tg_dtype dtype_in, tg_dtype dtype_out,
+                     void *stream, const tg_options *opt);
+
+/*
+ * tg_plan_gemm -- host only, touches no device: validates the arguments exactly
+ * as tg_gemm_ex does (pointers are inspected for alignment and overlap only,
+ * never dereferenced) and fills *plan with what tg_gemm_ex would launch on a
+ * device with `num_sms` SMs.  Returns the status tg_gemm_ex would return for
+ * an argument error, else TG_OK.
+ */
+tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K,
+                       const void *a, int64_t lda,
+                       const void *b, int64_t ldb,
+                       const void *c, int64_t ldc,
+                       tg_dtype dtype_in, tg_dtype dtype_out,
+                       int32_t num_sms, const tg_options *opt, tg_plan *plan);
+
+/* Static, human-readable name of a status code. */
+const char *tg_status_string(tg_status status);
+
+/*
+ * tg_last_device_error -- synchronises `stream`, then reads and clears the
+ * current device's status word.  Returns TG_OK if no kernel recorded a
+ * failure since the last call, TG_ERR_TIMEOUT if a bounded wait ran out, or
+ * TG_ERR_CUDA if the synchronisation itself failed.
+ */
+tg_status tg_last_device_error(void *stream);
+
+/* TG_ABI_VERSION of the loaded library. */
+int32_t tg_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_H */

@@ -1,0 +1,151 @@
+"""The C-ABI library: builds, loads, exports what the header declares, and its
+host-only logic (validation and planning).  No compute call is made here, so
+these run without a GPU."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import tiled_matrix_multiplication_gb300 as tg
+from tiled_matrix_multiplication_gb300 import build as tgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg_gemm.h")
+
+A, B, C = 0x10000, 0x100000000, 0x200000000   # aligned, disjoint placeholder addresses
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tgbuild.build()
+    return tg.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert names == sorted(tg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(tg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert tg.tg_abi_version() == 1
+    assert tg.tg_status_string(tg.TG_OK) == "TG_OK"
+    assert tg.tg_status_string(tg.TG_ERR_TIMEOUT) == "TG_ERR_TIMEOUT"
+    assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
+
+
+def plan(M, N, K, din="f16", dout=None, lda=None, ldb=None, ldc=None, a=A, b=B, c=C, sms=148,
+         **opts):
+    dout = din if dout is None else dout
+    o = tg.make_options(**opts) if opts else None
+    return tg.tg_plan_gemm(M, N, K, a, K if lda is None else lda, b, N if ldb is None else ldb,
+                           c, N if ldc is None else ldc, din, dout, sms, o)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(M=-1, N=4, K=4), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, lda=3), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, ldb=3), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, ldc=3), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, a=0), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, c=0), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=4, N=4, K=4, a=A + 1), tg.TG_ERR_INVALID_VALUE),          # not element aligned
+    (dict(M=4, N=4, K=4, c=A + 8), tg.TG_ERR_INVALID_VALUE),          # C overlaps A
+    (dict(M=4, N=4, K=4, c=B), tg.TG_ERR_INVALID_VALUE),              # C overlaps B
+    (dict(M=4, N=4, K=4, din="f16", dout="bf16"), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, din="bf16", dout="f16"), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, din="f32", dout="f16"), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, din=7), tg.TG_ERR_INVALID_VALUE),
+    (dict(M=1 << 31, N=4, K=4), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, block_n=96), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, splits=-2), tg.TG_ERR_INVALID_VALUE),
+])
+def test_validation(lib, args, status):
+    st, _ = plan(**args)
+    assert st == status
+
+
+def test_gemm_rejects_before_touching_the_device(lib):
+    # argument errors come back before any CUDA call, so they work without a GPU
+    assert tg.tg_gemm(-1, 4, 4, A, 4, B, 4, C, 4, "f16", "f16", 0) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_gemm(4, 4, 4, A, 4, B, 4, C, 4, "f16", "bf16", 0) == tg.TG_ERR_UNSUPPORTED
+    assert tg.tg_gemm(4, 4, 4, A, 4, B, 4, A, 4, "f16", "f16", 0) == tg.TG_ERR_INVALID_VALUE
+    # empty output: nothing to do
+    assert tg.tg_gemm(0, 4, 4, 0, 4, 0, 4, 0, 4, "f16", "f16", 0) == tg.TG_OK
+    assert tg.tg_gemm(4, 0, 4, 0, 4, 0, 0, 0, 0, "f16", "f16", 0) == tg.TG_OK
+
+
+def test_plan_square_4096(lib):
+    st, p = plan(4096, 4096, 4096, sms=148)
+    assert st == tg.TG_OK
+    assert p["path"] == tg.TG_PATH_TC and p["block_m"] == 128 and p["block_k"] == 64
+    assert p["tiles"] == (4096 // 128) * (4096 // p["block_n"])
+    assert p["splits"] == 1 and p["ctas"] == 148
+    assert p["pack_a"] == 0 and p["pack_b"] == 0 and p["c_vector"] == 1
+    assert p["workspace_bytes"] == 0 and p["kernels"] == 1
+
+
+def test_plan_config1_needs_pack(lib):
+    # 127x255x65 FP16 -> FP32: lda = 65 halves = 130 bytes, ldb = 255 halves = 510 bytes
+    st, p = plan(127, 255, 65, "f16", "f32")
+    assert st == tg.TG_OK
+    assert p["pack_a"] == 1 and p["pack_b"] == 1
+    assert p["c_vector"] == 0            # ldc = 255 floats = 1020 bytes
+    assert p["workspace_bytes"] >= 127 * 72 * 2 + 65 * 256 * 2
+
+
+def test_plan_tf32(lib):
+    st, p = plan(2048, 2048, 2048, "f32", "f32")
+    assert st == tg.TG_OK and p["block_k"] == 32
+    st, p = plan(1000, 1999, 777, "f32", "f32")
+    assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 1
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 128])
+def test_plan_skinny_splits_k(lib, M):
+    st, p = plan(M, 8192, 8192, sms=148)
+    assert st == tg.TG_OK
+    assert p["splits"] > 1
+    units = p["tiles"] * p["splits"]
+    assert units >= 148 // 2
+    k_tiles = 8192 // p["block_k"]
+    assert (p["splits"] - 1) * -(-k_tiles // p["splits"]) < k_tiles   # no empty split
+    assert p["workspace_bytes"] >= p["splits"] * M * 8192 * 4
+    assert p["kernels"] == 2
+
+
+def test_plan_forced_options(lib):
+    st, p = plan(512, 512, 512, splits=3, block_n=128, group_m=4, max_ctas=7)
+    assert st == tg.TG_OK
+    assert (p["splits"], p["block_n"], p["group_m"], p["ctas"]) == (3, 128, 4, 7)
+
+
+def test_plan_zero_sizes(lib):
+    st, p = plan(0, 5, 5)
+    assert st == tg.TG_OK and p["kernels"] == 0
+    st, p = plan(5, 5, 0, lda=0)
+    assert st == tg.TG_OK and p["kernels"] == 0
+
+
+def test_python_gemm_checks_shapes():
+    torch = pytest.importorskip("torch")
+    a = torch.zeros(3, 4, dtype=torch.float16)
+    b = torch.zeros(5, 2, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        tg.gemm(a, b)
+    with pytest.raises(ValueError):   # CPU tensors are refused: no CPU path exists
+        tg.gemm(a, torch.zeros(4, 2, dtype=torch.float16))

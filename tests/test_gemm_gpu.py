@@ -1,0 +1,99 @@
+"""GPU parity of the tensor-core GEMM against the CPU oracle on small and
+ragged problems: several tiles, partial tiles in M, N and K, strided and
+misaligned operands, split K, the degenerate sizes."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from tests.conftest import cuda_ok
+from tests.gemm_util import compare, padding_untouched, run_gemm
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA device")]
+
+PAIRS = [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32")]
+SHAPES = [(1, 1, 1), (5, 7, 5), (128, 256, 64), (127, 255, 65), (129, 257, 129),
+          (256, 512, 1000), (300, 130, 70), (64, 1000, 48), (1000, 64, 300)]
+
+
+@pytest.mark.parametrize("din,dout", PAIRS)
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_integer_inputs_bit_exact(M, N, K, din, dout):
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int")
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+
+
+@pytest.mark.parametrize("din,dout", PAIRS)
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_uniform_inputs_within_tolerance(M, N, K, din, dout):
+    a, b, c = run_gemm(M, N, K, din, dout, dist="uniform")
+    compare(a, b, c, M, N, K, din, dout)
+
+
+def test_config_small_fp16_to_fp32():
+    """127 x 255 x 65, FP16 in, FP32 out, U[-1,1]: the oracle checks every element."""
+    a, b, c = run_gemm(127, 255, 65, "f16", "f32")
+    compare(a, b, c, 127, 255, 65, "f16", "f32")
+
+
+@pytest.mark.parametrize("din,dout", PAIRS)
+@pytest.mark.parametrize("lda_pad,ldb_pad,ldc_pad", [(8, 64, 8), (3, 5, 1), (0, 0, 24)])
+def test_strided_operands(din, dout, lda_pad, ldb_pad, ldc_pad):
+    """Leading dimensions above the logical width, aligned and not; the padding
+    of A and B holds NaN (so reading it would poison C) and C's padding must
+    come back untouched."""
+    M, N, K = 200, 300, 150
+    a, b, c = run_gemm(M, N, K, din, dout, dist="uniform", lda=K + lda_pad, ldb=N + ldb_pad,
+                       ldc=N + ldc_pad)
+    compare(a, b, c, M, N, K, din, dout)
+    assert padding_untouched(c, N, dout)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+@pytest.mark.parametrize("din,dout", [("f16", "f16"), ("bf16", "f32"), ("f32", "f32")])
+def test_forced_split_k(splits, din, dout):
+    M, N, K = 256, 384, 1000
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", splits=splits)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+    a, b, c = run_gemm(M, N, K, din, dout, dist="uniform", splits=splits, ldc=N + 8)
+    compare(a, b, c, M, N, K, din, dout)
+    assert padding_untouched(c, N, dout)
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("group_m,max_ctas", [(1, 0), (8, 3), (3, 1)])
+def test_tile_width_raster_and_grid(block_n, group_m, max_ctas):
+    """Every tile is produced once whatever the tile width, raster height and
+    persistent-grid size (a grid of 1 CTA walks all tiles itself)."""
+    M, N, K = 700, 900, 256
+    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", block_n=block_n, group_m=group_m,
+                       max_ctas=max_ctas)
+    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
+
+
+def test_k_zero_gives_zeros():
+    a, b, c = run_gemm(33, 17, 0, "f16", "f32", ldc=20)
+    assert np.all(c[:, :17] == 0)
+    assert padding_untouched(c, 17, "f32")
+
+
+def test_empty_output_is_noop():
+    run_gemm(0, 16, 16, "bf16", "bf16")
+    run_gemm(16, 0, 16, "bf16", "bf16")
+
+
+def test_identity_and_permutation_exact():
+    """B = I gives C = A; a permutation matrix permutes A's columns."""
+    import oracle
+    from tiled_matrix_multiplication_gb300 import inputs
+    M, K = 300, 256
+    a = inputs.matrix_bits(M, K, "bf16", "uniform", 5)
+    eye = oracle.encode(np.eye(K), "bf16")
+    _, _, c = run_gemm(M, K, K, "bf16", "bf16", a_bits=a, b_bits=eye)
+    assert np.array_equal(c, a)
+    perm = np.random.default_rng(1).permutation(K)
+    P = np.zeros((K, K))
+    P[perm, np.arange(K)] = 1.0
+    _, _, c = run_gemm(M, K, K, "bf16", "f32", a_bits=a, b_bits=oracle.encode(P, "bf16"))
+    assert np.array_equal(oracle.decode(c, "f32"), oracle.decode(a, "bf16")[:, perm])

@@ -1,0 +1,146 @@
+"""ctypes binding of ``libtg_gemm.so`` -- argument marshalling only.
+
+The names mirror the C ABI in ``include/tg_gemm.h``.  Every GEMM runs in the
+library's CUDA kernels; there is no fallback of any kind: if the library has
+not been built, or the device is not an sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
+
+TG_F16, TG_BF16, TG_F32 = 0, 1, 2
+DTYPE_CODES = {"f16": TG_F16, "bf16": TG_BF16, "f32": TG_F32}
+
+TG_OK = 0
+TG_ERR_INVALID_VALUE = 1
+TG_ERR_UNSUPPORTED = 2
+TG_ERR_OUT_OF_MEMORY = 3
+TG_ERR_CUDA = 4
+TG_ERR_ARCH = 5
+TG_ERR_TIMEOUT = 6
+TG_ERR_NOT_IMPLEMENTED = 7
+
+TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
+
+# Every extern "C" symbol the header declares.
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
+           "tg_last_device_error", "tg_abi_version")
+
+
+class tg_options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("block_n", ctypes.c_int32), ("group_m", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
+
+
+class tg_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("block_m", ctypes.c_int32),
+                ("block_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
+                ("c_vector", ctypes.c_int32), ("kernels", ctypes.c_int32),
+                ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{status_name(status)}{': ' + what if what else ''}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the library (raises if it is missing -- build it with ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -m tiled_matrix_multiplication_gb300.build)")
+        lib = ctypes.CDLL(p)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32
+        gemm_args = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, vp]
+        lib.tg_gemm.argtypes = gemm_args
+        lib.tg_gemm.restype = ctypes.c_int
+        lib.tg_gemm_ex.argtypes = gemm_args + [ctypes.POINTER(tg_options)]
+        lib.tg_gemm_ex.restype = ctypes.c_int
+        lib.tg_plan_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                     ctypes.c_int, i32, ctypes.POINTER(tg_options),
+                                     ctypes.POINTER(tg_plan)]
+        lib.tg_plan_gemm.restype = ctypes.c_int
+        lib.tg_status_string.argtypes = [ctypes.c_int]
+        lib.tg_status_string.restype = ctypes.c_char_p
+        lib.tg_last_device_error.argtypes = [vp]
+        lib.tg_last_device_error.restype = ctypes.c_int
+        lib.tg_abi_version.argtypes = []
+        lib.tg_abi_version.restype = i32
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _code(dtype) -> int:
+    return DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def make_options(path=0, splits=0, block_n=0, group_m=0, max_ctas=0, timeout_ms=0):
+    o = tg_options()
+    o.path, o.splits, o.block_n, o.group_m = path, splits, block_n, group_m
+    o.max_ctas, o.timeout_ms = max_ctas, timeout_ms
+    return o
+
+
+def status_name(status: int) -> str:
+    try:
+        return load().tg_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"tg_status({int(status)})"
+
+
+def tg_status_string(status: int) -> str:
+    return load().tg_status_string(int(status)).decode()
+
+
+def tg_abi_version() -> int:
+    return int(load().tg_abi_version())
+
+
+def tg_gemm(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream) -> int:
+    """Raw C call; pointers and stream are integers.  Returns the tg_status."""
+    return int(load().tg_gemm(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                              _code(dtype_out), stream))
+
+
+def tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, options=None) -> int:
+    opt = ctypes.byref(options) if options is not None else None
+    return int(load().tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                                 _code(dtype_out), stream, opt))
+
+
+def tg_plan_gemm(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, options=None):
+    """Returns ``(status, plan_dict)``; host only, needs no GPU."""
+    plan = tg_plan()
+    opt = ctypes.byref(options) if options is not None else None
+    st = int(load().tg_plan_gemm(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                                 _code(dtype_out), num_sms, opt, ctypes.byref(plan)))
+    return st, plan.as_dict()
+
+
+def tg_last_device_error(stream) -> int:
+    return int(load().tg_last_device_error(stream))

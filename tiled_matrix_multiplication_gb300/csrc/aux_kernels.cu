@@ -1,0 +1,113 @@
+// aux_kernels.cu -- the two memory-bound helper kernels of the GEMM path.
+//
+// pack_rows: copies a row-major block whose base or row pitch is not
+//   16-byte aligned into a workspace with an aligned pitch.  The tensor-memory
+//   copy engine (TMA) behind the "tensor descriptors" of the teenygrad page
+//   ("Matrix Multiplication", section "The real tiled loop") imposes exactly
+//   this alignment on its source; the padded columns are never read because
+//   the descriptor's logical width stays the original one.
+// splitk_reduce: C[m,n] = round(sum_{s=0}^{S-1} P[s,m,n]) in increasing s --
+//   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
+//   both steps"), finished across work units instead of inside one.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+template <typename T>
+__global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
+                                 int64_t ld_dst, int64_t rows, int64_t cols) {
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / cols;
+        const int64_t c = i - r * cols;
+        dst[r * ld_dst + c] = src[r * ld_src + c];
+    }
+}
+
+__device__ __forceinline__ void store_out(void *c, int64_t off, int out_kind, float v) {
+    if (out_kind == OUT_F32)
+        static_cast<float *>(c)[off] = v;
+    else if (out_kind == OUT_F16)
+        static_cast<__half *>(c)[off] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(c)[off] = __float2bfloat16_rn(v);
+}
+
+// One thread per 4 consecutive columns of one row.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, int64_t M,
+                                     int64_t N, void *c, int64_t ldc, int out_kind,
+                                     int vec_ok) {
+    const int64_t groups_per_row = (N + 3) / 4;
+    const int64_t total = M * groups_per_row;
+    const int64_t plane = M * N;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = g / groups_per_row;
+        const int64_t n0 = (g - m * groups_per_row) * 4;
+        const int64_t src = m * N + n0;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (vec_ok && n0 + 4 <= N) {
+            for (int s = 0; s < splits; ++s) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(partial + s * plane + src));
+                acc[0] += v.x;
+                acc[1] += v.y;
+                acc[2] += v.z;
+                acc[3] += v.w;
+            }
+        } else {
+            const int nv = static_cast<int>(N - n0 < 4 ? N - n0 : 4);
+            for (int s = 0; s < splits; ++s)
+                for (int j = 0; j < nv; ++j) acc[j] += partial[s * plane + src + j];
+        }
+        const int nv = static_cast<int>(N - n0 < 4 ? N - n0 : 4);
+        for (int j = 0; j < nv; ++j) store_out(c, m * ldc + n0 + j, out_kind, acc[j]);
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+}
+
+}  // namespace
+
+cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t rows, int64_t cols, int esize, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int threads = 256;
+    const int blocks = grid_for(rows * cols, threads);
+    if (esize == 2)
+        pack_rows_kernel<uint16_t><<<blocks, threads, 0, stream>>>(
+            static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst, rows,
+            cols);
+    else if (esize == 4)
+        pack_rows_kernel<uint32_t><<<blocks, threads, 0, stream>>>(
+            static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst, rows,
+            cols);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N, void *c,
+                                 int64_t ldc, int out_kind, int c_vector, cudaStream_t stream) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    (void)c_vector;
+    const int threads = 256;
+    const int64_t work = M * ((N + 3) / 4);
+    const int vec_ok = (N % 4) == 0;
+    splitk_reduce_kernel<<<grid_for(work, threads), threads, 0, stream>>>(partial, splits, M, N, c,
+                                                                          ldc, out_kind, vec_ok);
+    return cudaGetLastError();
+}
+
+}  // namespace tg

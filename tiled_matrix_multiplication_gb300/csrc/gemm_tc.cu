@@ -1,0 +1,432 @@
+// gemm_tc.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// C[m,n] = sum_k A[m,k] * B[k,n], A [M,K] row-major (K-major), B [K,N]
+// row-major (N-major), FP32 accumulation in tensor memory.
+//
+// What the pages' tile kernels do ("Matrix Multiplication", teenygrad docs,
+// sections "Tiles" and "The real tiled loop"; "Triton tiled matmul",
+// llm-systems-cookbook, section "The kernel"; "Fast matrix multiplication",
+// ch. 12, section "The CUDA kernel") and how it maps here:
+//   * one output tile per program, grouped raster over tiles
+//       -> a persistent grid (one CTA per SM) walks tile indices
+//          blockIdx.x, blockIdx.x + gridDim.x, ...; each index goes through the
+//          same grouped ordering (GROUP_M tile rows down, then one tile right);
+//   * K walked in BLOCK_K chunks, tiles loaded through zero-padding tensor
+//     descriptors
+//       -> one producer thread issues TMA loads of the A tile [128 x BK] and the
+//          B tile [BK x BN] into a ring of shared-memory stages, each guarded by a
+//          "full" and an "empty" mbarrier; out-of-range rows/columns/K come back
+//          as zeros, which leave the dot products unchanged;
+//   * acc = dot(a, b, acc) on the tensor cores, accumulator on chip for the
+//     whole K loop
+//       -> one thread issues tcgen05.mma into an FP32 accumulator in tensor
+//          memory (128 lanes x BN columns), double buffered so the epilogue of
+//          tile i overlaps the main loop of tile i+1;
+//   * cast and masked store of the tile, written once
+//       -> four epilogue warps read the accumulator with tcgen05.ld, round to
+//          the output type and store only in-range rows and columns.
+//   * Split-K (several work units per tile, each over a K range) writes FP32
+//     partial tiles that a separate kernel sums in a fixed order.
+//
+// Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2..5 = epilogue (warp w may read TMEM lanes 32*(w%4) .. +31).
+//
+// Every mbarrier wait is bounded; on expiry the CTA records TG_ERR_TIMEOUT in
+// the status word, raises a shared abort flag so the other roles stop early,
+// lets its in-flight copies and MMAs finish (bounded), frees its tensor memory
+// and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tg_internal.h"
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+__device__ int g_status_word[2];
+
+cudaError_t status_word_address(int **out) {
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_status_word);
+}
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr int kSmemBudget = 200 * 1024;
+
+template <int IN_KIND, int BN>
+struct TcCfg {
+    static constexpr int ESIZE = IN_KIND == IN_TF32 ? 4 : 2;
+    static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
+    static constexpr int UMMA_K = 32 / ESIZE;     // K of one tcgen05.mma
+    static constexpr int CHUNK_N = 128 / ESIZE;   // N elements in one 128-byte B row
+    static constexpr int A_STAGE = kBM * 128;     // bytes
+    static constexpr int B_STAGE = BN * 128;      // BK rows x BN columns
+    static constexpr int B_BOX = BK * 128;        // one CHUNK_N-wide TMA box
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 8 ? 8 : kSmemBudget / STAGE_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;      // two accumulator buffers
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
+    static constexpr uint32_t IDESC =
+        make_idesc(IN_KIND == IN_TF32 ? 2u : (IN_KIND == IN_BF16 ? 1u : 0u), 0u, 1u, kBM, BN);
+    static_assert(BN % CHUNK_N == 0, "tile width must be whole 128-byte chunks");
+    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+};
+
+__device__ __forceinline__ void record_failure(int *status, int code, int where) {
+    if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, where);
+}
+
+struct Work {
+    int tm, tn, split, kt0, kt1;
+};
+
+__device__ __forceinline__ Work decode_work(const TcParams &p, int w) {
+    Work r;
+    const int t = w / p.splits;
+    r.split = w - t * p.splits;
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int size_m = min(p.tiles_m - first_m, p.group_m);
+    const int q = t - g * per_group;
+    r.tm = first_m + q % size_m;
+    r.tn = q / size_m;
+    r.kt0 = r.split * p.k_tiles_per_split;
+    r.kt1 = min(r.kt0 + p.k_tiles_per_split, p.k_tiles);
+    return r;
+}
+
+// Load 32 accumulator columns of this thread's row and wait for them in one
+// statement, so no use of r[] can be scheduled ahead of the wait.
+__device__ __forceinline__ void tmem_load_32cols_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t lo, uint32_t hi) {
+    __half2 h = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(uint32_t lo, uint32_t hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Store 32 consecutive accumulator values (columns col .. col+31 of `row`).
+__device__ __forceinline__ void store_chunk(const TcParams &p, int split, int row, int col,
+                                            const uint32_t (&r)[32]) {
+    const int ncols = min(32, p.N - col);
+    if (p.splits > 1) {
+        float *dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
+        if (ncols == 32 && (p.N & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<uint4 *>(dst + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncols) dst[j] = __uint_as_float(r[j]);
+        }
+        return;
+    }
+    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
+    if (p.out_kind == OUT_F32) {
+        float *dst = static_cast<float *>(p.c) + off;
+        if (ncols == 32 && p.c_vector) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<uint4 *>(dst + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncols) dst[j] = __uint_as_float(r[j]);
+        }
+    } else if (p.out_kind == OUT_F16) {
+        __half *dst = static_cast<__half *>(p.c) + off;
+        if (ncols == 32 && p.c_vector) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+                *reinterpret_cast<uint4 *>(dst + j) =
+                    make_uint4(pack_half2(r[j], r[j + 1]), pack_half2(r[j + 2], r[j + 3]),
+                               pack_half2(r[j + 4], r[j + 5]), pack_half2(r[j + 6], r[j + 7]));
+        } else {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncols) dst[j] = __float2half_rn(__uint_as_float(r[j]));
+        }
+    } else {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.c) + off;
+        if (ncols == 32 && p.c_vector) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+                *reinterpret_cast<uint4 *>(dst + j) =
+                    make_uint4(pack_bf162(r[j], r[j + 1]), pack_bf162(r[j + 2], r[j + 3]),
+                               pack_bf162(r[j + 4], r[j + 5]), pack_bf162(r[j + 6], r[j + 7]));
+        } else {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncols) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+    }
+}
+
+template <int IN_KIND, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    using Cfg = TcCfg<IN_KIND, BN>;
+    constexpr int S = Cfg::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;       // 1024-B aligned (swizzle atoms)
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;                            // S x A_STAGE
+    const uint32_t sB = base + S * Cfg::A_STAGE;         // S x B_STAGE
+    const uint32_t bars = sB + S * Cfg::B_STAGE;
+    uint8_t *gbars = gbase + (bars - base);
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = p.tiles_m * p.tiles_n * p.splits;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Work wk = decode_work(p, w);
+                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmA, full_bar(stage), kt * Cfg::BK,
+                                wk.tm * kBM);
+#pragma unroll
+                    for (int j = 0; j < BN / Cfg::CHUNK_N; ++j)
+                        tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
+                                    full_bar(stage), wk.tn * BN + j * Cfg::CHUNK_N, kt * Cfg::BK);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                record_failure(p.status, 6, (ROLE_PRODUCER << 16) | stage);
+                *abort_flag = 1;
+            }
+            // Every issued copy must land before the CTA may exit.
+            const int64_t first = issued > S ? issued - S : 0;
+            for (int64_t i = first; i < issued; ++i) {
+                if (!mbar_wait(full_bar(static_cast<int>(i % S)),
+                               static_cast<uint32_t>((i / S) & 1), p.timeout_ns, &never_abort)) {
+                    record_failure(p.status, 6, (ROLE_DRAIN << 16) | 1);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_count = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Work wk = decode_work(p, w);
+                const uint32_t buf = acc_count & 1u;
+                const uint32_t acc_phase = (acc_count >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
+                    if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + stage * Cfg::A_STAGE;
+                    const uint32_t b0 = sB + stage * Cfg::B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(b0 + kk * Cfg::UMMA_K * 128, Cfg::B_BOX, 1024);
+                        umma_ss<Cfg::KIND, 1>(d_tmem, ad, bd, Cfg::IDESC,
+                                              (kt > wk.kt0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(buf));
+                ++acc_count;
+            }
+            if (!ok) {
+                record_failure(p.status, 6, (ROLE_MMA << 16) | stage);
+                *abort_flag = 1;
+            }
+            // All issued MMAs complete before tensor memory is released.
+            umma_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, p.timeout_ns, &never_abort))
+                record_failure(p.status, 6, (ROLE_DRAIN << 16) | 2);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        uint32_t acc_count = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const Work wk = decode_work(p, w);
+            const uint32_t buf = acc_count & 1u;
+            const uint32_t acc_phase = (acc_count >> 1) & 1u;
+            const bool got = mbar_wait(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const int row = wk.tm * kBM + quad * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_load_32cols_sync(taddr + c0, r);
+                const int col = wk.tn * BN + c0;
+                if (row < p.M && col < p.N) store_chunk(p, wk.split, row, col, r);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            ++acc_count;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int IN_KIND, int BN>
+cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const TcParams &p,
+                        int ctas, cudaStream_t stream) {
+    using Cfg = TcCfg<IN_KIND, BN>;
+    auto kern = gemm_tc_kernel<IN_KIND, BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<ctas, kThreads, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+template <int IN_KIND>
+cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const TcParams &p, int ctas, cudaStream_t stream) {
+    switch (block_n) {
+    case 128: return launch_impl<IN_KIND, 128>(tmA, tmB, p, ctas, stream);
+    case 256: return launch_impl<IN_KIND, 256>(tmA, tmB, p, ctas, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool tc_supported_block_n(int block_n) { return block_n == 128 || block_n == 256; }
+
+int tc_stages(int in_kind, int block_n) {
+    const int esz = in_kind == IN_TF32 ? 4 : 2;
+    (void)esz;
+    const int stage = kBM * 128 + block_n * 128;
+    const int s = kSmemBudget / stage;
+    return s > 8 ? 8 : s;
+}
+
+int tc_smem_bytes(int in_kind, int block_n) {
+    const int s = tc_stages(in_kind, block_n);
+    return 1024 + s * (kBM * 128 + block_n * 128) + (2 * s + 5) * 8 + 16;
+}
+
+cudaError_t launch_gemm_tc(int in_kind, int block_n, const CUtensorMap &tmA,
+                           const CUtensorMap &tmB, const TcParams &p, int ctas,
+                           cudaStream_t stream) {
+    switch (in_kind) {
+    case IN_F16: return launch_kind<IN_F16>(block_n, tmA, tmB, p, ctas, stream);
+    case IN_BF16: return launch_kind<IN_BF16>(block_n, tmA, tmB, p, ctas, stream);
+    case IN_TF32: return launch_kind<IN_TF32>(block_n, tmA, tmB, p, ctas, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tg

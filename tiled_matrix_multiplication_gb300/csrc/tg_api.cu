@@ -1,0 +1,381 @@
+// tg_api.cu -- host side of the C ABI declared in include/tg_gemm.h:
+// argument validation, planning, TMA tensor maps, workspace and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tg_gemm.h"
+#include "tg_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kBlockM = 128;
+constexpr int kDefaultGroupM = 8;
+constexpr int kDefaultTimeoutMs = 2000;
+
+struct DeviceState {
+    bool init = false;
+    tg_status arch = TG_OK;
+    int sms = 0;
+    int *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int esize_of(tg_dtype t) { return t == TG_F32 ? 4 : 2; }
+
+bool valid_dtype(int t) { return t == TG_F16 || t == TG_BF16 || t == TG_F32; }
+
+bool supported_pair(tg_dtype in, tg_dtype out) {
+    if (in == TG_F16) return out == TG_F16 || out == TG_F32;
+    if (in == TG_BF16) return out == TG_BF16 || out == TG_F32;
+    if (in == TG_F32) return out == TG_F32;
+    return false;
+}
+
+int in_kind_of(tg_dtype t) {
+    return t == TG_F16 ? tg::IN_F16 : (t == TG_BF16 ? tg::IN_BF16 : tg::IN_TF32);
+}
+
+int out_kind_of(tg_dtype t) {
+    return t == TG_F16 ? tg::OUT_F16 : (t == TG_BF16 ? tg::OUT_BF16 : tg::OUT_F32);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// Byte span [lo, hi) touched by a rows x cols block with pitch ld.
+void span(const void *p, int64_t rows, int64_t cols, int64_t ld, int esize, uintptr_t *lo,
+          uintptr_t *hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * esize);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+struct Plan {
+    tg_plan pub;
+    int64_t k_tiles = 0, k_per_split = 0, tiles_m = 0, tiles_n = 0;
+    int64_t lda_p = 0, ldb_p = 0;              // pitches after packing
+    int64_t off_a = 0, off_b = 0, off_p = 0;   // workspace offsets
+    uint64_t timeout_ns = 0;
+};
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+                   int64_t ldb, const void *c, int64_t ldc, int din, int dout,
+                   const tg_options *opt) {
+    if (!valid_dtype(din) || !valid_dtype(dout)) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_VALUE;
+    if (lda < K || ldb < N || ldc < N) return TG_ERR_INVALID_VALUE;
+    if (!supported_pair(static_cast<tg_dtype>(din), static_cast<tg_dtype>(dout)))
+        return TG_ERR_UNSUPPORTED;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TG_ERR_UNSUPPORTED;
+    if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36) || ldc > (int64_t(1) << 36))
+        return TG_ERR_UNSUPPORTED;
+    if (opt) {
+        if (opt->reserved[0] || opt->reserved[1]) return TG_ERR_INVALID_VALUE;
+        if (opt->path < TG_PATH_AUTO || opt->path > TG_PATH_SKINNY) return TG_ERR_INVALID_VALUE;
+        if (opt->splits < 0 || opt->block_n < 0 || opt->group_m < 0 || opt->max_ctas < 0 ||
+            opt->timeout_ms < 0)
+            return TG_ERR_INVALID_VALUE;
+        if (opt->block_n && !tg::tc_supported_block_n(opt->block_n)) return TG_ERR_UNSUPPORTED;
+        if (opt->path == TG_PATH_TC_PAIR || opt->path == TG_PATH_SKINNY)
+            return TG_ERR_UNSUPPORTED;
+    }
+    const int ei = esize_of(static_cast<tg_dtype>(din));
+    const int eo = esize_of(static_cast<tg_dtype>(dout));
+    if (M == 0 || N == 0) return TG_OK;
+    if (c == nullptr) return TG_ERR_INVALID_VALUE;
+    if (K > 0 && (a == nullptr || b == nullptr)) return TG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(c) % eo) != 0) return TG_ERR_INVALID_VALUE;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(a) % ei) || (reinterpret_cast<uintptr_t>(b) % ei)))
+        return TG_ERR_INVALID_VALUE;
+    uintptr_t c0, c1;
+    span(c, M, N, ldc, eo, &c0, &c1);
+    if (K > 0) {
+        uintptr_t a0, a1, b0, b1;
+        span(a, M, K, lda, ei, &a0, &a1);
+        span(b, K, N, ldb, ei, &b0, &b1);
+        if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+               int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
+               const tg_options *opt, Plan *pl) {
+    tg_plan &p = pl->pub;
+    std::memset(&p, 0, sizeof(p));
+    const int ei = esize_of(din), eo = esize_of(dout);
+    const int align_elems = 16 / ei;
+    num_sms = std::max(num_sms, 1);
+    p.path = TG_PATH_TC;
+    p.block_m = kBlockM;
+    p.block_k = 128 / ei;
+    p.block_n = (opt && opt->block_n) ? opt->block_n : (N <= 128 ? 128 : 256);
+    p.stages = tg::tc_stages(in_kind_of(din), p.block_n);
+    p.group_m = (opt && opt->group_m) ? opt->group_m : kDefaultGroupM;
+    pl->tiles_m = cdiv(M, kBlockM);
+    pl->tiles_n = cdiv(N, p.block_n);
+    p.tiles = pl->tiles_m * pl->tiles_n;
+    pl->k_tiles = std::max<int64_t>(cdiv(K, p.block_k), 1);
+    int64_t splits = 1;
+    if (opt && opt->splits) {
+        splits = opt->splits;
+    } else if (p.tiles < num_sms / 2) {
+        // Too few tiles to occupy the GPU: split K so that about one work unit
+        // per SM exists, keeping at least 4 K tiles per split.
+        splits = cdiv(num_sms, p.tiles);
+        splits = std::min<int64_t>(splits, std::max<int64_t>(pl->k_tiles / 4, 1));
+    }
+    splits = std::max<int64_t>(1, std::min<int64_t>(splits, pl->k_tiles));
+    pl->k_per_split = cdiv(pl->k_tiles, splits);
+    splits = cdiv(pl->k_tiles, pl->k_per_split);   // no empty split
+    p.splits = static_cast<int32_t>(splits);
+    const int64_t units = p.tiles * splits;
+    const int64_t cap = (opt && opt->max_ctas) ? opt->max_ctas : num_sms;
+    p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
+    p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
+    p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
+    p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0;
+    pl->lda_p = p.pack_a ? round_up(K, align_elems) : lda;
+    pl->ldb_p = p.pack_b ? round_up(N, align_elems) : ldb;
+    int64_t ws = 0;
+    if (p.pack_a) {
+        pl->off_a = ws;
+        ws = round_up(ws + M * pl->lda_p * ei, 256);
+    }
+    if (p.pack_b) {
+        pl->off_b = ws;
+        ws = round_up(ws + K * pl->ldb_p * ei, 256);
+    }
+    if (splits > 1) {
+        pl->off_p = ws;
+        ws = round_up(ws + splits * M * N * 4, 256);
+    }
+    p.workspace_bytes = ws;
+    p.kernels = p.pack_a + p.pack_b + 1 + (splits > 1 ? 1 : 0);
+    const int tmo = (opt && opt->timeout_ms) ? opt->timeout_ms : kDefaultTimeoutMs;
+    pl->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
+}
+
+tg_status init_encoder() {
+    if (g_encode) return TG_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return TG_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return TG_OK;
+}
+
+tg_status device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TG_ERR_CUDA;
+        d.sms = sms;
+        d.arch = (major == 10 && minor == 3) ? TG_OK : TG_ERR_ARCH;
+        if (d.arch == TG_OK) {
+            if (tg::status_word_address(&d.status) != cudaSuccess) return TG_ERR_CUDA;
+            if (init_encoder() != TG_OK) return TG_ERR_CUDA;
+        }
+        d.init = true;
+    }
+    *out = &d;
+    return d.arch;
+}
+
+CUtensorMapDataType tma_type(tg_dtype t) {
+    return t == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                       : (t == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+}
+
+// Row-major [rows, cols] with pitch `ld` elements; boxes of box_cols x box_rows
+// (box_cols * esize == 128 bytes), 128-byte swizzle, zero fill out of range.
+tg_status encode_2d(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
+                    int64_t ld, int box_cols, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esize_of(t))};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, tma_type(t), 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return TG_OK;
+    if (e == cudaErrorMemoryAllocation) return TG_ERR_OUT_OF_MEMORY;
+    return TG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t tg_abi_version(void) { return TG_ABI_VERSION; }
+
+const char *tg_status_string(tg_status s) {
+    switch (s) {
+    case TG_OK: return "TG_OK";
+    case TG_ERR_INVALID_VALUE: return "TG_ERR_INVALID_VALUE";
+    case TG_ERR_UNSUPPORTED: return "TG_ERR_UNSUPPORTED";
+    case TG_ERR_OUT_OF_MEMORY: return "TG_ERR_OUT_OF_MEMORY";
+    case TG_ERR_CUDA: return "TG_ERR_CUDA";
+    case TG_ERR_ARCH: return "TG_ERR_ARCH";
+    case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT";
+    case TG_ERR_NOT_IMPLEMENTED: return "TG_ERR_NOT_IMPLEMENTED";
+    default: return "TG_ERR_UNKNOWN";
+    }
+}
+
+tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda,
+                       const void *b, int64_t ldb, const void *c, int64_t ldc, tg_dtype dtype_in,
+                       tg_dtype dtype_out, int32_t num_sms, const tg_options *opt,
+                       tg_plan *plan) {
+    if (plan == nullptr) return TG_ERR_INVALID_VALUE;
+    const tg_status v = validate(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, opt);
+    if (v != TG_OK) return v;
+    Plan pl;
+    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, opt, &pl);
+    if (M == 0 || N == 0) {
+        pl.pub.kernels = 0;
+        pl.pub.workspace_bytes = 0;
+    } else if (K == 0) {
+        pl.pub.kernels = 0;   // a memset, no kernel of the library
+        pl.pub.workspace_bytes = 0;
+    }
+    *plan = pl.pub;
+    return TG_OK;
+}
+
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+                     int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
+                     void *stream, const tg_options *opt) {
+    tg_status st = validate(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, opt);
+    if (st != TG_OK) return st;
+    if (M == 0 || N == 0) return TG_OK;
+    DeviceState *dev = nullptr;
+    st = device_state(&dev);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int eo = esize_of(dtype_out);
+    if (K == 0)
+        return cuda_status(cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s));
+
+    Plan pl;
+    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl);
+    const tg_plan &p = pl.pub;
+    const int ei = esize_of(dtype_in);
+
+    uint8_t *ws = nullptr;
+    if (p.workspace_bytes > 0) {
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), p.workspace_bytes, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    auto fail = [&](tg_status code) {
+        if (ws) cudaFreeAsync(ws, s);
+        return code;
+    };
+    const void *A = a;
+    const void *B = b;
+    if (p.pack_a) {
+        A = ws + pl.off_a;
+        st = cuda_status(tg::launch_pack_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, ei, s));
+        if (st != TG_OK) return fail(st);
+    }
+    if (p.pack_b) {
+        B = ws + pl.off_b;
+        st = cuda_status(tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
+        if (st != TG_OK) return fail(st);
+    }
+    CUtensorMap tmA, tmB;
+    const int chunk = 128 / ei;
+    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, kBlockM) != TG_OK ||
+        encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k) != TG_OK)
+        return fail(TG_ERR_CUDA);
+
+    tg::TcParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    tp.M = static_cast<int32_t>(M);
+    tp.N = static_cast<int32_t>(N);
+    tp.K = static_cast<int32_t>(K);
+    tp.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    tp.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    tp.k_tiles = static_cast<int32_t>(pl.k_tiles);
+    tp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
+    tp.splits = p.splits;
+    tp.group_m = p.group_m;
+    tp.out_kind = out_kind_of(dtype_out);
+    tp.c_vector = p.c_vector;
+    tp.ldc = ldc;
+    tp.c = c;
+    tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
+    tp.status = dev->status;
+    tp.timeout_ns = pl.timeout_ns;
+    st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, tmA, tmB, tp, p.ctas, s));
+    if (st != TG_OK) return fail(st);
+    if (p.splits > 1) {
+        st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,
+                                                  tp.out_kind, p.c_vector, s));
+        if (st != TG_OK) return fail(st);
+    }
+    if (ws) {
+        if (cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
+    }
+    return TG_OK;
+}
+
+tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+                  int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
+                  void *stream) {
+    return tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, nullptr);
+}
+
+tg_status tg_last_device_error(void *stream) {
+    DeviceState *dev = nullptr;
+    const tg_status st = device_state(&dev);
+    if (st != TG_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TG_ERR_CUDA;
+    int words[2] = {0, 0};
+    if (cudaMemcpy(words, dev->status, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TG_ERR_CUDA;
+    if (words[0] != 0) {
+        const int zero[2] = {0, 0};
+        if (cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return TG_ERR_CUDA;
+        return static_cast<tg_status>(words[0]);
+    }
+    return TG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// tg_internal.h -- interface between the host side of the library (tg_api.cu)
+// and its kernels.  Not installed; the public ABI is include/tg_gemm.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tg {
+
+enum InKind : int { IN_F16 = 0, IN_BF16 = 1, IN_TF32 = 2 };
+enum OutKind : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
+
+// Device status word layout: [0] first tg_status code recorded, [1] where it
+// was recorded (role << 16 | detail).
+enum FailRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
+
+// Parameters of the tensor-core GEMM kernel (one persistent launch).
+struct TcParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n;
+    int32_t k_tiles;            // ceil(K / BK)
+    int32_t k_tiles_per_split;  // K tiles per split
+    int32_t splits;             // 1: write C; > 1: write FP32 partials
+    int32_t group_m;            // grouped raster height (tiles)
+    int32_t out_kind;           // OutKind of C
+    int32_t c_vector;           // C base and row pitch allow 16-byte stores
+    int32_t pad_;
+    int64_t ldc;                // elements
+    void *c;
+    float *partial;             // [splits][M][N] when splits > 1
+    int *status;                // device status word (2 ints)
+    uint64_t timeout_ns;
+};
+
+// gemm_tc.cu
+int tc_stages(int in_kind, int block_n);
+int tc_smem_bytes(int in_kind, int block_n);
+bool tc_supported_block_n(int block_n);
+cudaError_t launch_gemm_tc(int in_kind, int block_n, const CUtensorMap &tmA,
+                           const CUtensorMap &tmB, const TcParams &p, int ctas,
+                           cudaStream_t stream);
+cudaError_t status_word_address(int **out);
+
+// aux_kernels.cu
+cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                             int64_t rows, int64_t cols, int esize, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N,
+                                 void *c, int64_t ldc, int out_kind, int c_vector,
+                                 cudaStream_t stream);
+
+}  // namespace tg
