@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the tiled GEMM library on GB300.
+
+Default workload: one square GEMM M = N = K = 4096, FP16 operands drawn from
+U[-1, 1) (seeded), FP32 accumulation, FP16 output -- 137.4 GFLOP per call.
+A "step" is one call of the library's C ABI (``tg_gemm``) on that problem.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Measurement:
+  * inputs are resident in HBM before the timed region; each step uses the
+    next of R rotating (A, B, C) sets whose total exceeds twice the L2 size, so
+    no step finds its operands in L2;
+  * the timed region is K back-to-back steps between a barrier +
+    torch.cuda.synchronize() on both sides, timed with CUDA events recorded on
+    the stream the kernels are launched on (max over ranks);
+  * ``roofline.achieved`` divides the algorithmic FLOPs of one launch (2MNK) by
+    the average duration of the GEMM kernel, from per-step event pairs on the
+    same stream inside the timed region;
+  * ``e2e`` repeats the workload through the same C ABI with pinned HOST
+    buffers: the host->device copy of A and B and the device->host copy of C
+    are inside its timed region;
+  * SM clocks and throttle reasons are sampled with nvidia-smi during the timed
+    region;
+  * ``cpu_baseline`` times the CPU FP64 oracle (rank 0, N = 1 only) on a
+    bounded sample of output rows of the same problem.
+
+``--impl reference`` runs the CPU oracle arm instead (rank 0 only under
+torchrun); each step is a bounded sample of output rows of the same workload.
+Multi-GPU runs are independent replicas (the GEMM is not sharded): value is
+the total FLOP rate of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (FP16/BF16 at 4096³) and % of GB300 dense tensor peak, 1 GPU"
+
+WORKLOADS = {
+    # name: (M, N, K, dtype_in, dtype_out, dist, description)
+    "square4096_f16": (4096, 4096, 4096, "f16", "f16", "uniform",
+                       "square GEMM 4096^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square8192_f16": (8192, 8192, 8192, "f16", "f16", "uniform",
+                       "square GEMM 8192^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square16384_f16": (16384, 16384, 16384, "f16", "f16", "uniform",
+                        "square GEMM 16384^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "prefill_qkv_bf16": (8192, 6144, 4096, "bf16", "bf16", "normal",
+                         "prefill QKV projection 8192x6144x4096, BF16 in N(0,0.02), BF16 out"),
+    "prefill_o_bf16": (8192, 4096, 4096, "bf16", "bf16", "normal",
+                       "prefill output projection 8192x4096x4096, BF16 N(0,0.02)"),
+    "prefill_up_bf16": (8192, 14336, 4096, "bf16", "bf16", "normal",
+                        "prefill MLP up/gate (each) 8192x14336x4096, BF16 N(0,0.02)"),
+    "prefill_down_bf16": (8192, 4096, 14336, "bf16", "bf16", "normal",
+                          "prefill MLP down 8192x4096x14336, BF16 N(0,0.02)"),
+    "tf32_2048": (2048, 2048, 2048, "f32", "f32", "uniform",
+                  "FP32 operands at TF32 2048^3, FP32 out"),
+    "skinny1_f16": (1, 8192, 8192, "f16", "f16", "uniform", "skinny M=1, N=K=8192 FP16"),
+    "skinny16_f16": (16, 8192, 8192, "f16", "f16", "uniform", "skinny M=16, N=K=8192 FP16"),
+    "skinny64_f16": (64, 8192, 8192, "f16", "f16", "uniform", "skinny M=64, N=K=8192 FP16"),
+    "skinny128_f16": (128, 8192, 8192, "f16", "f16", "uniform", "skinny M=128, N=K=8192 FP16"),
+}
+DEFAULT_WORKLOAD = "square4096_f16"
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, local):
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world > 1
+
+
+def barrier(on):
+    if on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, on: bool) -> float:
+    if not on:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_matrix_multiplication_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(workload)
+    if not ent or ent.get("source_sha") != kernel_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def _gpu_id(self):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(self.dev)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:  # noqa: BLE001
+            return str(self.dev)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", self._gpu_id()],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def oracle_rate(M, N, K, din, dist, rows: int, seed_rows=12345):
+    """Time the FP64 oracle on `rows` sampled output rows; returns
+    (TFLOP/s, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    from tiled_matrix_multiplication_gb300 import inputs
+    rng = np.random.default_rng(seed_rows)
+    sel = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+    a_rows = np.concatenate([inputs.matrix_bits(1, K, din, dist, inputs.SEED_A, row_start=int(r))
+                             for r in sel])
+    b = inputs.matrix_bits(K, N, din, dist, inputs.SEED_B)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.gemm_ref_bits(a_rows, b, K=K, N=N, fmt=din)
+    dt = time.perf_counter() - t0
+    return 2.0 * len(sel) * N * K / dt / 1e12, dt, oracle.num_threads()
+
+
+def cpu_baseline(M, N, K, din, dist, target_s=10.0):
+    rate, dt, thr = oracle_rate(M, N, K, din, dist, rows=8)
+    per_row = dt / 8
+    rows = int(max(8, min(M, target_s / max(per_row, 1e-9))))
+    rate, dt, thr = oracle_rate(M, N, K, din, dist, rows=rows)
+    return {"value": rate, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"{rows} seeded output rows x all {N} columns of the {M}x{N}x{K} problem "
+                      f"({dt:.1f} s, FP64 three-loop oracle incl. decoding B)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    M, N, K, din, dout, dist, desc = WORKLOADS[args.workload]
+    _, dt0, thr = oracle_rate(M, N, K, din, dist, rows=4)
+    per_row = dt0 / 4
+    budget = 120.0
+    rows = int(max(1, min(M, budget / max(per_row * (args.steps + args.warmup), 1e-9))))
+    for _ in range(args.warmup):
+        oracle_rate(M, N, K, din, dist, rows=rows)
+    times = []
+    for s in range(args.steps):
+        _, dt, thr = oracle_rate(M, N, K, din, dist, rows=rows, seed_rows=1000 + s)
+        times.append(dt)
+    total = sum(times)
+    value = 2.0 * rows * N * K * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "M": M, "N": N, "K": K, "dtype_in": din,
+                   "dtype_out": dout, "step": f"{rows} sampled output rows of the problem"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{rows} seeded output rows x {N} columns per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import tiled_matrix_multiplication_gb300 as tg
+    from tiled_matrix_multiplication_gb300 import build as tgbuild
+    from tiled_matrix_multiplication_gb300 import inputs
+
+    dist_on = init_dist(world, local)
+    torch.cuda.set_device(local)
+    tgbuild.build()
+    tg.load()
+    M, N, K, din, dout, dist, desc = WORKLOADS[args.workload]
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    iview = {"f16": np.int16, "bf16": np.int16, "f32": np.int32}
+
+    a_bits = inputs.matrix_bits(M, K, din, dist, inputs.SEED_A)
+    b_bits = inputs.matrix_bits(K, N, din, dist, inputs.SEED_B)
+    a_host = torch.from_numpy(a_bits.view(iview[din])).view(tdt[din])
+    b_host = torch.from_numpy(b_bits.view(iview[din])).view(tdt[din])
+    set_bytes = (M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout]
+    R = max(2, -(-2 * l2 // set_bytes) + 1)
+    A0 = a_host.cuda()
+    B0 = b_host.cuda()
+    sets = []
+    for i in range(R):
+        sets.append((A0 if i == 0 else A0.clone(), B0 if i == 0 else B0.clone(),
+                     torch.empty((M, N), dtype=tdt[dout], device="cuda")))
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count)
+    code_in, code_out = tg.dtype_code(din), tg.dtype_code(dout)
+
+    def step(i):
+        a, b, c = sets[i % R]
+        st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                        code_in, code_out, sh)
+        if st != tg.TG_OK:
+            raise tg.TgError(st, "tg_gemm")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    tg.check_device_error()
+
+    K_steps = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)                                   # let nvidia-smi start sampling
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K_steps):
+        ev0[i].record(stream)
+        step(i)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(dist_on)
+    clocks = sampler.stop()
+    tg.check_device_error()
+    region_ms = ev0[0].elapsed_time(ev1[-1])
+    per_launch = [ev0[i].elapsed_time(ev1[i]) for i in range(K_steps)]
+    kernel_ms = statistics.mean(per_launch)
+    region_ms = max_over_ranks(region_ms, dist_on)
+    kernel_ms = max_over_ranks(kernel_ms, dist_on)
+
+    flops = 2.0 * M * N * K
+    ms_per_step = region_ms / K_steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e_steps = max(3, min(K_steps, 50))
+    a_pin = a_host.pin_memory()
+    b_pin = b_host.pin_memory()
+    c_pin = torch.empty((M, N), dtype=tdt[dout]).pin_memory()
+    a_d, b_d, c_d = sets[0]
+
+    def e2e_step():
+        a_d.copy_(a_pin, non_blocking=True)
+        b_d.copy_(b_pin, non_blocking=True)
+        st = tg.tg_gemm(M, N, K, a_d.data_ptr(), K, b_d.data_ptr(), N, c_d.data_ptr(), N,
+                        code_in, code_out, sh)
+        if st != tg.TG_OK:
+            raise tg.TgError(st, "tg_gemm")
+        c_pin.copy_(c_d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist_on)
+    tg.check_device_error()
+    h2d = (M * K + K * N) * ESIZE[din]
+    d2h = M * N * ESIZE[dout]
+
+    if rank != 0:
+        if dist_on:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    skinny = M <= 128
+    if skinny:
+        bound, unit = "hbm", "GB/s"
+        alg = (M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout]
+        achieved = alg / (kernel_ms * 1e-3) / 1e9
+        peak = float(pk["hbm_gbs"])
+    else:
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        peak = float(pk["bf16_tflops"]) * (0.5 if din == "f32" else 1.0)
+    roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
+            "peak_source": f"{pk_kind} ({'hbm_gbs' if skinny else 'bf16_tflops'} burst"
+                           f"{', x0.5 nominal TF32/BF16 ratio' if din == 'f32' and not skinny else ''})",
+            "kernel": "gemm_tc_kernel" + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
+            "launch_ms": round(kernel_ms, 5)}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": din,
+        "data": "synthetic",
+        "config": {"workload": desc, "M": M, "N": N, "K": K, "dtype_in": din, "dtype_out": dout,
+                   "accumulate": "f32", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB "
+                         f"(> 2x L2 {l2 / 1e6:.0f} MB)",
+                   "tile": f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}",
+                   "splits": plan["splits"], "ctas": plan["ctas"]},
+        "pct_of_peak": round(100.0 * value / world / peak, 2) if not skinny else None,
+        "clocks": clocks,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": K_steps * plan["kernels"],
+        "roofline": roof,
+        "wall_s": round(t_wall, 3),
+        "gpu": props.name,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(M, N, K, din, dist, target_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

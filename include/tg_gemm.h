@@ -106,7 +106,8 @@ typedef struct tg_plan {
     int32_t group_m;
     int32_t ctas;          /* persistent grid size */
     int32_t pack_a;        /* 1 if A is first copied to an aligned workspace */
-    int32_t pack_b;        /* 1 if B is first copied to an aligned workspace */
+    int32_t pack_b;        /* 1 if B is first copied to an aligned workspace,
+                              2 if B is first transposed into it (TF32 operands) */
     int32_t c_vector;      /* 1 if C gets 16-byte vector stores */
     int32_t kernels;       /* kernel launches per call */
     int64_t tiles;         /* output tiles */

@@ -111,8 +111,11 @@ def test_plan_config1_needs_pack(lib):
 def test_plan_tf32(lib):
     st, p = plan(2048, 2048, 2048, "f32", "f32")
     assert st == tg.TG_OK and p["block_k"] == 32
+    assert p["pack_a"] == 0 and p["pack_b"] == 2          # B^T for the K-major TF32 MMA
+    assert p["workspace_bytes"] >= 2048 * 2048 * 4 and p["kernels"] == 2
     st, p = plan(1000, 1999, 777, "f32", "f32")
-    assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 1
+    assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 2
+    assert p["workspace_bytes"] >= 1000 * 780 * 4 + 1999 * 780 * 4
 
 
 @pytest.mark.parametrize("M", [1, 16, 64, 128])

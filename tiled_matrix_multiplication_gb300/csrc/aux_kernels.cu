@@ -6,6 +6,8 @@
 //   ("Matrix Multiplication", section "The real tiled loop") imposes exactly
 //   this alignment on its source; the padded columns are never read because
 //   the descriptor's logical width stays the original one.
+// pack_transpose: writes B^T ([N, K], K contiguous) into the workspace for
+//   operand types whose MMA wants B K-major.
 // splitk_reduce: C[m,n] = round(sum_{s=0}^{S-1} P[s,m,n]) in increasing s --
 //   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
 //   both steps"), finished across work units instead of inside one.
@@ -26,6 +28,31 @@ __global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *_
         const int64_t r = i / cols;
         const int64_t c = i - r * cols;
         dst[r * ld_dst + c] = src[r * ld_src + c];
+    }
+}
+
+// dst[c * ld_dst + r] = src[r * ld_src + c] for a rows x cols block, through
+// 32 x 32 shared-memory tiles so both the reads and the writes are coalesced.
+template <typename T>
+__global__ void pack_transpose_kernel(const T *__restrict__ src, int64_t ld_src,
+                                      T *__restrict__ dst, int64_t ld_dst, int64_t rows,
+                                      int64_t cols) {
+    __shared__ T tile[32][33];
+    const int64_t tiles_c = (cols + 31) / 32;
+    const int64_t tiles_r = (rows + 31) / 32;
+    for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+        const int64_t r0 = (t / tiles_c) * 32;
+        const int64_t c0 = (t % tiles_c) * 32;
+        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+            const int64_t r = r0 + i, c = c0 + threadIdx.x;
+            if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * ld_src + c];
+        }
+        __syncthreads();
+        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+            const int64_t c = c0 + i, r = r0 + threadIdx.x;
+            if (r < rows && c < cols) dst[c * ld_dst + r] = tile[threadIdx.x][i];
+        }
+        __syncthreads();
     }
 }
 
@@ -93,6 +120,25 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
         pack_rows_kernel<uint32_t><<<blocks, threads, 0, stream>>>(
             static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst, rows,
             cols);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                                  int64_t rows, int64_t cols, int esize, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+    const dim3 block(32, 8);
+    const int blocks = grid_for(tiles * 256, 256);
+    if (esize == 2)
+        pack_transpose_kernel<uint16_t><<<blocks, block, 0, stream>>>(
+            static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst,
+            rows, cols);
+    else if (esize == 4)
+        pack_transpose_kernel<uint32_t><<<blocks, block, 0, stream>>>(
+            static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst,
+            rows, cols);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

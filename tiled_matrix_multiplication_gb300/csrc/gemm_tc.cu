@@ -70,8 +70,14 @@ struct TcCfg {
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
+    // B operand layout in shared memory.  16-bit operands are consumed
+    // N-major, straight from row-major B.  kind::tf32 is given a K-major B
+    // (the host transposes B into the workspace first): an N-major B tile
+    // produced all-zero results with kind::tf32 on this hardware.
+    static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
     static constexpr uint32_t IDESC =
-        make_idesc(IN_KIND == IN_TF32 ? 2u : (IN_KIND == IN_BF16 ? 1u : 0u), 0u, 1u, kBM, BN);
+        make_idesc(IN_KIND == IN_TF32 ? 2u : (IN_KIND == IN_BF16 ? 1u : 0u), 0u,
+                   B_KMAJOR ? 0u : 1u, kBM, BN);
     static_assert(BN % CHUNK_N == 0, "tile width must be whole 128-byte chunks");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
@@ -261,10 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
                     tma_load_2d(sA + stage * Cfg::A_STAGE, &tmA, full_bar(stage), kt * Cfg::BK,
                                 wk.tm * kBM);
+                    if constexpr (Cfg::B_KMAJOR) {
+                        // B^T tile [BN rows of N] x [BK of K], one box
+                        tma_load_2d(sB + stage * Cfg::B_STAGE, &tmB, full_bar(stage), kt * Cfg::BK,
+                                    wk.tn * BN);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < BN / Cfg::CHUNK_N; ++j)
-                        tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
-                                    full_bar(stage), wk.tn * BN + j * Cfg::CHUNK_N, kt * Cfg::BK);
+                        for (int j = 0; j < BN / Cfg::CHUNK_N; ++j)
+                            tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
+                                        full_bar(stage), wk.tn * BN + j * Cfg::CHUNK_N,
+                                        kt * Cfg::BK);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -316,7 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                         const uint64_t bd =
-                            smem_desc_sw128(b0 + kk * Cfg::UMMA_K * 128, Cfg::B_BOX, 1024);
+                            Cfg::B_KMAJOR
+                                ? smem_desc_sw128(b0 + kk * 32, 16, 1024)
+                                : smem_desc_sw128(b0 + kk * Cfg::UMMA_K * 128, Cfg::B_BOX, 1024);
                         umma_ss<Cfg::KIND, 1>(d_tmem, ad, bd, Cfg::IDESC,
                                               (kt > wk.kt0 || kk > 0) ? 1u : 0u);
                     }

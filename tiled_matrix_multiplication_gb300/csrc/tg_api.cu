@@ -154,9 +154,11 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
     p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
     p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
+    if (din == TG_F32) p.pack_b = 2;   // kind::tf32 reads B K-major: B^T into the workspace
     p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0;
     pl->lda_p = p.pack_a ? round_up(K, align_elems) : lda;
-    pl->ldb_p = p.pack_b ? round_up(N, align_elems) : ldb;
+    pl->ldb_p = p.pack_b == 2 ? round_up(K, align_elems)
+                              : (p.pack_b ? round_up(N, align_elems) : ldb);
     int64_t ws = 0;
     if (p.pack_a) {
         pl->off_a = ws;
@@ -164,14 +166,14 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     }
     if (p.pack_b) {
         pl->off_b = ws;
-        ws = round_up(ws + K * pl->ldb_p * ei, 256);
+        ws = round_up(ws + (p.pack_b == 2 ? N : K) * pl->ldb_p * ei, 256);
     }
     if (splits > 1) {
         pl->off_p = ws;
         ws = round_up(ws + splits * M * N * 4, 256);
     }
     p.workspace_bytes = ws;
-    p.kernels = p.pack_a + p.pack_b + 1 + (splits > 1 ? 1 : 0);
+    p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (splits > 1 ? 1 : 0);
     const int tmo = (opt && opt->timeout_ms) ? opt->timeout_ms : kDefaultTimeoutMs;
     pl->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
 }
@@ -315,13 +317,17 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     }
     if (p.pack_b) {
         B = ws + pl.off_b;
-        st = cuda_status(tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
+        st = cuda_status(p.pack_b == 2
+                             ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
+                             : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
         if (st != TG_OK) return fail(st);
     }
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
-    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, kBlockM) != TG_OK ||
-        encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k) != TG_OK)
+    const tg_status sb = p.pack_b == 2
+                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, p.block_n)
+                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k);
+    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, kBlockM) != TG_OK || sb != TG_OK)
         return fail(TG_ERR_CUDA);
 
     tg::TcParams tp;

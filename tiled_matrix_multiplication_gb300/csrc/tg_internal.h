@@ -45,6 +45,8 @@ cudaError_t status_word_address(int **out);
 // aux_kernels.cu
 cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int esize, cudaStream_t stream);
+cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                                  int64_t rows, int64_t cols, int esize, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N,
                                  void *c, int64_t ldc, int out_kind, int c_vector,
                                  cudaStream_t stream);
