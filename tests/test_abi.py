@@ -92,8 +92,8 @@ def test_gemm_rejects_before_touching_the_device(lib):
 def test_plan_square_4096(lib):
     st, p = plan(4096, 4096, 4096, sms=148)
     assert st == tg.TG_OK
-    assert p["path"] == tg.TG_PATH_TC and p["block_m"] == 128 and p["block_k"] == 64
-    assert p["tiles"] == (4096 // 128) * (4096 // p["block_n"])
+    assert p["path"] == tg.TG_PATH_TC_PAIR and p["block_m"] == 256 and p["block_k"] == 64
+    assert p["tiles"] == (4096 // 256) * (4096 // p["block_n"])
     assert p["splits"] == 1 and p["ctas"] == 148
     assert p["pack_a"] == 0 and p["pack_b"] == 0 and p["c_vector"] == 1
     assert p["workspace_bytes"] == 0 and p["kernels"] == 1
@@ -132,9 +132,29 @@ def test_plan_skinny_splits_k(lib, M):
 
 
 def test_plan_forced_options(lib):
-    st, p = plan(512, 512, 512, splits=3, block_n=128, group_m=4, max_ctas=7)
+    st, p = plan(512, 512, 512, splits=3, block_n=128, group_m=4, max_ctas=7, path=tg.TG_PATH_TC)
     assert st == tg.TG_OK
     assert (p["splits"], p["block_n"], p["group_m"], p["ctas"]) == (3, 128, 4, 7)
+    st, p = plan(512, 512, 512, max_ctas=1)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC and p["ctas"] == 1
+    st, p = plan(1024, 1024, 512, path=tg.TG_PATH_TC_PAIR, block_n=128, max_ctas=10)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR and p["block_m"] == 256
+    assert p["ctas"] == 10 and p["tiles"] == 4 * 8
+
+
+def test_plan_pair_width_limits(lib):
+    st, _ = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=224)
+    assert st == tg.TG_ERR_UNSUPPORTED
+    st, _ = plan(512, 512, 512, path=tg.TG_PATH_SKINNY)
+    assert st == tg.TG_ERR_UNSUPPORTED
+
+
+def test_plan_prefers_pairs_for_large_and_single_ctas_for_skinny(lib):
+    for M, N, K in [(8192, 8192, 8192), (8192, 14336, 4096), (8192, 4096, 14336)]:
+        st, p = plan(M, N, K, "bf16", sms=148)
+        assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR
+    st, p = plan(16, 8192, 8192, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC
 
 
 def test_plan_zero_sizes(lib):

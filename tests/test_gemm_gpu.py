@@ -97,3 +97,28 @@ def test_identity_and_permutation_exact():
     P[perm, np.arange(K)] = 1.0
     _, _, c = run_gemm(M, K, K, "bf16", "f32", a_bits=a, b_bits=oracle.encode(P, "bf16"))
     assert np.array_equal(oracle.decode(c, "f32"), oracle.decode(a, "bf16")[:, perm])
+
+
+PATHS = {"tc": 1, "pair": 2}
+
+
+@pytest.mark.parametrize("path", ["tc", "pair"])
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("din,dout", [("f16", "f16"), ("bf16", "f32"), ("f32", "f32")])
+@pytest.mark.parametrize("M,N,K", [(100, 300, 200), (300, 520, 333), (513, 257, 1000),
+                                   (1024, 1024, 64)])
+def test_forced_paths_exact(path, block_n, din, dout, M, N, K):
+    """Each kernel variant on its own, with ragged tiles: for a pair, M = 100 leaves
+    the peer CTA's rows entirely out of range and M = 300 leaves a partial peer."""
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=PATHS[path], block_n=block_n)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("max_ctas", [0, 2, 6])
+def test_pair_split_and_grid(splits, max_ctas):
+    M, N, K = 700, 900, 640
+    a, b, c = run_gemm(M, N, K, "bf16", "bf16", dist="uniform", path=PATHS["pair"], splits=splits,
+                       max_ctas=max_ctas, ldc=N + 8)
+    compare(a, b, c, M, N, K, "bf16", "bf16")
+    assert padding_untouched(c, N, "bf16")

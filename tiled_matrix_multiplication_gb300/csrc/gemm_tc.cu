@@ -8,25 +8,41 @@
 // llm-systems-cookbook, section "The kernel"; "Fast matrix multiplication",
 // ch. 12, section "The CUDA kernel") and how it maps here:
 //   * one output tile per program, grouped raster over tiles
-//       -> a persistent grid (one CTA per SM) walks tile indices
-//          blockIdx.x, blockIdx.x + gridDim.x, ...; each index goes through the
-//          same grouped ordering (GROUP_M tile rows down, then one tile right);
+//       -> a persistent grid (one CTA, or one CTA pair, per SM / SM pair)
+//          walks tile indices unit0, unit0 + units_per_step, ...; each index
+//          goes through the grouped ordering (GROUP_M tile rows down, then one
+//          tile right);
 //   * K walked in BLOCK_K chunks, tiles loaded through zero-padding tensor
 //     descriptors
-//       -> one producer thread issues TMA loads of the A tile [128 x BK] and the
-//          B tile [BK x BN] into a ring of shared-memory stages, each guarded by a
-//          "full" and an "empty" mbarrier; out-of-range rows/columns/K come back
-//          as zeros, which leave the dot products unchanged;
+//       -> one producer thread issues TMA loads of the A tile and the B tile
+//          into a ring of shared-memory stages, each guarded by a "full" and an
+//          "empty" mbarrier; out-of-range rows/columns/K come back as zeros,
+//          which leave the dot products unchanged;
 //   * acc = dot(a, b, acc) on the tensor cores, accumulator on chip for the
 //     whole K loop
 //       -> one thread issues tcgen05.mma into an FP32 accumulator in tensor
-//          memory (128 lanes x BN columns), double buffered so the epilogue of
-//          tile i overlaps the main loop of tile i+1;
+//          memory (128 lanes x BN columns per CTA), double buffered so the
+//          epilogue of tile i overlaps the main loop of tile i+1;
 //   * cast and masked store of the tile, written once
 //       -> four epilogue warps read the accumulator with tcgen05.ld, round to
 //          the output type and store only in-range rows and columns.
 //   * Split-K (several work units per tile, each over a K range) writes FP32
 //     partial tiles that a separate kernel sums in a fixed order.
+//
+// Two variants:
+//   PAIR = false: one CTA owns a 128 x BN tile (tcgen05 cta_group::1).
+//   PAIR = true : a cluster of two CTAs owns a 256 x BN tile (cta_group::2).
+//     Each CTA loads its own 128 rows of A and half (BN/2 columns) of B; the
+//     leader CTA (rank 0) issues the MMAs, which read A and B from both CTAs'
+//     shared memory and leave rows 0..127 of the accumulator in the leader's
+//     tensor memory and rows 128..255 in the peer's.  Per SM this halves the
+//     B bytes that have to be staged per FLOP.
+//     Synchronisation of the pair:
+//       full[s]   leader's only: one arrive (leader, expect_tx of both CTAs'
+//                 bytes) + the TMA completions of both CTAs;
+//       empty[s]  in both CTAs: the leader's MMA commit, multicast to both;
+//       tfull[b]  in both CTAs: the leader's commit after a tile's last MMA;
+//       tempty[b] leader's only: one arrive per epilogue warp of both CTAs.
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = epilogue (warp w may read TMEM lanes 32*(w%4) .. +31).
@@ -37,6 +53,8 @@
 // and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "tg_internal.h"
 #include "tg_ptx.cuh"
@@ -51,36 +69,46 @@ cudaError_t status_word_address(int **out) {
 
 namespace {
 
-constexpr int kBM = 128;
 constexpr int kThreads = 192;
 constexpr int kSmemBudget = 200 * 1024;
 
-template <int IN_KIND, int BN>
+template <int IN_KIND, int BN, bool PAIR>
 struct TcCfg {
     static constexpr int ESIZE = IN_KIND == IN_TF32 ? 4 : 2;
     static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
     static constexpr int UMMA_K = 32 / ESIZE;     // K of one tcgen05.mma
     static constexpr int CHUNK_N = 128 / ESIZE;   // N elements in one 128-byte B row
-    static constexpr int A_STAGE = kBM * 128;     // bytes
-    static constexpr int B_STAGE = BN * 128;      // BK rows x BN columns
-    static constexpr int B_BOX = BK * 128;        // one CHUNK_N-wide TMA box
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 8 ? 8 : kSmemBudget / STAGE_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;      // two accumulator buffers
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
+    static constexpr int CTA_GROUP = PAIR ? 2 : 1;
+    static constexpr int CTA_M = 128;             // accumulator rows held by one CTA
+    static constexpr int TILE_M = PAIR ? 256 : 128;
+    static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
     // B operand layout in shared memory.  16-bit operands are consumed
     // N-major, straight from row-major B.  kind::tf32 is given a K-major B
     // (the host transposes B into the workspace first): an N-major B tile
     // produced all-zero results with kind::tf32 on this hardware.
     static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
+    static constexpr int A_STAGE = CTA_M * 128;   // bytes
+    static constexpr int B_BOX = BK * 128;        // one CHUNK_N-wide N-major TMA box
+    static constexpr int B_CHUNKS = (BN_CTA + CHUNK_N - 1) / CHUNK_N;
+    // N-major: whole 128-byte chunks (the last one may run past BN_CTA);
+    // K-major: BN_CTA rows of 128 bytes.
+    static constexpr int B_STAGE = B_KMAJOR ? BN_CTA * 128 : B_CHUNKS * B_BOX;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int TX_BYTES = STAGE_BYTES * CTA_GROUP;   // per full-barrier phase
+    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 8 ? 8 : kSmemBudget / STAGE_BYTES;
+    static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;   // TMEM columns per buffer
+    static constexpr int TMEM_COLS = 2 * ACC_STRIDE;           // two accumulator buffers
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     static constexpr uint32_t IDESC =
         make_idesc(IN_KIND == IN_TF32 ? 2u : (IN_KIND == IN_BF16 ? 1u : 0u), 0u,
-                   B_KMAJOR ? 0u : 1u, kBM, BN);
-    static_assert(BN % CHUNK_N == 0, "tile width must be whole 128-byte chunks");
+                   B_KMAJOR ? 0u : 1u, TILE_M, BN);
+    static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
+    static_assert(!PAIR || (BN_CTA % CHUNK_N == 0 || B_KMAJOR), "pair halves of whole chunks");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
 };
 
 __device__ __forceinline__ void record_failure(int *status, int code, int where) {
@@ -147,7 +175,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<uint4 *>(dst + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
         } else {
-            #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j < ncols) dst[j] = __uint_as_float(r[j]);
         }
@@ -161,7 +189,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<uint4 *>(dst + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
         } else {
-            #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j < ncols) dst[j] = __uint_as_float(r[j]);
         }
@@ -174,7 +202,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
                     make_uint4(pack_half2(r[j], r[j + 1]), pack_half2(r[j + 2], r[j + 3]),
                                pack_half2(r[j + 4], r[j + 5]), pack_half2(r[j + 6], r[j + 7]));
         } else {
-            #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j < ncols) dst[j] = __float2half_rn(__uint_as_float(r[j]));
         }
@@ -187,19 +215,20 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
                     make_uint4(pack_bf162(r[j], r[j + 1]), pack_bf162(r[j + 2], r[j + 3]),
                                pack_bf162(r[j + 4], r[j + 5]), pack_bf162(r[j + 6], r[j + 7]));
         } else {
-            #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j < ncols) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
         }
     }
 }
 
-template <int IN_KIND, int BN>
+template <int IN_KIND, int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
-    using Cfg = TcCfg<IN_KIND, BN>;
+    using Cfg = TcCfg<IN_KIND, BN, PAIR>;
     constexpr int S = Cfg::STAGES;
+    constexpr int CG = Cfg::CTA_GROUP;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -220,6 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
+    const bool leader = rank == 0;
+    const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -228,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);
+            mbar_init(tempty_bar(b), 4 * CG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -240,11 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
-        tmem_relinquish<1>();
+        tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();   // peer barriers initialised before any remote signal
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -257,26 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int w = unit0; w < total && ok; w += unit_step) {
                 const Work wk = decode_work(p, w);
+                const int row0 = wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M;
+                const int col0 = wk.tn * BN + static_cast<int>(rank) * Cfg::BN_CTA;
                 for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
-                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmA, full_bar(stage), kt * Cfg::BK,
-                                wk.tm * kBM);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+                    const uint32_t fb = PAIR ? map_to_cta(full_bar(stage), 0) : full_bar(stage);
+                    auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
+                        if constexpr (PAIR)
+                            tma_load_2d_pair(dst, map, fb, x, y);
+                        else
+                            tma_load_2d(dst, map, fb, x, y);
+                    };
+                    load(sA + stage * Cfg::A_STAGE, &tmA, kt * Cfg::BK, row0);
                     if constexpr (Cfg::B_KMAJOR) {
-                        // B^T tile [BN rows of N] x [BK of K], one box
-                        tma_load_2d(sB + stage * Cfg::B_STAGE, &tmB, full_bar(stage), kt * Cfg::BK,
-                                    wk.tn * BN);
+                        // B^T tile [BN_CTA rows of N] x [BK of K], one box
+                        load(sB + stage * Cfg::B_STAGE, &tmB, kt * Cfg::BK, col0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / Cfg::CHUNK_N; ++j)
-                            tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
-                                        full_bar(stage), wk.tn * BN + j * Cfg::CHUNK_N,
-                                        kt * Cfg::BK);
+                        for (int j = 0; j < Cfg::B_CHUNKS; ++j)
+                            load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
+                                 col0 + j * Cfg::CHUNK_N, kt * Cfg::BK);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -289,34 +329,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 record_failure(p.status, 6, (ROLE_PRODUCER << 16) | stage);
                 *abort_flag = 1;
             }
-            // Every issued copy must land before the CTA may exit.
-            const int64_t first = issued > S ? issued - S : 0;
-            for (int64_t i = first; i < issued; ++i) {
-                if (!mbar_wait(full_bar(static_cast<int>(i % S)),
-                               static_cast<uint32_t>((i / S) & 1), p.timeout_ns, &never_abort)) {
-                    record_failure(p.status, 6, (ROLE_DRAIN << 16) | 1);
-                    break;
+            // Every issued copy must land before the CTA may exit.  The full
+            // barriers live in the leader, which waits for both CTAs' copies.
+            if (leader) {
+                const int64_t first = issued > S ? issued - S : 0;
+                for (int64_t i = first; i < issued; ++i) {
+                    if (!mbar_wait(full_bar(static_cast<int>(i % S)),
+                                   static_cast<uint32_t>((i / S) & 1), p.timeout_ns,
+                                   &never_abort)) {
+                        record_failure(p.status, 6, (ROLE_DRAIN << 16) | 1);
+                        break;
+                    }
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_count = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int w = unit0; w < total && ok; w += unit_step) {
                 const Work wk = decode_work(p, w);
                 const uint32_t buf = acc_count & 1u;
                 const uint32_t acc_phase = (acc_count >> 1) & 1u;
-                if (!mbar_wait(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                if (!mbar_wait<PAIR>(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * BN;
+                const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_STRIDE;
                 for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
                     if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
                         ok = false;
@@ -332,17 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             Cfg::B_KMAJOR
                                 ? smem_desc_sw128(b0 + kk * 32, 16, 1024)
                                 : smem_desc_sw128(b0 + kk * Cfg::UMMA_K * 128, Cfg::B_BOX, 1024);
-                        umma_ss<Cfg::KIND, 1>(d_tmem, ad, bd, Cfg::IDESC,
-                                              (kt > wk.kt0 || kk > 0) ? 1u : 0u);
+                        umma_ss<Cfg::KIND, CG>(d_tmem, ad, bd, Cfg::IDESC,
+                                               (kt > wk.kt0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(stage));
+                    if constexpr (PAIR)
+                        umma_commit_pair(empty_bar(stage), 0x3);
+                    else
+                        umma_commit(empty_bar(stage));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(buf));
+                if constexpr (PAIR)
+                    umma_commit_pair(tfull_bar(buf), 0x3);
+                else
+                    umma_commit(tfull_bar(buf));
                 ++acc_count;
             }
             if (!ok) {
@@ -350,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
             }
             // All issued MMAs complete before tensor memory is released.
-            umma_commit(drain_bar);
+            if constexpr (PAIR)
+                umma_commit_pair(drain_bar, 0x1);
+            else
+                umma_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, p.timeout_ns, &never_abort))
                 record_failure(p.status, 6, (ROLE_DRAIN << 16) | 2);
         }
@@ -359,19 +412,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
         uint32_t acc_count = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        for (int w = unit0; w < total; w += unit_step) {
             const Work wk = decode_work(p, w);
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
-            const bool got = mbar_wait(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
+            const bool got = mbar_wait<PAIR>(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after_sync();
-            const int row = wk.tm * kBM + quad * 32 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
+            const int row =
+                wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M + quad * 32 + lane;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_STRIDE;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
@@ -381,65 +436,142 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(tempty_bar(buf), 0);
+                else
+                    mbar_arrive(tempty_bar(buf));
+            }
             ++acc_count;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();   // the peer is done with this CTA's smem/TMEM
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
-template <int IN_KIND, int BN>
+struct ClusterCache {
+    std::mutex mu;
+    int max_clusters[64] = {0};
+};
+
+template <int IN_KIND, int BN, bool PAIR>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const TcParams &p,
                         int ctas, cudaStream_t stream) {
-    using Cfg = TcCfg<IN_KIND, BN>;
-    auto kern = gemm_tc_kernel<IN_KIND, BN>;
+    using Cfg = TcCfg<IN_KIND, BN, PAIR>;
+    auto kern = gemm_tc_kernel<IN_KIND, BN, PAIR>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<ctas, kThreads, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    if constexpr (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // Cap the persistent grid at the clusters that fit at once.
+        static ClusterCache cache;
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        int maxc = 0;
+        {
+            std::lock_guard<std::mutex> lk(cache.mu);
+            maxc = (dev >= 0 && dev < 64) ? cache.max_clusters[dev] : 0;
+        }
+        if (maxc == 0) {
+            cfg.gridDim = dim3(2, 1, 1);
+            if ((e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg)) != cudaSuccess) return e;
+            if (maxc < 1) return cudaErrorInvalidConfiguration;
+            std::lock_guard<std::mutex> lk(cache.mu);
+            if (dev >= 0 && dev < 64) cache.max_clusters[dev] = maxc;
+        }
+        int pairs = (ctas + 1) / 2;
+        if (pairs > maxc) pairs = maxc;
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+    } else {
+        cfg.gridDim = dim3(ctas, 1, 1);
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int IN_KIND>
+template <int IN_KIND, bool PAIR>
 cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const TcParams &p, int ctas, cudaStream_t stream) {
+    if constexpr (PAIR) {
+        switch (block_n) {
+        case 128: return launch_impl<IN_KIND, 128, true>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, true>(tmA, tmB, p, ctas, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (block_n) {
+        case 128: return launch_impl<IN_KIND, 128, false>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, false>(tmA, tmB, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, false>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, false>(tmA, tmB, p, ctas, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+template <int IN_KIND, bool PAIR>
+int stages_kind(int block_n) {
     switch (block_n) {
-    case 128: return launch_impl<IN_KIND, 128>(tmA, tmB, p, ctas, stream);
-    case 256: return launch_impl<IN_KIND, 256>(tmA, tmB, p, ctas, stream);
-    default: return cudaErrorInvalidValue;
+    case 128: return TcCfg<IN_KIND, 128, PAIR>::STAGES;
+    case 192: return PAIR ? 0 : TcCfg<IN_KIND, 192, false>::STAGES;
+    case 224: return PAIR ? 0 : TcCfg<IN_KIND, 224, false>::STAGES;
+    case 256: return TcCfg<IN_KIND, 256, PAIR>::STAGES;
+    default: return 0;
     }
 }
 
 }  // namespace
 
-bool tc_supported_block_n(int block_n) { return block_n == 128 || block_n == 256; }
-
-int tc_stages(int in_kind, int block_n) {
-    const int esz = in_kind == IN_TF32 ? 4 : 2;
-    (void)esz;
-    const int stage = kBM * 128 + block_n * 128;
-    const int s = kSmemBudget / stage;
-    return s > 8 ? 8 : s;
+bool tc_supported_block_n(int block_n, bool pair) {
+    if (pair) return block_n == 128 || block_n == 256;
+    return block_n == 128 || block_n == 192 || block_n == 224 || block_n == 256;
 }
 
-int tc_smem_bytes(int in_kind, int block_n) {
-    const int s = tc_stages(in_kind, block_n);
-    return 1024 + s * (kBM * 128 + block_n * 128) + (2 * s + 5) * 8 + 16;
+int tc_stages(int in_kind, int block_n, bool pair) {
+    switch (in_kind) {
+    case IN_F16:
+        return pair ? stages_kind<IN_F16, true>(block_n) : stages_kind<IN_F16, false>(block_n);
+    case IN_BF16:
+        return pair ? stages_kind<IN_BF16, true>(block_n) : stages_kind<IN_BF16, false>(block_n);
+    case IN_TF32:
+        return pair ? stages_kind<IN_TF32, true>(block_n) : stages_kind<IN_TF32, false>(block_n);
+    default: return 0;
+    }
 }
 
-cudaError_t launch_gemm_tc(int in_kind, int block_n, const CUtensorMap &tmA,
+cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream) {
     switch (in_kind) {
-    case IN_F16: return launch_kind<IN_F16>(block_n, tmA, tmB, p, ctas, stream);
-    case IN_BF16: return launch_kind<IN_BF16>(block_n, tmA, tmB, p, ctas, stream);
-    case IN_TF32: return launch_kind<IN_TF32>(block_n, tmA, tmB, p, ctas, stream);
+    case IN_F16:
+        return pair ? launch_kind<IN_F16, true>(block_n, tmA, tmB, p, ctas, stream)
+                    : launch_kind<IN_F16, false>(block_n, tmA, tmB, p, ctas, stream);
+    case IN_BF16:
+        return pair ? launch_kind<IN_BF16, true>(block_n, tmA, tmB, p, ctas, stream)
+                    : launch_kind<IN_BF16, false>(block_n, tmA, tmB, p, ctas, stream);
+    case IN_TF32:
+        return pair ? launch_kind<IN_TF32, true>(block_n, tmA, tmB, p, ctas, stream)
+                    : launch_kind<IN_TF32, false>(block_n, tmA, tmB, p, ctas, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -95,9 +95,14 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
         if (opt->splits < 0 || opt->block_n < 0 || opt->group_m < 0 || opt->max_ctas < 0 ||
             opt->timeout_ms < 0)
             return TG_ERR_INVALID_VALUE;
-        if (opt->block_n && !tg::tc_supported_block_n(opt->block_n)) return TG_ERR_UNSUPPORTED;
-        if (opt->path == TG_PATH_TC_PAIR || opt->path == TG_PATH_SKINNY)
-            return TG_ERR_UNSUPPORTED;
+        if (opt->path == TG_PATH_SKINNY) return TG_ERR_UNSUPPORTED;
+        if (opt->block_n) {
+            const bool one = tg::tc_supported_block_n(opt->block_n, false);
+            const bool two = tg::tc_supported_block_n(opt->block_n, true);
+            if ((opt->path == TG_PATH_TC && !one) || (opt->path == TG_PATH_TC_PAIR && !two) ||
+                (!one && !two))
+                return TG_ERR_UNSUPPORTED;
+        }
     }
     const int ei = esize_of(static_cast<tg_dtype>(din));
     const int eo = esize_of(static_cast<tg_dtype>(dout));
@@ -126,32 +131,70 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     const int ei = esize_of(din), eo = esize_of(dout);
     const int align_elems = 16 / ei;
     num_sms = std::max(num_sms, 1);
-    p.path = TG_PATH_TC;
-    p.block_m = kBlockM;
     p.block_k = 128 / ei;
-    p.block_n = (opt && opt->block_n) ? opt->block_n : (N <= 128 ? 128 : 256);
-    p.stages = tg::tc_stages(in_kind_of(din), p.block_n);
     p.group_m = (opt && opt->group_m) ? opt->group_m : kDefaultGroupM;
-    pl->tiles_m = cdiv(M, kBlockM);
-    pl->tiles_n = cdiv(N, p.block_n);
-    p.tiles = pl->tiles_m * pl->tiles_n;
     pl->k_tiles = std::max<int64_t>(cdiv(K, p.block_k), 1);
-    int64_t splits = 1;
-    if (opt && opt->splits) {
-        splits = opt->splits;
-    } else if (p.tiles < num_sms / 2) {
-        // Too few tiles to occupy the GPU: split K so that about one work unit
-        // per SM exists, keeping at least 4 K tiles per split.
-        splits = cdiv(num_sms, p.tiles);
-        splits = std::min<int64_t>(splits, std::max<int64_t>(pl->k_tiles / 4, 1));
-    }
-    splits = std::max<int64_t>(1, std::min<int64_t>(splits, pl->k_tiles));
-    pl->k_per_split = cdiv(pl->k_tiles, splits);
-    splits = cdiv(pl->k_tiles, pl->k_per_split);   // no empty split
-    p.splits = static_cast<int32_t>(splits);
-    const int64_t units = p.tiles * splits;
     const int64_t cap = (opt && opt->max_ctas) ? opt->max_ctas : num_sms;
-    p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
+
+    // Choose the kernel variant (single CTA with a 128-row tile, or CTA pair
+    // with a 256-row tile), the tile width and the K split by a simple time
+    // model.  Every CTA (pair) runs ceil(units / slots) work units one after
+    // the other; a unit costs (tile width x K tiles) divided by the measured
+    // relative efficiency of the variant; under a split each unit also writes
+    // an FP32 partial tile that a second kernel sums (about 24 K tiles' worth
+    // for 128 rows, less for fewer rows).  Ties go to the earlier candidate.
+    struct Cand { bool pair; int bn; int eff; };   // eff in percent
+    static const Cand kCands[] = {
+        {true, 256, 100}, {true, 128, 88}, {false, 256, 86}, {false, 192, 79},
+        {false, 224, 76}, {false, 128, 62}};
+    double best_cost = -1.0;
+    for (const Cand &cd : kCands) {
+        if (opt && opt->path == TG_PATH_TC && cd.pair) continue;
+        if (opt && opt->path == TG_PATH_TC_PAIR && !cd.pair) continue;
+        if (opt && opt->block_n && opt->block_n != cd.bn) continue;
+        if (cd.pair && cap < 2) continue;
+        const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
+        const int64_t slots = std::max<int64_t>(1, cd.pair ? cap / 2 : cap);
+        const int64_t tiles = cdiv(M, tile_m) * cdiv(N, cd.bn);
+        int64_t s_lo = 1, s_hi = 1;
+        if (opt && opt->splits) {
+            s_lo = s_hi = opt->splits;
+        } else if (tiles < slots / 2) {
+            s_hi = std::min<int64_t>(pl->k_tiles, 16);   // too few tiles: consider split K
+        }
+        for (int64_t s = s_lo; s <= s_hi; ++s) {
+            const int64_t sc = std::max<int64_t>(1, std::min<int64_t>(s, pl->k_tiles));
+            const int64_t kps = cdiv(pl->k_tiles, sc);
+            const int64_t se = cdiv(pl->k_tiles, kps);   // no empty split
+            const int64_t units = tiles * se;
+            const int64_t waves = units > 0 ? cdiv(units, std::min(units, slots)) : 0;
+            const int64_t rows = std::min<int64_t>(M, kBlockM);
+            const int64_t partial = se > 1 ? std::max<int64_t>(1, 24 * rows / kBlockM) : 0;
+            const double cost =
+                static_cast<double>(waves * cd.bn * (kps + partial)) * 100.0 / cd.eff;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                p.path = cd.pair ? TG_PATH_TC_PAIR : TG_PATH_TC;
+                p.block_m = static_cast<int32_t>(tile_m);
+                p.block_n = cd.bn;
+                pl->k_per_split = kps;
+                p.splits = static_cast<int32_t>(se);
+                p.tiles = tiles;
+            }
+        }
+    }
+    const bool pair = p.path == TG_PATH_TC_PAIR;
+    p.stages = tg::tc_stages(in_kind_of(din), p.block_n, pair);
+    pl->tiles_m = cdiv(M, p.block_m);
+    pl->tiles_n = cdiv(N, p.block_n);
+    const int64_t splits = p.splits;
+    const int64_t units = p.tiles * splits;
+    if (pair) {
+        const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(units, cap / 2));
+        p.ctas = static_cast<int32_t>(2 * pairs);
+    } else {
+        p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
+    }
     p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
     p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
     if (din == TG_F32) p.pack_b = 2;   // kind::tf32 reads B K-major: B^T into the workspace
@@ -324,8 +367,10 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     }
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
+    const bool pair = p.path == TG_PATH_TC_PAIR;
+    const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
     const tg_status sb = p.pack_b == 2
-                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, p.block_n)
+                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
                              : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k);
     if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, kBlockM) != TG_OK || sb != TG_OK)
         return fail(TG_ERR_CUDA);
@@ -348,7 +393,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
     tp.status = dev->status;
     tp.timeout_ns = pl.timeout_ns;
-    st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, tmA, tmB, tp, p.ctas, s));
+    st = cuda_status(
+        tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair, tmA, tmB, tp, p.ctas, s));
     if (st != TG_OK) return fail(st);
     if (p.splits > 1) {
         st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,

@@ -34,10 +34,10 @@ struct TcParams {
 };
 
 // gemm_tc.cu
-int tc_stages(int in_kind, int block_n);
-int tc_smem_bytes(int in_kind, int block_n);
-bool tc_supported_block_n(int block_n);
-cudaError_t launch_gemm_tc(int in_kind, int block_n, const CUtensorMap &tmA,
+// `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `ctas` counts CTAs.
+int tc_stages(int in_kind, int block_n, bool pair);
+bool tc_supported_block_n(int block_n, bool pair);
+cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);
 cudaError_t status_word_address(int **out);
