@@ -142,8 +142,11 @@ def test_plan_forced_options(lib):
     assert p["ctas"] == 10 and p["tiles"] == 4 * 8
 
 
-def test_plan_pair_width_limits(lib):
-    st, _ = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=224)
+def test_plan_width_limits(lib):
+    for bn in (128, 192, 224, 256):
+        st, p = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=bn)
+        assert st == tg.TG_OK and p["block_n"] == bn
+    st, _ = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=160)
     assert st == tg.TG_ERR_UNSUPPORTED
     st, _ = plan(512, 512, 512, path=tg.TG_PATH_SKINNY)
     assert st == tg.TG_ERR_UNSUPPORTED

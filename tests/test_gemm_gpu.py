@@ -103,7 +103,7 @@ PATHS = {"tc": 1, "pair": 2}
 
 
 @pytest.mark.parametrize("path", ["tc", "pair"])
-@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("block_n", [128, 192, 224, 256])
 @pytest.mark.parametrize("din,dout", [("f16", "f16"), ("bf16", "f32"), ("f32", "f32")])
 @pytest.mark.parametrize("M,N,K", [(100, 300, 200), (300, 520, 333), (513, 257, 1000),
                                    (1024, 1024, 64)])

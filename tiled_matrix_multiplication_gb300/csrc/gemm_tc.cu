@@ -70,7 +70,9 @@ cudaError_t status_word_address(int **out) {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kSmemBudget = 200 * 1024;
+// Dynamic shared memory for the stage ring: the 227 KB a CTA may use, less
+// the alignment slack and the barriers.
+constexpr int kSmemBudget = 232448 - 1024 - 256;
 
 template <int IN_KIND, int BN, bool PAIR>
 struct TcCfg {
@@ -105,7 +107,7 @@ struct TcCfg {
         make_idesc(IN_KIND == IN_TF32 ? 2u : (IN_KIND == IN_BF16 ? 1u : 0u), 0u,
                    B_KMAJOR ? 0u : 1u, TILE_M, BN);
     static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
-    static_assert(!PAIR || (BN_CTA % CHUNK_N == 0 || B_KMAJOR), "pair halves of whole chunks");
+    static_assert(BN_CTA % 16 == 0, "each CTA stages whole 16-column groups of B");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -515,6 +517,8 @@ cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &
     if constexpr (PAIR) {
         switch (block_n) {
         case 128: return launch_impl<IN_KIND, 128, true>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, true>(tmA, tmB, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, true>(tmA, tmB, p, ctas, stream);
         case 256: return launch_impl<IN_KIND, 256, true>(tmA, tmB, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
@@ -533,8 +537,8 @@ template <int IN_KIND, bool PAIR>
 int stages_kind(int block_n) {
     switch (block_n) {
     case 128: return TcCfg<IN_KIND, 128, PAIR>::STAGES;
-    case 192: return PAIR ? 0 : TcCfg<IN_KIND, 192, false>::STAGES;
-    case 224: return PAIR ? 0 : TcCfg<IN_KIND, 224, false>::STAGES;
+    case 192: return TcCfg<IN_KIND, 192, PAIR>::STAGES;
+    case 224: return TcCfg<IN_KIND, 224, PAIR>::STAGES;
     case 256: return TcCfg<IN_KIND, 256, PAIR>::STAGES;
     default: return 0;
     }
@@ -543,7 +547,7 @@ int stages_kind(int block_n) {
 }  // namespace
 
 bool tc_supported_block_n(int block_n, bool pair) {
-    if (pair) return block_n == 128 || block_n == 256;
+    (void)pair;
     return block_n == 128 || block_n == 192 || block_n == 224 || block_n == 256;
 }
 
