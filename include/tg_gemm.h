@@ -167,6 +167,36 @@ tg_status tg_last_device_error(void *stream);
 /* TG_ABI_VERSION of the loaded library. */
 int32_t tg_abi_version(void);
 
+/* Size of the library-owned device array used by tg_gemm_splitk_noalloc. */
+#define TG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * tg_gemm_splitk_noalloc -- C = A * B split over `splits` ranges of K, with the
+ * FP32 partial tiles kept in a fixed device array of TG_NOALLOC_SCRATCH_BYTES
+ * that the library owns, so that the call allocates no device memory.  The
+ * pages have no counterpart: this serves callers that cannot let a library
+ * allocate -- an application whose device memory is all held by its own
+ * allocator, or a code path that must not enter the allocator at all.
+ *
+ *   M, N, K, a, lda, b, ldb, c, ldc, dtype_out, stream  as for tg_gemm
+ *   dtype_in   TG_F16 or TG_BF16 (TF32 needs a transposed copy of B: unsupported)
+ *   splits     1 .. 128 K ranges; the planner may use fewer when K is short
+ *
+ * Returns TG_ERR_UNSUPPORTED when splits x M x N x 4 bytes exceeds
+ * TG_NOALLOC_SCRATCH_BYTES, when A or B is not 16-byte aligned in base and row
+ * pitch (they are read in place), or for TF32 operands; argument errors as for
+ * tg_gemm.  The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call outside
+ * any stream capture.  Every call on a device shares the one array: calls
+ * whose work may overlap on the GPU (unordered streams) race on it.
+ */
+tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K,
+                                 const void *a, int64_t lda,
+                                 const void *b, int64_t ldb,
+                                 void *c, int64_t ldc,
+                                 tg_dtype dtype_in, tg_dtype dtype_out,
+                                 int32_t splits, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,14 +17,16 @@ from __future__ import annotations
 from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_ERR_ARCH, TG_ERR_CUDA,
                    TG_ERR_INVALID_VALUE, TG_ERR_NOT_IMPLEMENTED, TG_ERR_OUT_OF_MEMORY,
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
-                   TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, TgError, load, make_options,
-                   status_name, tg_abi_version, tg_gemm, tg_gemm_ex, tg_last_device_error,
-                   tg_options, tg_plan, tg_plan_gemm, tg_status_string)
+                   TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, NOALLOC_SCRATCH_BYTES, TgError,
+                   load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
+                   tg_gemm_splitk_noalloc, tg_last_device_error, tg_options, tg_plan,
+                   tg_plan_gemm, tg_status_string)
 
 __all__ = [
     "gemm", "plan", "check_device_error", "dtype_code", "TgError", "load", "make_options",
     "tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string", "tg_last_device_error",
-    "tg_abi_version", "tg_options", "tg_plan", "EXPORTS", "LIB_PATH",
+    "tg_abi_version", "tg_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
+    "EXPORTS", "LIB_PATH",
     "TG_F16", "TG_BF16", "TG_F32", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
     "TG_ERR_OUT_OF_MEMORY", "TG_ERR_CUDA", "TG_ERR_ARCH", "TG_ERR_TIMEOUT",
     "TG_ERR_NOT_IMPLEMENTED", "TG_PATH_AUTO", "TG_PATH_TC", "TG_PATH_TC_PAIR", "TG_PATH_SKINNY",

@@ -29,7 +29,10 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 
 # Every extern "C" symbol the header declares.
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
-           "tg_last_device_error", "tg_abi_version")
+           "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc")
+
+# Bytes of the library-owned partial-tile array of tg_gemm_splitk_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class tg_options(ctypes.Structure):
@@ -90,6 +93,8 @@ def load(path: str | None = None):
         lib.tg_last_device_error.restype = ctypes.c_int
         lib.tg_abi_version.argtypes = []
         lib.tg_abi_version.restype = i32
+        lib.tg_gemm_splitk_noalloc.argtypes = gemm_args[:-1] + [i32, vp]
+        lib.tg_gemm_splitk_noalloc.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -144,3 +149,13 @@ def tg_plan_gemm(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, 
 
 def tg_last_device_error(stream) -> int:
     return int(load().tg_last_device_error(stream))
+
+
+def tg_gemm_splitk_noalloc(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, splits,
+                           stream) -> int:
+    """Split-K GEMM whose partial tiles live in the library's fixed device array
+    (NOALLOC_SCRATCH_BYTES): for callers that must not have the library
+    allocate device memory.  Returns the tg_status (TG_ERR_UNSUPPORTED when
+    splits * M * N * 4 exceeds the array, for misaligned operands or TF32)."""
+    return int(load().tg_gemm_splitk_noalloc(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                                             _code(dtype_out), splits, stream))
