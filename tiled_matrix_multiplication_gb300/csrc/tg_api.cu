@@ -138,7 +138,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
 
     // Choose the kernel variant (single CTA with a 128-row tile, or CTA pair
     // with a 256-row tile), the tile width and the K split by a simple time
-    // model.  Every CTA (pair) runs ceil(units / slots) work units one after
+    // model.  Every CTA (pair) runs about units / slots work units one after
     // the other; a unit costs (tile width x K tiles) divided by the measured
     // relative efficiency of the variant; under a split each unit also writes
     // an FP32 partial tile that a second kernel sums (about 24 K tiles' worth
@@ -169,11 +169,15 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             const int64_t kps = cdiv(pl->k_tiles, sc);
             const int64_t se = cdiv(pl->k_tiles, kps);   // no empty split
             const int64_t units = tiles * se;
-            const int64_t waves = units > 0 ? cdiv(units, std::min(units, slots)) : 0;
+            // Fractional waves, with the idle part of a partial last wave charged
+            // at a quarter: fewer busy CTAs run faster (less contention for L2
+            // bandwidth and power), so an idle slot costs less than a busy one.
+            const double used = static_cast<double>(units) / static_cast<double>(std::max<int64_t>(1, std::min(units, slots)));
+            const double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
             const int64_t rows = std::min<int64_t>(M, kBlockM);
             const int64_t partial = se > 1 ? std::max<int64_t>(1, 24 * rows / kBlockM) : 0;
             const double cost =
-                static_cast<double>(waves * cd.bn * (kps + partial)) * 100.0 / cd.eff;
+                waves * static_cast<double>(cd.bn * (kps + partial)) * 100.0 / cd.eff;
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 p.path = cd.pair ? TG_PATH_TC_PAIR : TG_PATH_TC;
