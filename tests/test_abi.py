@@ -122,13 +122,14 @@ def test_plan_tf32(lib):
 def test_plan_skinny_splits_k(lib, M):
     st, p = plan(M, 8192, 8192, sms=148)
     assert st == tg.TG_OK
-    assert p["splits"] > 1
+    assert p["path"] == tg.TG_PATH_SKINNY and p["block_n"] == 128
+    assert p["block_m"] == {1: 16, 16: 16, 64: 64, 128: 128}[M]
+    assert p["tiles"] == 64 and p["splits"] > 1
     units = p["tiles"] * p["splits"]
-    assert units >= 148 // 2
+    assert units >= 148
     k_tiles = 8192 // p["block_k"]
     assert (p["splits"] - 1) * -(-k_tiles // p["splits"]) < k_tiles   # no empty split
     assert p["workspace_bytes"] >= p["splits"] * M * 8192 * 4
-    assert p["kernels"] == 2
 
 
 def test_plan_forced_options(lib):
@@ -157,7 +158,11 @@ def test_plan_prefers_pairs_for_large_and_single_ctas_for_skinny(lib):
         st, p = plan(M, N, K, "bf16", sms=148)
         assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR
     st, p = plan(16, 8192, 8192, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_SKINNY
+    st, p = plan(16, 8192, 8192, "f32", sms=148)          # TF32: no small-M kernel
     assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC
+    st, _ = plan(129, 512, 512, path=tg.TG_PATH_SKINNY)
+    assert st == tg.TG_ERR_UNSUPPORTED
 
 
 def test_plan_zero_sizes(lib):

@@ -122,3 +122,23 @@ def test_pair_split_and_grid(splits, max_ctas):
                        max_ctas=max_ctas, ldc=N + 8)
     compare(a, b, c, M, N, K, "bf16", "bf16")
     assert padding_untouched(c, N, "bf16")
+
+
+@pytest.mark.parametrize("din,dout", [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 64, 100, 128])
+@pytest.mark.parametrize("N,K,splits", [(1000, 777, 1), (128, 64, 1), (1, 300, 1), (520, 2000, 3),
+                                        (4096, 1024, 0)])
+def test_skinny_path_exact(din, dout, M, N, K, splits):
+    """The small-M kernel (C^T = B^T A^T) for every row-count bucket, ragged N and K,
+    with and without a K split."""
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=3, splits=splits)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+
+
+@pytest.mark.parametrize("M", [1, 16, 128])
+def test_skinny_path_strided_uniform(M):
+    N, K = 700, 900
+    a, b, c = run_gemm(M, N, K, "bf16", "bf16", dist="uniform", path=3, lda=K + 8, ldb=N + 36,
+                       ldc=N + 8, splits=2)
+    compare(a, b, c, M, N, K, "bf16", "bf16")
+    assert padding_untouched(c, N, "bf16")

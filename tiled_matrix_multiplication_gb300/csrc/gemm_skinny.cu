@@ -1,0 +1,335 @@
+// gemm_skinny.cu -- tcgen05 GEMM for small M (decode-like shapes), HBM-bound.
+//
+// "Fast matrix multiplication" (ch. 12), section "Decode is a different
+// problem: GEMV": with a handful of rows there is almost nothing to reuse, so
+// the kernel's job is to stream B -- the large operand -- at full bandwidth,
+// with coalesced wide reads and enough parallelism.
+//
+// The product is computed transposed, C^T = B^T A^T, so that the MMA's
+// 128-row dimension runs over 128 output COLUMNS n and its N dimension over
+// the few output rows m (M rounded up to MP = 16, 32, 64 or 128):
+//   * MMA operand A = a B^T tile [128 n x 64 k], read N-major straight from
+//     row-major B (two 64-column TMA boxes per stage);
+//   * MMA operand B = an A^T tile [64 k x MP m], read K-major from row-major A
+//     (one TMA box of MP rows);
+//   * the FP32 accumulator is 128 TMEM lanes (n) x MP columns (m).
+// Almost all of each shared-memory stage is B, so the ring holds 7-12 stages
+// of the streamed operand; the epilogue writes a row of C as 32 consecutive
+// n per warp (coalesced).  When there are too few column tiles to occupy the
+// GPU, K is split across work units whose FP32 partials the split-K reduce
+// kernel sums in a fixed order.
+//
+// Roles, barriers, bounded waits and the drain on failure are those of the
+// single-CTA tensor-core kernel (gemm_tc.cu).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tg_internal.h"
+#include "tg_kernel_common.cuh"
+#include "tg_ptx.cuh"
+
+namespace tg {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSmemBudget = 232448 - 1024 - 256;
+constexpr int kTileN = 128;   // output columns per work tile (the MMA's M)
+
+template <int IN_KIND, int MP>
+struct SkCfg {
+    static constexpr int BK = 64;                 // 128 bytes of K per row
+    static constexpr int UMMA_K = 16;
+    static constexpr int CHUNK_N = 64;            // n per 128-byte B row
+    static constexpr int BT_BOX = BK * 128;       // one 64-column box: 8 KB
+    static constexpr int BT_STAGE = 2 * BT_BOX;   // 128 columns of B
+    static constexpr int AT_STAGE = MP * 128;     // MP rows of A
+    static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
+    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 12 ? 12 : kSmemBudget / STAGE_BYTES;
+    static constexpr int ACC_COLS = MP < 32 ? 32 : MP;
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+    // A operand (B^T) N-major, B operand (A^T) K-major; M = 128, N = MP.
+    static constexpr uint32_t IDESC =
+        make_idesc(IN_KIND == IN_BF16 ? 1u : 0u, 1u, 0u, kTileN, MP);
+    static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte swizzle alignment");
+    static_assert(MP % 16 == 0 && MP >= 16 && MP <= 128, "MMA N");
+};
+
+struct SkWork {
+    int tn, split, kt0, kt1;
+};
+
+__device__ __forceinline__ SkWork sk_decode(const SkParams &p, int w) {
+    SkWork r;
+    r.tn = w / p.splits;
+    r.split = w - r.tn * p.splits;
+    r.kt0 = r.split * p.k_tiles_per_split;
+    r.kt1 = min(r.kt0 + p.k_tiles_per_split, p.k_tiles);
+    return r;
+}
+
+__device__ __forceinline__ void sk_store(const SkParams &p, int split, int m, int n, float v) {
+    if (p.splits > 1) {
+        p.partial[(static_cast<int64_t>(split) * p.M + m) * p.N + n] = v;
+        return;
+    }
+    const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+    if (p.out_kind == OUT_F32)
+        static_cast<float *>(p.c)[off] = v;
+    else if (p.out_kind == OUT_F16)
+        static_cast<__half *>(p.c)[off] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(p.c)[off] = __float2bfloat16_rn(v);
+}
+
+template <int IN_KIND, int MP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const SkParams p) {
+    using Cfg = SkCfg<IN_KIND, MP>;
+    constexpr int S = Cfg::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sBt = base;                           // S x BT_STAGE
+    const uint32_t sAt = base + S * Cfg::BT_STAGE;       // S x AT_STAGE
+    const uint32_t bars = sAt + S * Cfg::AT_STAGE;
+    uint8_t *gbars = gbase + (bars - base);
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = p.tiles_n * p.splits;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const SkWork wk = sk_decode(p, w);
+                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    const uint32_t fb = full_bar(stage);
+                    tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
+                    tma_load_2d(sBt + stage * Cfg::BT_STAGE, &tmB, fb, wk.tn * kTileN, kt * Cfg::BK);
+                    tma_load_2d(sBt + stage * Cfg::BT_STAGE + Cfg::BT_BOX, &tmB, fb,
+                                wk.tn * kTileN + Cfg::CHUNK_N, kt * Cfg::BK);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                record_failure(p.status, 6, (ROLE_PRODUCER << 16) | stage);
+                *abort_flag = 1;
+            }
+            const int64_t first = issued > S ? issued - S : 0;
+            for (int64_t i = first; i < issued; ++i) {
+                if (!mbar_wait(full_bar(static_cast<int>(i % S)),
+                               static_cast<uint32_t>((i / S) & 1), p.timeout_ns, &never_abort)) {
+                    record_failure(p.status, 6, (ROLE_DRAIN << 16) | 1);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_count = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const SkWork wk = sk_decode(p, w);
+                const uint32_t buf = acc_count & 1u;
+                const uint32_t acc_phase = (acc_count >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
+                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
+                    if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t bt0 = sBt + stage * Cfg::BT_STAGE;
+                    const uint32_t at0 = sAt + stage * Cfg::AT_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
+                        const uint64_t ad =
+                            smem_desc_sw128(bt0 + kk * Cfg::UMMA_K * 128, Cfg::BT_BOX, 1024);
+                        const uint64_t bd = smem_desc_sw128(at0 + kk * 32, 16, 1024);
+                        umma_ss<0, 1>(d_tmem, ad, bd, Cfg::IDESC, (kt > wk.kt0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(buf));
+                ++acc_count;
+            }
+            if (!ok) {
+                record_failure(p.status, 6, (ROLE_MMA << 16) | stage);
+                *abort_flag = 1;
+            }
+            umma_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, p.timeout_ns, &never_abort))
+                record_failure(p.status, 6, (ROLE_DRAIN << 16) | 2);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- epilogue
+        // Thread (quad, lane) owns output column n; the TMEM columns are m.
+        const int quad = warp & 3;
+        uint32_t acc_count = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const SkWork wk = sk_decode(p, w);
+            const uint32_t buf = acc_count & 1u;
+            const uint32_t acc_phase = (acc_count >> 1) & 1u;
+            const bool got = mbar_wait(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const int n = wk.tn * kTileN + quad * 32 + lane;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_COLS;
+            if constexpr (MP == 16) {
+                uint32_t r[16];
+                tmem_load_16cols_sync(taddr, r);
+                if (n < p.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < p.M) sk_store(p, wk.split, j, n, __uint_as_float(r[j]));
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < MP; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_load_32cols_sync(taddr + c0, r);
+                    if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < p.M) sk_store(p, wk.split, c0 + j, n, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            ++acc_count;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int IN_KIND, int MP>
+cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p, int ctas,
+                      cudaStream_t stream) {
+    using Cfg = SkCfg<IN_KIND, MP>;
+    auto kern = gemm_skinny_kernel<IN_KIND, MP>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<ctas, kThreads, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+template <int IN_KIND>
+cudaError_t sk_launch_kind(int mp, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                           const SkParams &p, int ctas, cudaStream_t stream) {
+    switch (mp) {
+    case 16: return sk_launch<IN_KIND, 16>(tmA, tmB, p, ctas, stream);
+    case 32: return sk_launch<IN_KIND, 32>(tmA, tmB, p, ctas, stream);
+    case 64: return sk_launch<IN_KIND, 64>(tmA, tmB, p, ctas, stream);
+    case 128: return sk_launch<IN_KIND, 128>(tmA, tmB, p, ctas, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
+
+int skinny_stages(int mp) {
+    switch (mp) {
+    case 16: return SkCfg<IN_F16, 16>::STAGES;
+    case 32: return SkCfg<IN_F16, 32>::STAGES;
+    case 64: return SkCfg<IN_F16, 64>::STAGES;
+    case 128: return SkCfg<IN_F16, 128>::STAGES;
+    default: return 0;
+    }
+}
+
+cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
+                               const CUtensorMap &tmB, const SkParams &p, int ctas,
+                               cudaStream_t stream) {
+    switch (in_kind) {
+    case IN_F16: return sk_launch_kind<IN_F16>(mp, tmA, tmB, p, ctas, stream);
+    case IN_BF16: return sk_launch_kind<IN_BF16>(mp, tmA, tmB, p, ctas, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tg

@@ -95,8 +95,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
         if (opt->splits < 0 || opt->block_n < 0 || opt->group_m < 0 || opt->max_ctas < 0 ||
             opt->timeout_ms < 0)
             return TG_ERR_INVALID_VALUE;
-        if (opt->path == TG_PATH_SKINNY) return TG_ERR_UNSUPPORTED;
-        if (opt->block_n) {
+        if (opt->path == TG_PATH_SKINNY) {
+            // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128
+            if (din == TG_F32 || M > 128 || opt->block_n) return TG_ERR_UNSUPPORTED;
+        }
+        if (opt->block_n && opt->path != TG_PATH_SKINNY) {
             const bool one = tg::tc_supported_block_n(opt->block_n, false);
             const bool two = tg::tc_supported_block_n(opt->block_n, true);
             if ((opt->path == TG_PATH_TC && !one) || (opt->path == TG_PATH_TC_PAIR && !two) ||
@@ -189,8 +192,43 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             }
         }
     }
+    // Small M with 16-bit operands: the transposed streaming kernel (one tile
+    // holds all rows; work is spread over 128-column tiles and K splits).
+    const bool skinny_ok = din != TG_F32 && M <= 128 && !(opt && opt->block_n) &&
+                           !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR));
+    if (skinny_ok) {
+        const int64_t ktiles = std::max<int64_t>(cdiv(K, 64), 1);
+        const int64_t tiles = cdiv(N, 128);
+        int64_t s_lo = 1, s_hi = std::min<int64_t>(ktiles, 32);
+        if (opt && opt->splits) s_lo = s_hi = opt->splits;
+        double best = -1.0;
+        for (int64_t s = s_lo; s <= s_hi; ++s) {
+            const int64_t sc = std::max<int64_t>(1, std::min<int64_t>(s, ktiles));
+            const int64_t kps = cdiv(ktiles, sc);
+            const int64_t se = cdiv(ktiles, kps);
+            const int64_t units = tiles * se;
+            const int64_t slots = std::max<int64_t>(1, std::min(units, cap));
+            const double used = static_cast<double>(units) / static_cast<double>(slots);
+            const double waves = used + 0.25 * (static_cast<double>(cdiv(units, slots)) - used);
+            // bytes of B streamed per unit, plus the FP32 partial it writes and
+            // the reduction reads back
+            const double cost = waves * (16384.0 * kps + (se > 1 ? 1024.0 * M : 0.0));
+            if (best < 0 || cost < best) {
+                best = cost;
+                pl->k_per_split = kps;
+                p.splits = static_cast<int32_t>(se);
+                p.tiles = tiles;
+            }
+        }
+        p.path = TG_PATH_SKINNY;
+        p.block_m = tg::skinny_rows(M);
+        p.block_n = 128;
+        p.block_k = 64;
+        pl->k_tiles = ktiles;
+    }
     const bool pair = p.path == TG_PATH_TC_PAIR;
-    p.stages = tg::tc_stages(in_kind_of(din), p.block_n, pair);
+    p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m)
+                                         : tg::tc_stages(in_kind_of(din), p.block_n, pair);
     pl->tiles_m = cdiv(M, p.block_m);
     pl->tiles_n = cdiv(N, p.block_n);
     const int64_t splits = p.splits;
@@ -373,6 +411,36 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     }
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
+    if (p.path == TG_PATH_SKINNY) {
+        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, p.block_m) != TG_OK ||
+            encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k) != TG_OK)
+            return fail(TG_ERR_CUDA);
+        tg::SkParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.M = static_cast<int32_t>(M);
+        sp.N = static_cast<int32_t>(N);
+        sp.K = static_cast<int32_t>(K);
+        sp.tiles_n = static_cast<int32_t>(p.tiles);
+        sp.k_tiles = static_cast<int32_t>(pl.k_tiles);
+        sp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
+        sp.splits = p.splits;
+        sp.out_kind = out_kind_of(dtype_out);
+        sp.ldc = ldc;
+        sp.c = c;
+        sp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
+        sp.status = dev->status;
+        sp.timeout_ns = pl.timeout_ns;
+        st = cuda_status(
+            tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, tmA, tmB, sp, p.ctas, s));
+        if (st != TG_OK) return fail(st);
+        if (p.splits > 1) {
+            st = cuda_status(tg::launch_splitk_reduce(sp.partial, p.splits, M, N, c, ldc,
+                                                      sp.out_kind, p.c_vector, s));
+            if (st != TG_OK) return fail(st);
+        }
+        if (ws && cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
+        return TG_OK;
+    }
     const bool pair = p.path == TG_PATH_TC_PAIR;
     const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
     const tg_status sb = p.pack_b == 2

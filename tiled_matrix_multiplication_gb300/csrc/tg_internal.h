@@ -33,6 +33,29 @@ struct TcParams {
     uint64_t timeout_ns;
 };
 
+// Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with 128
+// output columns per work tile and all M <= 128 rows in one tile.
+struct SkParams {
+    int32_t M, N, K;
+    int32_t tiles_n;            // ceil(N / 128)
+    int32_t k_tiles;            // ceil(K / 64)
+    int32_t k_tiles_per_split;
+    int32_t splits;
+    int32_t out_kind;
+    int64_t ldc;
+    void *c;
+    float *partial;             // [splits][M][N] when splits > 1
+    int *status;
+    uint64_t timeout_ns;
+};
+
+// gemm_skinny.cu
+int skinny_rows(int64_t M);      // MMA N used for M rows: 16, 32, 64 or 128
+int skinny_stages(int mp);
+cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
+                               const CUtensorMap &tmB, const SkParams &p, int ctas,
+                               cudaStream_t stream);
+
 // gemm_tc.cu
 // `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `ctas` counts CTAs.
 int tc_stages(int in_kind, int block_n, bool pair);
