@@ -124,12 +124,22 @@ def test_plan_skinny_splits_k(lib, M):
     assert st == tg.TG_OK
     assert p["path"] == tg.TG_PATH_SKINNY and p["block_n"] == 128
     assert p["block_m"] == {1: 16, 16: 16, 64: 64, 128: 128}[M]
-    assert p["tiles"] == 64 and p["splits"] > 1
-    units = p["tiles"] * p["splits"]
-    assert units >= 148
-    k_tiles = 8192 // p["block_k"]
-    assert (p["splits"] - 1) * -(-k_tiles // p["splits"]) < k_tiles   # no empty split
-    assert p["workspace_bytes"] >= p["splits"] * M * 8192 * 4
+    assert p["tiles"] == 64 and p["splits"] in (2, 4, 8)
+    assert p["ctas"] == p["tiles"] * p["splits"] <= 148    # one resident CTA per unit
+    assert p["ctas"] * 2 > 148                               # the largest cluster that fits
+    assert p["workspace_bytes"] == 0 and p["kernels"] == 1  # partials summed on chip
+
+
+def test_plan_skinny_cluster_limits(lib):
+    st, p = plan(16, 4096, 4096, path=tg.TG_PATH_SKINNY, splits=8)
+    assert st == tg.TG_OK and p["splits"] == 8
+    for s in (3, 5, 16):
+        st, _ = plan(16, 4096, 4096, path=tg.TG_PATH_SKINNY, splits=s)
+        assert st == tg.TG_ERR_UNSUPPORTED
+    st, _ = plan(16, 4096, 64, path=tg.TG_PATH_SKINNY, splits=2)   # one K tile: empty range
+    assert st == tg.TG_ERR_UNSUPPORTED
+    st, p = plan(16, 4096, 64, sms=148)                           # planner keeps 1 range
+    assert st == tg.TG_OK and p["splits"] == 1
 
 
 def test_plan_forced_options(lib):

@@ -126,11 +126,11 @@ def test_pair_split_and_grid(splits, max_ctas):
 
 @pytest.mark.parametrize("din,dout", [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 64, 100, 128])
-@pytest.mark.parametrize("N,K,splits", [(1000, 777, 1), (128, 64, 1), (1, 300, 1), (520, 2000, 3),
-                                        (4096, 1024, 0)])
+@pytest.mark.parametrize("N,K,splits", [(1000, 777, 1), (128, 64, 1), (1, 300, 2), (520, 2000, 4),
+                                        (4096, 1024, 0), (300, 4100, 8)])
 def test_skinny_path_exact(din, dout, M, N, K, splits):
     """The small-M kernel (C^T = B^T A^T) for every row-count bucket, ragged N and K,
-    with and without a K split."""
+    without a K split and with K split over clusters of 2, 4 and 8 CTAs."""
     a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=3, splits=splits)
     compare(a, b, c, M, N, K, din, dout, exact=True)
 

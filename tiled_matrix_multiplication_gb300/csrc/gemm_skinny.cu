@@ -14,13 +14,21 @@
 //     (one TMA box of MP rows);
 //   * the FP32 accumulator is 128 TMEM lanes (n) x MP columns (m).
 // Almost all of each shared-memory stage is B, so the ring holds 7-12 stages
-// of the streamed operand; the epilogue writes a row of C as 32 consecutive
-// n per warp (coalesced).  When there are too few column tiles to occupy the
-// GPU, K is split across work units whose FP32 partials the split-K reduce
-// kernel sums in a fixed order.
+// of the streamed operand.
 //
-// Roles, barriers, bounded waits and the drain on failure are those of the
-// single-CTA tensor-core kernel (gemm_tc.cu).
+// Work split: one CTA per (128-column tile, K range).  The S CTAs that share a
+// column tile form a thread-block cluster (S = 1, 2, 4 or 8, cluster rank =
+// K range).  After its main loop each CTA parks its FP32 partial tile in its
+// own shared memory; after a cluster barrier, CTA r sums columns
+// [r*128/S, (r+1)*128/S) of the tile over all S partials, read in rank order
+// from the peers' shared memory (distributed shared memory), rounds once and
+// writes C.  No partials go to global memory and no second kernel runs; the
+// sum order is fixed, so results do not depend on timing.
+//
+// Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2..5 = TMEM -> shared epilogue; all six warps then do the cluster
+// reduction.  Every mbarrier wait is bounded (status word + abort flag, as in
+// gemm_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -33,7 +41,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSmemBudget = 232448 - 1024 - 256;
-constexpr int kTileN = 128;   // output columns per work tile (the MMA's M)
+constexpr int kTileN = 128;   // output columns per tile (the MMA's M)
 
 template <int IN_KIND, int MP>
 struct SkCfg {
@@ -45,35 +53,19 @@ struct SkCfg {
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
     static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 12 ? 12 : kSmemBudget / STAGE_BYTES;
-    static constexpr int ACC_COLS = MP < 32 ? 32 : MP;
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int PARTIAL_BYTES = kTileN * MP * 4;   // FP32 partial tile, [m][n]
+    static constexpr int TMEM_COLS = MP < 32 ? 32 : MP;
+    static constexpr int NUM_BARS = 2 * STAGES + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     // A operand (B^T) N-major, B operand (A^T) K-major; M = 128, N = MP.
     static constexpr uint32_t IDESC =
         make_idesc(IN_KIND == IN_BF16 ? 1u : 0u, 1u, 0u, kTileN, MP);
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte swizzle alignment");
+    static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "partial tile reuses the ring");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 128, "MMA N");
 };
 
-struct SkWork {
-    int tn, split, kt0, kt1;
-};
-
-__device__ __forceinline__ SkWork sk_decode(const SkParams &p, int w) {
-    SkWork r;
-    r.tn = w / p.splits;
-    r.split = w - r.tn * p.splits;
-    r.kt0 = r.split * p.k_tiles_per_split;
-    r.kt1 = min(r.kt0 + p.k_tiles_per_split, p.k_tiles);
-    return r;
-}
-
-__device__ __forceinline__ void sk_store(const SkParams &p, int split, int m, int n, float v) {
-    if (p.splits > 1) {
-        p.partial[(static_cast<int64_t>(split) * p.M + m) * p.N + n] = v;
-        return;
-    }
+__device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float v) {
     const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
     if (p.out_kind == OUT_F32)
         static_cast<float *>(p.c)[off] = v;
@@ -100,26 +92,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gbars = gbase + (bars - base);
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
-    auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
-    auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
-    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    const uint32_t tfull_bar = bars + 8u * (2 * S);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *partial = reinterpret_cast<float *>(gbase);  // after the main loop: [MP][128]
     __shared__ int never_abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int splits = static_cast<int>(cluster_num_ctas());   // == p.splits
+    const int split = static_cast<int>(cluster_cta_rank());
+    const int tn = static_cast<int>(blockIdx.x) / splits;
+    const int kt0 = split * p.k_tiles_per_split;
+    const int kt1 = min(kt0 + p.k_tiles_per_split, p.k_tiles);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);
-        }
-        mbar_init(drain_bar, 1);
+        mbar_init(tfull_bar, 1);
         *abort_flag = 0;
         never_abort = 0;
         fence_mbar_init();
@@ -136,7 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = p.tiles_n * p.splits;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -145,24 +136,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                const SkWork wk = sk_decode(p, w);
-                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
-                    const uint32_t fb = full_bar(stage);
-                    tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
-                    tma_load_2d(sBt + stage * Cfg::BT_STAGE, &tmB, fb, wk.tn * kTileN, kt * Cfg::BK);
-                    tma_load_2d(sBt + stage * Cfg::BT_STAGE + Cfg::BT_BOX, &tmB, fb,
-                                wk.tn * kTileN + Cfg::CHUNK_N, kt * Cfg::BK);
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            for (int kt = kt0; kt < kt1; ++kt) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                const uint32_t fb = full_bar(stage);
+                tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
+                tma_load_2d(sBt + stage * Cfg::BT_STAGE, &tmB, fb, tn * kTileN, kt * Cfg::BK);
+                tma_load_2d(sBt + stage * Cfg::BT_STAGE + Cfg::BT_BOX, &tmB, fb,
+                            tn * kTileN + Cfg::CHUNK_N, kt * Cfg::BK);
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             if (!ok) {
@@ -184,100 +172,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t acc_count = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                const SkWork wk = sk_decode(p, w);
-                const uint32_t buf = acc_count & 1u;
-                const uint32_t acc_phase = (acc_count >> 1) & 1u;
-                if (!mbar_wait(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+            for (int kt = kt0; kt < kt1; ++kt) {
+                if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
-                for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
-                    if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t bt0 = sBt + stage * Cfg::BT_STAGE;
-                    const uint32_t at0 = sAt + stage * Cfg::AT_STAGE;
+                const uint32_t bt0 = sBt + stage * Cfg::BT_STAGE;
+                const uint32_t at0 = sAt + stage * Cfg::AT_STAGE;
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
-                        const uint64_t ad =
-                            smem_desc_sw128(bt0 + kk * Cfg::UMMA_K * 128, Cfg::BT_BOX, 1024);
-                        const uint64_t bd = smem_desc_sw128(at0 + kk * 32, 16, 1024);
-                        umma_ss<0, 1>(d_tmem, ad, bd, Cfg::IDESC, (kt > wk.kt0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(empty_bar(stage));
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
+                    const uint64_t ad =
+                        smem_desc_sw128(bt0 + kk * Cfg::UMMA_K * 128, Cfg::BT_BOX, 1024);
+                    const uint64_t bd = smem_desc_sw128(at0 + kk * 32, 16, 1024);
+                    umma_ss<0, 1>(tmem_base, ad, bd, Cfg::IDESC, (kt > kt0 || kk > 0) ? 1u : 0u);
                 }
-                if (!ok) break;
-                umma_commit(tfull_bar(buf));
-                ++acc_count;
+                umma_commit(empty_bar(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
             if (!ok) {
                 record_failure(p.status, 6, (ROLE_MMA << 16) | stage);
                 *abort_flag = 1;
             }
-            umma_commit(drain_bar);
-            if (!mbar_wait(drain_bar, 0, p.timeout_ns, &never_abort))
+            // Accumulator complete; waiting for it also drains every issued MMA
+            // before tensor memory is released.
+            umma_commit(tfull_bar);
+            if (!mbar_wait(tfull_bar, 0, p.timeout_ns, &never_abort))
                 record_failure(p.status, 6, (ROLE_DRAIN << 16) | 2);
         }
         __syncwarp();
     } else {
-        // --------------------------------------------------------- epilogue
-        // Thread (quad, lane) owns output column n; the TMEM columns are m.
+        // ---------------------------------------------- epilogue: TMEM -> smem
+        // Thread (quad, lane) owns column n = quad*32 + lane of the tile.
         const int quad = warp & 3;
-        uint32_t acc_count = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const SkWork wk = sk_decode(p, w);
-            const uint32_t buf = acc_count & 1u;
-            const uint32_t acc_phase = (acc_count >> 1) & 1u;
-            const bool got = mbar_wait(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
-                *abort_flag = 1;
-                break;
-            }
+        const bool got = mbar_wait(tfull_bar, 0, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
+            *abort_flag = 1;
+        } else {
             tc_fence_after_sync();
-            const int n = wk.tn * kTileN + quad * 32 + lane;
-            const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_COLS;
-            if constexpr (MP == 16) {
-                uint32_t r[16];
-                tmem_load_16cols_sync(taddr, r);
-                if (n < p.N) {
+            const int nl = quad * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+            if (splits == 1) {
+                const int n = tn * kTileN + nl;
+                if constexpr (MP == 16) {
+                    uint32_t r[16];
+                    tmem_load_16cols_sync(taddr, r);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (j < p.M) sk_store(p, wk.split, j, n, __uint_as_float(r[j]));
-                }
-            } else {
+                        if (j < p.M && n < p.N) sk_store(p, j, n, __uint_as_float(r[j]));
+                } else {
 #pragma unroll 1
-                for (int c0 = 0; c0 < MP; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_load_32cols_sync(taddr + c0, r);
-                    if (n < p.N) {
+                    for (int c0 = 0; c0 < MP; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_load_32cols_sync(taddr + c0, r);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (c0 + j < p.M) sk_store(p, wk.split, c0 + j, n, __uint_as_float(r[j]));
+                            if (c0 + j < p.M && n < p.N) sk_store(p, c0 + j, n, __uint_as_float(r[j]));
+                    }
+                }
+            } else {
+                // The ring is idle: every stage was consumed before tfull.
+                if constexpr (MP == 16) {
+                    uint32_t r[16];
+                    tmem_load_16cols_sync(taddr, r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) partial[j * kTileN + nl] = __uint_as_float(r[j]);
+                } else {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < MP; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_load_32cols_sync(taddr + c0, r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            partial[(c0 + j) * kTileN + nl] = __uint_as_float(r[j]);
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
-            ++acc_count;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if (splits > 1) {
+        // --------------------------- cluster reduction over distributed smem
+        cluster_sync_all();                       // every CTA's partial is in place
+        const int cols = kTileN / splits;         // columns reduced by this CTA
+        const int rows = min(p.M, MP);
+        const uint32_t part_addr = smem_addr(partial);
+        for (int i = threadIdx.x; i < rows * cols; i += kThreads) {
+            const int m = i / cols;
+            const int nl = split * cols + (i - m * cols);
+            const int n = tn * kTileN + nl;
+            const uint32_t off = part_addr + static_cast<uint32_t>((m * kTileN + nl) * 4);
+            float acc = 0.f;
+            for (int s = 0; s < splits; ++s) acc += ld_shared_cluster_f32(map_to_cta(off, s));
+            if (n < p.N) sk_store(p, m, n, acc);
+        }
+        cluster_sync_all();                       // peers are done reading this CTA's smem
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
@@ -285,25 +282,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int IN_KIND, int MP>
-cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p, int ctas,
+cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p,
                       cudaStream_t stream) {
     using Cfg = SkCfg<IN_KIND, MP>;
     auto kern = gemm_skinny_kernel<IN_KIND, MP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<ctas, kThreads, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int IN_KIND>
 cudaError_t sk_launch_kind(int mp, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                           const SkParams &p, int ctas, cudaStream_t stream) {
+                           const SkParams &p, cudaStream_t stream) {
     switch (mp) {
-    case 16: return sk_launch<IN_KIND, 16>(tmA, tmB, p, ctas, stream);
-    case 32: return sk_launch<IN_KIND, 32>(tmA, tmB, p, ctas, stream);
-    case 64: return sk_launch<IN_KIND, 64>(tmA, tmB, p, ctas, stream);
-    case 128: return sk_launch<IN_KIND, 128>(tmA, tmB, p, ctas, stream);
+    case 16: return sk_launch<IN_KIND, 16>(tmA, tmB, p, stream);
+    case 32: return sk_launch<IN_KIND, 32>(tmA, tmB, p, stream);
+    case 64: return sk_launch<IN_KIND, 64>(tmA, tmB, p, stream);
+    case 128: return sk_launch<IN_KIND, 128>(tmA, tmB, p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -323,11 +333,12 @@ int skinny_stages(int mp) {
 }
 
 cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
-                               const CUtensorMap &tmB, const SkParams &p, int ctas,
-                               cudaStream_t stream) {
+                               const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream) {
+    if (p.splits != 1 && p.splits != 2 && p.splits != 4 && p.splits != 8)
+        return cudaErrorInvalidValue;
     switch (in_kind) {
-    case IN_F16: return sk_launch_kind<IN_F16>(mp, tmA, tmB, p, ctas, stream);
-    case IN_BF16: return sk_launch_kind<IN_BF16>(mp, tmA, tmB, p, ctas, stream);
+    case IN_F16: return sk_launch_kind<IN_F16>(mp, tmA, tmB, p, stream);
+    case IN_BF16: return sk_launch_kind<IN_BF16>(mp, tmA, tmB, p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

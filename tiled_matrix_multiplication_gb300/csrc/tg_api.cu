@@ -96,8 +96,13 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             opt->timeout_ms < 0)
             return TG_ERR_INVALID_VALUE;
         if (opt->path == TG_PATH_SKINNY) {
-            // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128
+            // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128,
+            // K split over a cluster of 1, 2, 4 or 8 CTAs (none of them empty)
             if (din == TG_F32 || M > 128 || opt->block_n) return TG_ERR_UNSUPPORTED;
+            const int64_t s = opt->splits;
+            if (s != 0 && s != 1 && s != 2 && s != 4 && s != 8) return TG_ERR_UNSUPPORTED;
+            const int64_t kt = std::max<int64_t>(cdiv(K, 64), 1);
+            if (s > 1 && (s - 1) * cdiv(kt, s) >= kt) return TG_ERR_UNSUPPORTED;
         }
         if (opt->block_n && opt->path != TG_PATH_SKINNY) {
             const bool one = tg::tc_supported_block_n(opt->block_n, false);
@@ -197,34 +202,30 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     const bool skinny_ok = din != TG_F32 && M <= 128 && !(opt && opt->block_n) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR));
     if (skinny_ok) {
+        // One CTA per (128-column tile, K range); the K ranges of a tile form a
+        // cluster of 1, 2, 4 or 8 CTAs that sums its partials on chip.  Take the
+        // largest cluster that keeps every CTA resident at once (and every K
+        // range non-empty): the kernel streams B, so more CTAs means more bytes
+        // in flight.
         const int64_t ktiles = std::max<int64_t>(cdiv(K, 64), 1);
         const int64_t tiles = cdiv(N, 128);
-        int64_t s_lo = 1, s_hi = std::min<int64_t>(ktiles, 32);
-        if (opt && opt->splits) s_lo = s_hi = opt->splits;
-        double best = -1.0;
-        for (int64_t s = s_lo; s <= s_hi; ++s) {
-            const int64_t sc = std::max<int64_t>(1, std::min<int64_t>(s, ktiles));
+        int64_t best_s = 1;
+        for (int64_t sc : {2, 4, 8}) {
             const int64_t kps = cdiv(ktiles, sc);
-            const int64_t se = cdiv(ktiles, kps);
-            const int64_t units = tiles * se;
-            const int64_t slots = std::max<int64_t>(1, std::min(units, cap));
-            const double used = static_cast<double>(units) / static_cast<double>(slots);
-            const double waves = used + 0.25 * (static_cast<double>(cdiv(units, slots)) - used);
-            // bytes of B streamed per unit, plus the FP32 partial it writes and
-            // the reduction reads back
-            const double cost = waves * (16384.0 * kps + (se > 1 ? 1024.0 * M : 0.0));
-            if (best < 0 || cost < best) {
-                best = cost;
-                pl->k_per_split = kps;
-                p.splits = static_cast<int32_t>(se);
-                p.tiles = tiles;
-            }
+            if ((sc - 1) * kps >= ktiles) continue;          // a K range would be empty
+            if (tiles * sc > cap) continue;
+            if (opt && opt->splits && opt->splits != sc) continue;
+            best_s = sc;
         }
+        if (opt && opt->splits) best_s = opt->splits;      // validated below
         p.path = TG_PATH_SKINNY;
         p.block_m = tg::skinny_rows(M);
         p.block_n = 128;
         p.block_k = 64;
+        p.splits = static_cast<int32_t>(best_s);
+        p.tiles = tiles;
         pl->k_tiles = ktiles;
+        pl->k_per_split = cdiv(ktiles, best_s);
     }
     const bool pair = p.path == TG_PATH_TC_PAIR;
     p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m)
@@ -233,7 +234,9 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     pl->tiles_n = cdiv(N, p.block_n);
     const int64_t splits = p.splits;
     const int64_t units = p.tiles * splits;
-    if (pair) {
+    if (p.path == TG_PATH_SKINNY) {
+        p.ctas = static_cast<int32_t>(units);   // not persistent: one CTA per unit
+    } else if (pair) {
         const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(units, cap / 2));
         p.ctas = static_cast<int32_t>(2 * pairs);
     } else {
@@ -255,12 +258,13 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         pl->off_b = ws;
         ws = round_up(ws + (p.pack_b == 2 ? N : K) * pl->ldb_p * ei, 256);
     }
-    if (splits > 1) {
+    const bool global_partials = splits > 1 && p.path != TG_PATH_SKINNY;
+    if (global_partials) {
         pl->off_p = ws;
         ws = round_up(ws + splits * M * N * 4, 256);
     }
     p.workspace_bytes = ws;
-    p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (splits > 1 ? 1 : 0);
+    p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (global_partials ? 1 : 0);
     const int tmo = (opt && opt->timeout_ms) ? opt->timeout_ms : kDefaultTimeoutMs;
     pl->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
 }
@@ -427,17 +431,10 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         sp.out_kind = out_kind_of(dtype_out);
         sp.ldc = ldc;
         sp.c = c;
-        sp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
-        st = cuda_status(
-            tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, tmA, tmB, sp, p.ctas, s));
+        st = cuda_status(tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, tmA, tmB, sp, s));
         if (st != TG_OK) return fail(st);
-        if (p.splits > 1) {
-            st = cuda_status(tg::launch_splitk_reduce(sp.partial, p.splits, M, N, c, ldc,
-                                                      sp.out_kind, p.c_vector, s));
-            if (st != TG_OK) return fail(st);
-        }
         if (ws && cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
         return TG_OK;
     }

@@ -34,17 +34,17 @@ struct TcParams {
 };
 
 // Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with 128
-// output columns per work tile and all M <= 128 rows in one tile.
+// output columns per tile and all M <= 128 rows in one tile; one CTA per
+// (tile, K range), the K ranges of a tile forming one cluster.
 struct SkParams {
     int32_t M, N, K;
     int32_t tiles_n;            // ceil(N / 128)
     int32_t k_tiles;            // ceil(K / 64)
     int32_t k_tiles_per_split;
-    int32_t splits;
+    int32_t splits;             // cluster size: 1, 2, 4 or 8
     int32_t out_kind;
     int64_t ldc;
     void *c;
-    float *partial;             // [splits][M][N] when splits > 1
     int *status;
     uint64_t timeout_ns;
 };
@@ -53,8 +53,7 @@ struct SkParams {
 int skinny_rows(int64_t M);      // MMA N used for M rows: 16, 32, 64 or 128
 int skinny_stages(int mp);
 cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
-                               const CUtensorMap &tmB, const SkParams &p, int ctas,
-                               cudaStream_t stream);
+                               const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream);
 
 // gemm_tc.cu
 // `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `ctas` counts CTAs.
