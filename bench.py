@@ -409,7 +409,8 @@ def run_ours(args, world, rank, local):
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
             "peak_source": f"{pk_kind} ({'hbm_gbs' if skinny else 'bf16_tflops'} burst"
                            f"{', x0.5 nominal TF32/BF16 ratio' if din == 'f32' and not skinny else ''})",
-            "kernel": "gemm_tc_kernel" + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
+            "kernel": ("gemm_skinny_kernel" if plan["path"] == tg.TG_PATH_SKINNY else "gemm_tc_kernel")
+                      + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
             "launch_ms": round(kernel_ms, 5)}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,

@@ -122,12 +122,22 @@ def test_plan_tf32(lib):
 def test_plan_skinny_splits_k(lib, M):
     st, p = plan(M, 8192, 8192, sms=148)
     assert st == tg.TG_OK
-    assert p["path"] == tg.TG_PATH_SKINNY and p["block_n"] == 128
+    assert p["path"] == tg.TG_PATH_SKINNY and p["block_n"] in (128, 256, 512)
     assert p["block_m"] == {1: 16, 16: 16, 64: 64, 128: 128}[M]
-    assert p["tiles"] == 64 and p["splits"] in (2, 4, 8)
+    assert p["tiles"] == 8192 // p["block_n"] and p["splits"] in (2, 4, 8)
     assert p["ctas"] == p["tiles"] * p["splits"] <= 148    # one resident CTA per unit
     assert p["ctas"] * 2 > 148                               # the largest cluster that fits
     assert p["workspace_bytes"] == 0 and p["kernels"] == 1  # partials summed on chip
+
+
+def test_plan_skinny_tile_widths(lib):
+    for bn in (128, 256, 512):
+        st, p = plan(16, 4096, 4096, path=tg.TG_PATH_SKINNY, block_n=bn)
+        assert st == tg.TG_OK and p["block_n"] == bn and p["tiles"] == 4096 // bn
+    st, _ = plan(128, 4096, 4096, path=tg.TG_PATH_SKINNY, block_n=512)   # 128x512 FP32 partial
+    assert st == tg.TG_ERR_UNSUPPORTED
+    st, _ = plan(16, 4096, 4096, path=tg.TG_PATH_SKINNY, block_n=192)
+    assert st == tg.TG_ERR_UNSUPPORTED
 
 
 def test_plan_skinny_cluster_limits(lib):

@@ -135,6 +135,18 @@ def test_skinny_path_exact(din, dout, M, N, K, splits):
     compare(a, b, c, M, N, K, din, dout, exact=True)
 
 
+@pytest.mark.parametrize("M", [1, 16, 40, 64, 128])
+@pytest.mark.parametrize("block_n", [128, 256, 512])
+@pytest.mark.parametrize("splits", [1, 4])
+def test_skinny_tile_widths_exact(M, block_n, splits):
+    """Each column-tile width (1, 2 or 4 MMAs per k step), ragged N."""
+    if M > 64 and block_n == 512:
+        pytest.skip("128 x 512 FP32 partial tile does not fit shared memory (unsupported)")
+    N, K = 1300, 1000
+    a, b, c = run_gemm(M, N, K, "f16", "f32", dist="int", path=3, block_n=block_n, splits=splits)
+    compare(a, b, c, M, N, K, "f16", "f32", exact=True)
+
+
 @pytest.mark.parametrize("M", [1, 16, 128])
 def test_skinny_path_strided_uniform(M):
     N, K = 700, 900

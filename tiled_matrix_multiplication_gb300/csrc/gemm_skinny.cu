@@ -9,18 +9,20 @@
 // 128-row dimension runs over 128 output COLUMNS n and its N dimension over
 // the few output rows m (M rounded up to MP = 16, 32, 64 or 128):
 //   * MMA operand A = a B^T tile [128 n x 64 k], read N-major straight from
-//     row-major B (two 64-column TMA boxes per stage);
+//     row-major B (two 64-column TMA boxes);
 //   * MMA operand B = an A^T tile [64 k x MP m], read K-major from row-major A
 //     (one TMA box of MP rows);
 //   * the FP32 accumulator is 128 TMEM lanes (n) x MP columns (m).
-// Almost all of each shared-memory stage is B, so the ring holds 7-12 stages
-// of the streamed operand.
+// A CTA owns NT = 128, 256 or 512 consecutive columns (NT/128 MMAs per k step,
+// each into its own accumulator), so each row of B is read in NT*2-byte
+// contiguous runs and A is re-read once per NT columns.  Almost all of each
+// shared-memory stage is B.
 //
-// Work split: one CTA per (128-column tile, K range).  The S CTAs that share a
+// Work split: one CTA per (NT-column tile, K range).  The S CTAs that share a
 // column tile form a thread-block cluster (S = 1, 2, 4 or 8, cluster rank =
 // K range).  After its main loop each CTA parks its FP32 partial tile in its
 // own shared memory; after a cluster barrier, CTA r sums columns
-// [r*128/S, (r+1)*128/S) of the tile over all S partials, read in rank order
+// [r*NT/S, (r+1)*NT/S) of the tile over all S partials, read in rank order
 // from the peers' shared memory (distributed shared memory), rounds once and
 // writes C.  No partials go to global memory and no second kernel runs; the
 // sum order is fixed, so results do not depend on timing.
@@ -41,28 +43,33 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSmemBudget = 232448 - 1024 - 256;
-constexpr int kTileN = 128;   // output columns per tile (the MMA's M)
+constexpr int kSubN = 128;    // output columns per MMA (the MMA's M)
 
-template <int IN_KIND, int MP>
+template <int IN_KIND, int MP, int NT>
 struct SkCfg {
     static constexpr int BK = 64;                 // 128 bytes of K per row
     static constexpr int UMMA_K = 16;
     static constexpr int CHUNK_N = 64;            // n per 128-byte B row
+    static constexpr int SUB = NT / kSubN;        // MMAs (accumulators) per k step
     static constexpr int BT_BOX = BK * 128;       // one 64-column box: 8 KB
-    static constexpr int BT_STAGE = 2 * BT_BOX;   // 128 columns of B
+    static constexpr int BT_STAGE = (NT / CHUNK_N) * BT_BOX;   // NT columns of B
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
     static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 12 ? 12 : kSmemBudget / STAGE_BYTES;
-    static constexpr int PARTIAL_BYTES = kTileN * MP * 4;   // FP32 partial tile, [m][n]
-    static constexpr int TMEM_COLS = MP < 32 ? 32 : MP;
+    static constexpr int PARTIAL_BYTES = NT * MP * 4;   // FP32 partial tile, [m][n]
+    static constexpr int ACC_COLS = MP < 32 ? 32 : MP;  // TMEM columns per accumulator
+    static constexpr int TMEM_COLS = SUB * ACC_COLS;
     static constexpr int NUM_BARS = 2 * STAGES + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     // A operand (B^T) N-major, B operand (A^T) K-major; M = 128, N = MP.
     static constexpr uint32_t IDESC =
-        make_idesc(IN_KIND == IN_BF16 ? 1u : 0u, 1u, 0u, kTileN, MP);
+        make_idesc(IN_KIND == IN_BF16 ? 1u : 0u, 1u, 0u, kSubN, MP);
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte swizzle alignment");
     static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "partial tile reuses the ring");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 128, "MMA N");
+    static_assert(NT % kSubN == 0 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "accumulators fit one power-of-two TMEM allocation");
+    static_assert(STAGES >= 2, "at least a double-buffered ring");
 };
 
 __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float v) {
@@ -75,11 +82,11 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float 
         static_cast<__nv_bfloat16 *>(p.c)[off] = __float2bfloat16_rn(v);
 }
 
-template <int IN_KIND, int MP>
+template <int IN_KIND, int MP, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const SkParams p) {
-    using Cfg = SkCfg<IN_KIND, MP>;
+    using Cfg = SkCfg<IN_KIND, MP, NT>;
     constexpr int S = Cfg::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tfull_bar = bars + 8u * (2 * S);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *partial = reinterpret_cast<float *>(gbase);  // after the main loop: [MP][128]
+    float *partial = reinterpret_cast<float *>(gbase);  // after the main loop: [MP][NT]
     __shared__ int never_abort;
 
     const int warp = threadIdx.x >> 5;
@@ -144,9 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
                 const uint32_t fb = full_bar(stage);
                 tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
-                tma_load_2d(sBt + stage * Cfg::BT_STAGE, &tmB, fb, tn * kTileN, kt * Cfg::BK);
-                tma_load_2d(sBt + stage * Cfg::BT_STAGE + Cfg::BT_BOX, &tmB, fb,
-                            tn * kTileN + Cfg::CHUNK_N, kt * Cfg::BK);
+#pragma unroll
+                for (int j = 0; j < NT / Cfg::CHUNK_N; ++j)
+                    tma_load_2d(sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX, &tmB, fb,
+                                tn * NT + j * Cfg::CHUNK_N, kt * Cfg::BK);
                 ++issued;
                 if (++stage == S) {
                     stage = 0;
@@ -183,10 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t at0 = sAt + stage * Cfg::AT_STAGE;
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
-                    const uint64_t ad =
-                        smem_desc_sw128(bt0 + kk * Cfg::UMMA_K * 128, Cfg::BT_BOX, 1024);
                     const uint64_t bd = smem_desc_sw128(at0 + kk * 32, 16, 1024);
-                    umma_ss<0, 1>(tmem_base, ad, bd, Cfg::IDESC, (kt > kt0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int j = 0; j < Cfg::SUB; ++j) {
+                        // columns [j*128, j*128+128): boxes 2j and 2j+1 of the stage
+                        const uint64_t ad = smem_desc_sw128(
+                            bt0 + j * 2 * Cfg::BT_BOX + kk * Cfg::UMMA_K * 128, Cfg::BT_BOX, 1024);
+                        umma_ss<0, 1>(tmem_base + j * Cfg::ACC_COLS, ad, bd, Cfg::IDESC,
+                                      (kt > kt0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(empty_bar(stage));
                 if (++stage == S) {
@@ -215,41 +228,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
         } else {
             tc_fence_after_sync();
-            const int nl = quad * 32 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-            if (splits == 1) {
-                const int n = tn * kTileN + nl;
+#pragma unroll 1
+            for (int j = 0; j < Cfg::SUB; ++j) {
+                const int nl = j * kSubN + quad * 32 + lane;   // column within the tile
+                const int n = tn * NT + nl;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       j * Cfg::ACC_COLS;
                 if constexpr (MP == 16) {
                     uint32_t r[16];
                     tmem_load_16cols_sync(taddr, r);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < p.M && n < p.N) sk_store(p, j, n, __uint_as_float(r[j]));
-                } else {
-#pragma unroll 1
-                    for (int c0 = 0; c0 < MP; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_load_32cols_sync(taddr + c0, r);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < p.M && n < p.N) sk_store(p, c0 + j, n, __uint_as_float(r[j]));
+                    for (int q = 0; q < 16; ++q) {
+                        if (splits > 1)
+                            partial[q * NT + nl] = __uint_as_float(r[q]);
+                        else if (q < p.M && n < p.N)
+                            sk_store(p, q, n, __uint_as_float(r[q]));
                     }
-                }
-            } else {
-                // The ring is idle: every stage was consumed before tfull.
-                if constexpr (MP == 16) {
-                    uint32_t r[16];
-                    tmem_load_16cols_sync(taddr, r);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) partial[j * kTileN + nl] = __uint_as_float(r[j]);
                 } else {
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 32) {
                         uint32_t r[32];
                         tmem_load_32cols_sync(taddr + c0, r);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            partial[(c0 + j) * kTileN + nl] = __uint_as_float(r[j]);
+                        for (int q = 0; q < 32; ++q) {
+                            if (splits > 1)
+                                partial[(c0 + q) * NT + nl] = __uint_as_float(r[q]);
+                            else if (c0 + q < p.M && n < p.N)
+                                sk_store(p, c0 + q, n, __uint_as_float(r[q]));
+                        }
                     }
                 }
             }
@@ -261,14 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (splits > 1) {
         // --------------------------- cluster reduction over distributed smem
         cluster_sync_all();                       // every CTA's partial is in place
-        const int cols = kTileN / splits;         // columns reduced by this CTA
+        const int cols = NT / splits;             // columns reduced by this CTA
         const int rows = min(p.M, MP);
         const uint32_t part_addr = smem_addr(partial);
         for (int i = threadIdx.x; i < rows * cols; i += kThreads) {
             const int m = i / cols;
             const int nl = split * cols + (i - m * cols);
-            const int n = tn * kTileN + nl;
-            const uint32_t off = part_addr + static_cast<uint32_t>((m * kTileN + nl) * 4);
+            const int n = tn * NT + nl;
+            const uint32_t off = part_addr + static_cast<uint32_t>((m * NT + nl) * 4);
             float acc = 0.f;
             for (int s = 0; s < splits; ++s) acc += ld_shared_cluster_f32(map_to_cta(off, s));
             if (n < p.N) sk_store(p, m, n, acc);
@@ -281,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int IN_KIND, int MP>
+template <int IN_KIND, int MP, int NT>
 cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p,
                       cudaStream_t stream) {
-    using Cfg = SkCfg<IN_KIND, MP>;
-    auto kern = gemm_skinny_kernel<IN_KIND, MP>;
+    using Cfg = SkCfg<IN_KIND, MP, NT>;
+    auto kern = gemm_skinny_kernel<IN_KIND, MP, NT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -306,15 +312,39 @@ cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkPa
     return cudaGetLastError();
 }
 
-template <int IN_KIND>
-cudaError_t sk_launch_kind(int mp, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                           const SkParams &p, cudaStream_t stream) {
+template <int IN_KIND, int NT>
+cudaError_t sk_launch_mp(int mp, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                         const SkParams &p, cudaStream_t stream) {
     switch (mp) {
-    case 16: return sk_launch<IN_KIND, 16>(tmA, tmB, p, stream);
-    case 32: return sk_launch<IN_KIND, 32>(tmA, tmB, p, stream);
-    case 64: return sk_launch<IN_KIND, 64>(tmA, tmB, p, stream);
-    case 128: return sk_launch<IN_KIND, 128>(tmA, tmB, p, stream);
+    case 16: return sk_launch<IN_KIND, 16, NT>(tmA, tmB, p, stream);
+    case 32: return sk_launch<IN_KIND, 32, NT>(tmA, tmB, p, stream);
+    case 64: return sk_launch<IN_KIND, 64, NT>(tmA, tmB, p, stream);
+    case 128:
+        if constexpr (NT <= 256) return sk_launch<IN_KIND, 128, NT>(tmA, tmB, p, stream);
+        return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int IN_KIND>
+cudaError_t sk_launch_kind(int mp, int nt, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                           const SkParams &p, cudaStream_t stream) {
+    switch (nt) {
+    case 128: return sk_launch_mp<IN_KIND, 128>(mp, tmA, tmB, p, stream);
+    case 256: return sk_launch_mp<IN_KIND, 256>(mp, tmA, tmB, p, stream);
+    case 512: return sk_launch_mp<IN_KIND, 512>(mp, tmA, tmB, p, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int NT>
+int stages_nt(int mp) {
+    switch (mp) {
+    case 16: return SkCfg<IN_F16, 16, NT>::STAGES;
+    case 32: return SkCfg<IN_F16, 32, NT>::STAGES;
+    case 64: return SkCfg<IN_F16, 64, NT>::STAGES;
+    case 128: if constexpr (NT <= 256) return SkCfg<IN_F16, 128, NT>::STAGES; return 0;
+    default: return 0;
     }
 }
 
@@ -322,23 +352,26 @@ cudaError_t sk_launch_kind(int mp, const CUtensorMap &tmA, const CUtensorMap &tm
 
 int skinny_rows(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
 
-int skinny_stages(int mp) {
-    switch (mp) {
-    case 16: return SkCfg<IN_F16, 16>::STAGES;
-    case 32: return SkCfg<IN_F16, 32>::STAGES;
-    case 64: return SkCfg<IN_F16, 64>::STAGES;
-    case 128: return SkCfg<IN_F16, 128>::STAGES;
+bool skinny_supported(int mp, int nt) {
+    return (nt == 128 || nt == 256 || nt == 512) && !(mp == 128 && nt == 512);
+}
+
+int skinny_stages(int mp, int nt) {
+    switch (nt) {
+    case 128: return stages_nt<128>(mp);
+    case 256: return stages_nt<256>(mp);
+    case 512: return stages_nt<512>(mp);
     default: return 0;
     }
 }
 
-cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
+cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &tmA,
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream) {
     if (p.splits != 1 && p.splits != 2 && p.splits != 4 && p.splits != 8)
         return cudaErrorInvalidValue;
     switch (in_kind) {
-    case IN_F16: return sk_launch_kind<IN_F16>(mp, tmA, tmB, p, stream);
-    case IN_BF16: return sk_launch_kind<IN_BF16>(mp, tmA, tmB, p, stream);
+    case IN_F16: return sk_launch_kind<IN_F16>(mp, nt, tmA, tmB, p, stream);
+    case IN_BF16: return sk_launch_kind<IN_BF16>(mp, nt, tmA, tmB, p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -97,8 +97,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             return TG_ERR_INVALID_VALUE;
         if (opt->path == TG_PATH_SKINNY) {
             // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128,
-            // K split over a cluster of 1, 2, 4 or 8 CTAs (none of them empty)
-            if (din == TG_F32 || M > 128 || opt->block_n) return TG_ERR_UNSUPPORTED;
+            // K split over a cluster of 1, 2, 4 or 8 CTAs (none of them empty),
+            // 128, 256 or 512 columns per CTA
+            if (din == TG_F32 || M > 128) return TG_ERR_UNSUPPORTED;
+            if (opt->block_n && !tg::skinny_supported(tg::skinny_rows(M), opt->block_n))
+                return TG_ERR_UNSUPPORTED;
             const int64_t s = opt->splits;
             if (s != 0 && s != 1 && s != 2 && s != 4 && s != 8) return TG_ERR_UNSUPPORTED;
             const int64_t kt = std::max<int64_t>(cdiv(K, 64), 1);
@@ -199,7 +202,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     }
     // Small M with 16-bit operands: the transposed streaming kernel (one tile
     // holds all rows; work is spread over 128-column tiles and K splits).
-    const bool skinny_ok = din != TG_F32 && M <= 128 && !(opt && opt->block_n) &&
+    const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
+    const bool skinny_ok = din != TG_F32 && M <= 128 && (forced_skinny || !(opt && opt->block_n)) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR));
     if (skinny_ok) {
         // One CTA per (128-column tile, K range); the K ranges of a tile form a
@@ -208,7 +212,19 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         // range non-empty): the kernel streams B, so more CTAs means more bytes
         // in flight.
         const int64_t ktiles = std::max<int64_t>(cdiv(K, 64), 1);
-        const int64_t tiles = cdiv(N, 128);
+        const int mp = tg::skinny_rows(M);
+        // Columns per CTA: longer contiguous runs of B per row and fewer re-reads
+        // of A for wider tiles, as long as enough tiles remain to occupy the GPU.
+        int nt = (opt && opt->block_n) ? opt->block_n : 128;
+        if (!(opt && opt->block_n)) {
+            for (int cand : {512, 256}) {
+                if (!tg::skinny_supported(mp, cand)) continue;
+                if (cdiv(N, cand) * 8 >= cap / 2 || cand == 256) {
+                    if (cdiv(N, cand) * 8 >= cap / 2) { nt = cand; break; }
+                }
+            }
+        }
+        const int64_t tiles = cdiv(N, nt);
         int64_t best_s = 1;
         for (int64_t sc : {2, 4, 8}) {
             const int64_t kps = cdiv(ktiles, sc);
@@ -219,8 +235,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         }
         if (opt && opt->splits) best_s = opt->splits;      // validated below
         p.path = TG_PATH_SKINNY;
-        p.block_m = tg::skinny_rows(M);
-        p.block_n = 128;
+        p.block_m = mp;
+        p.block_n = nt;
         p.block_k = 64;
         p.splits = static_cast<int32_t>(best_s);
         p.tiles = tiles;
@@ -228,7 +244,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         pl->k_per_split = cdiv(ktiles, best_s);
     }
     const bool pair = p.path == TG_PATH_TC_PAIR;
-    p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m)
+    p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m, p.block_n)
                                          : tg::tc_stages(in_kind_of(din), p.block_n, pair);
     pl->tiles_m = cdiv(M, p.block_m);
     pl->tiles_n = cdiv(N, p.block_n);
@@ -433,7 +449,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         sp.c = c;
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
-        st = cuda_status(tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, tmA, tmB, sp, s));
+        st = cuda_status(
+            tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));
         if (st != TG_OK) return fail(st);
         if (ws && cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
         return TG_OK;

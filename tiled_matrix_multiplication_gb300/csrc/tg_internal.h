@@ -33,12 +33,12 @@ struct TcParams {
     uint64_t timeout_ns;
 };
 
-// Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with 128
+// Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with NT
 // output columns per tile and all M <= 128 rows in one tile; one CTA per
 // (tile, K range), the K ranges of a tile forming one cluster.
 struct SkParams {
     int32_t M, N, K;
-    int32_t tiles_n;            // ceil(N / 128)
+    int32_t tiles_n;            // ceil(N / NT)
     int32_t k_tiles;            // ceil(K / 64)
     int32_t k_tiles_per_split;
     int32_t splits;             // cluster size: 1, 2, 4 or 8
@@ -49,10 +49,12 @@ struct SkParams {
     uint64_t timeout_ns;
 };
 
-// gemm_skinny.cu
-int skinny_rows(int64_t M);      // MMA N used for M rows: 16, 32, 64 or 128
-int skinny_stages(int mp);
-cudaError_t launch_gemm_skinny(int in_kind, int mp, const CUtensorMap &tmA,
+// gemm_skinny.cu -- mp: MMA N used for the M rows (16, 32, 64, 128); nt: output
+// columns per CTA (128, 256, 512)
+int skinny_rows(int64_t M);
+bool skinny_supported(int mp, int nt);
+int skinny_stages(int mp, int nt);
+cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &tmA,
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream);
 
 // gemm_tc.cu
