@@ -154,3 +154,12 @@ def test_skinny_path_strided_uniform(M):
                        ldc=N + 8, splits=2)
     compare(a, b, c, M, N, K, "bf16", "bf16")
     assert padding_untouched(c, N, "bf16")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 128])
+def test_skinny_two_ctas_per_sm_exact(M):
+    """The half-ring variant (two CTAs per SM), forced by a small CTA budget."""
+    N, K = 4100, 2000
+    a, b, c = run_gemm(M, N, K, "bf16", "bf16", dist="int", path=3, block_n=128, splits=4,
+                       max_ctas=16)
+    compare(a, b, c, M, N, K, "bf16", "bf16", exact=True)

@@ -45,7 +45,9 @@ constexpr int kThreads = 192;
 constexpr int kSmemBudget = 232448 - 1024 - 256;
 constexpr int kSubN = 128;    // output columns per MMA (the MMA's M)
 
-template <int IN_KIND, int MP, int NT>
+// TWO: a half-size ring so that two CTAs share an SM (twice the CTAs, and
+// twice the independent TMA streams, for the same shared memory).
+template <int IN_KIND, int MP, int NT, bool TWO>
 struct SkCfg {
     static constexpr int BK = 64;                 // 128 bytes of K per row
     static constexpr int UMMA_K = 16;
@@ -55,7 +57,8 @@ struct SkCfg {
     static constexpr int BT_STAGE = (NT / CHUNK_N) * BT_BOX;   // NT columns of B
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
-    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 12 ? 12 : kSmemBudget / STAGE_BYTES;
+    static constexpr int BUDGET = TWO ? 112 * 1024 : kSmemBudget;
+    static constexpr int STAGES = BUDGET / STAGE_BYTES > 12 ? 12 : BUDGET / STAGE_BYTES;
     static constexpr int PARTIAL_BYTES = NT * MP * 4;   // FP32 partial tile, [m][n]
     static constexpr int ACC_COLS = MP < 32 ? 32 : MP;  // TMEM columns per accumulator
     static constexpr int TMEM_COLS = SUB * ACC_COLS;
@@ -82,11 +85,11 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float 
         static_cast<__nv_bfloat16 *>(p.c)[off] = __float2bfloat16_rn(v);
 }
 
-template <int IN_KIND, int MP, int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int IN_KIND, int MP, int NT, bool TWO>
+__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const SkParams p) {
-    using Cfg = SkCfg<IN_KIND, MP, NT>;
+    using Cfg = SkCfg<IN_KIND, MP, NT, TWO>;
     constexpr int S = Cfg::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -287,11 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int IN_KIND, int MP, int NT>
-cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p,
-                      cudaStream_t stream) {
-    using Cfg = SkCfg<IN_KIND, MP, NT>;
-    auto kern = gemm_skinny_kernel<IN_KIND, MP, NT>;
+template <int IN_KIND, int MP, int NT, bool TWO>
+cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p,
+                          cudaStream_t stream) {
+    using Cfg = SkCfg<IN_KIND, MP, NT, TWO>;
+    auto kern = gemm_skinny_kernel<IN_KIND, MP, NT, TWO>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -312,6 +315,16 @@ cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkPa
     return cudaGetLastError();
 }
 
+template <int IN_KIND, int MP, int NT>
+cudaError_t sk_launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const SkParams &p,
+                      cudaStream_t stream) {
+    if (p.two_per_sm) {
+        // the half-size ring exists for 128-column tiles only
+        if constexpr (NT == 128) return sk_launch_cfg<IN_KIND, MP, NT, true>(tmA, tmB, p, stream);
+        return cudaErrorInvalidValue;
+    }
+    return sk_launch_cfg<IN_KIND, MP, NT, false>(tmA, tmB, p, stream);
+}
 template <int IN_KIND, int NT>
 cudaError_t sk_launch_mp(int mp, const CUtensorMap &tmA, const CUtensorMap &tmB,
                          const SkParams &p, cudaStream_t stream) {
@@ -340,10 +353,10 @@ cudaError_t sk_launch_kind(int mp, int nt, const CUtensorMap &tmA, const CUtenso
 template <int NT>
 int stages_nt(int mp) {
     switch (mp) {
-    case 16: return SkCfg<IN_F16, 16, NT>::STAGES;
-    case 32: return SkCfg<IN_F16, 32, NT>::STAGES;
-    case 64: return SkCfg<IN_F16, 64, NT>::STAGES;
-    case 128: if constexpr (NT <= 256) return SkCfg<IN_F16, 128, NT>::STAGES; return 0;
+    case 16: return SkCfg<IN_F16, 16, NT, false>::STAGES;
+    case 32: return SkCfg<IN_F16, 32, NT, false>::STAGES;
+    case 64: return SkCfg<IN_F16, 64, NT, false>::STAGES;
+    case 128: if constexpr (NT <= 256) return SkCfg<IN_F16, 128, NT, false>::STAGES; return 0;
     default: return 0;
     }
 }

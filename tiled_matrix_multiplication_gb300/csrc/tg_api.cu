@@ -73,6 +73,7 @@ struct Plan {
     int64_t k_tiles = 0, k_per_split = 0, tiles_m = 0, tiles_n = 0;
     int64_t lda_p = 0, ldb_p = 0;              // pitches after packing
     int64_t off_a = 0, off_b = 0, off_p = 0;   // workspace offsets
+    bool skinny_two = false;                   // small-M kernel: two CTAs per SM
     uint64_t timeout_ns = 0;
 };
 
@@ -226,14 +227,26 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         }
         const int64_t tiles = cdiv(N, nt);
         int64_t best_s = 1;
+        bool two = false;
         for (int64_t sc : {2, 4, 8}) {
             const int64_t kps = cdiv(ktiles, sc);
             if ((sc - 1) * kps >= ktiles) continue;          // a K range would be empty
-            if (tiles * sc > cap) continue;
             if (opt && opt->splits && opt->splits != sc) continue;
-            best_s = sc;
+            if (tiles * sc <= cap) {
+                best_s = sc;
+                two = false;
+            } else if (nt == 128 && tiles * sc <= 2 * cap && tiles * best_s * 2 <= cap + cap / 2) {
+                // more CTAs than SMs: two half-size CTAs per SM keep them all resident
+                best_s = sc;
+                two = true;
+                break;
+            }
         }
-        if (opt && opt->splits) best_s = opt->splits;      // validated below
+        if (opt && opt->splits) {
+            best_s = opt->splits;                            // validated in validate()
+            two = nt == 128 && tiles * best_s > cap;
+        }
+        pl->skinny_two = two;
         p.path = TG_PATH_SKINNY;
         p.block_m = mp;
         p.block_n = nt;
@@ -449,6 +462,7 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         sp.c = c;
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
+        sp.two_per_sm = pl.skinny_two ? 1 : 0;
         st = cuda_status(
             tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));
         if (st != TG_OK) return fail(st);

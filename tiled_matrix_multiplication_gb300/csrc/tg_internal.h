@@ -43,6 +43,8 @@ struct SkParams {
     int32_t k_tiles_per_split;
     int32_t splits;             // cluster size: 1, 2, 4 or 8
     int32_t out_kind;
+    int32_t two_per_sm;         // half-size ring, two CTAs per SM
+    int32_t pad_;
     int64_t ldc;
     void *c;
     int *status;
