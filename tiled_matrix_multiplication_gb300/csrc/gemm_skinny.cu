@@ -350,13 +350,13 @@ cudaError_t sk_launch_kind(int mp, int nt, const CUtensorMap &tmA, const CUtenso
     }
 }
 
-template <int NT>
+template <int NT, bool TWO>
 int stages_nt(int mp) {
     switch (mp) {
-    case 16: return SkCfg<IN_F16, 16, NT, false>::STAGES;
-    case 32: return SkCfg<IN_F16, 32, NT, false>::STAGES;
-    case 64: return SkCfg<IN_F16, 64, NT, false>::STAGES;
-    case 128: if constexpr (NT <= 256) return SkCfg<IN_F16, 128, NT, false>::STAGES; return 0;
+    case 16: return SkCfg<IN_F16, 16, NT, TWO>::STAGES;
+    case 32: return SkCfg<IN_F16, 32, NT, TWO>::STAGES;
+    case 64: return SkCfg<IN_F16, 64, NT, TWO>::STAGES;
+    case 128: if constexpr (NT <= 256) return SkCfg<IN_F16, 128, NT, TWO>::STAGES; return 0;
     default: return 0;
     }
 }
@@ -369,11 +369,11 @@ bool skinny_supported(int mp, int nt) {
     return (nt == 128 || nt == 256 || nt == 512) && !(mp == 128 && nt == 512);
 }
 
-int skinny_stages(int mp, int nt) {
+int skinny_stages(int mp, int nt, bool two) {
     switch (nt) {
-    case 128: return stages_nt<128>(mp);
-    case 256: return stages_nt<256>(mp);
-    case 512: return stages_nt<512>(mp);
+    case 128: return two ? stages_nt<128, true>(mp) : stages_nt<128, false>(mp);
+    case 256: return two ? 0 : stages_nt<256, false>(mp);
+    case 512: return two ? 0 : stages_nt<512, false>(mp);
     default: return 0;
     }
 }

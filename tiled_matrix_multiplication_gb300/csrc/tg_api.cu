@@ -214,17 +214,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         // in flight.
         const int64_t ktiles = std::max<int64_t>(cdiv(K, 64), 1);
         const int mp = tg::skinny_rows(M);
-        // Columns per CTA: longer contiguous runs of B per row and fewer re-reads
-        // of A for wider tiles, as long as enough tiles remain to occupy the GPU.
-        int nt = (opt && opt->block_n) ? opt->block_n : 128;
-        if (!(opt && opt->block_n)) {
-            for (int cand : {512, 256}) {
-                if (!tg::skinny_supported(mp, cand)) continue;
-                if (cdiv(N, cand) * 8 >= cap / 2 || cand == 256) {
-                    if (cdiv(N, cand) * 8 >= cap / 2) { nt = cand; break; }
-                }
-            }
-        }
+        // 128 columns per CTA by default: on GB300 wider tiles (256, 512: longer
+        // contiguous runs of B, fewer re-reads of A) measured no faster at
+        // M <= 64 and slower at M = 128; they remain selectable.
+        const int nt = (opt && opt->block_n) ? opt->block_n : 128;
         const int64_t tiles = cdiv(N, nt);
         int64_t best_s = 1;
         bool two = false;
@@ -235,8 +228,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             if (tiles * sc <= cap) {
                 best_s = sc;
                 two = false;
-            } else if (nt == 128 && tiles * sc <= 2 * cap && tiles * best_s * 2 <= cap + cap / 2) {
-                // more CTAs than SMs: two half-size CTAs per SM keep them all resident
+            } else if (nt == 128 && tiles * sc <= 2 * cap) {
+                // more CTAs than SMs: two half-size CTAs per SM keep them all
+                // resident (measured faster than one full-size CTA per SM for
+                // every M from 1 to 128 at N = K = 8192)
                 best_s = sc;
                 two = true;
                 break;
@@ -257,7 +252,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         pl->k_per_split = cdiv(ktiles, best_s);
     }
     const bool pair = p.path == TG_PATH_TC_PAIR;
-    p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m, p.block_n)
+    p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m, p.block_n, pl->skinny_two)
                                          : tg::tc_stages(in_kind_of(din), p.block_n, pair);
     pl->tiles_m = cdiv(M, p.block_m);
     pl->tiles_n = cdiv(N, p.block_n);

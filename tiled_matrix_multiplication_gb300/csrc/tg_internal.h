@@ -55,7 +55,7 @@ struct SkParams {
 // columns per CTA (128, 256, 512)
 int skinny_rows(int64_t M);
 bool skinny_supported(int mp, int nt);
-int skinny_stages(int mp, int nt);
+int skinny_stages(int mp, int nt, bool two);
 cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &tmA,
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream);
 
