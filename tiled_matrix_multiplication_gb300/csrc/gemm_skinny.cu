@@ -138,6 +138,10 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Prologue done: let the next kernel's prologue start, then wait for the
+    // previous kernel's writes before the first global-memory access.
+    if (threadIdx.x == 0) grid_launch_dependents();
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -295,11 +299,10 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
                           cudaStream_t stream) {
     using Cfg = SkCfg<IN_KIND, MP, NT, TWO>;
     auto kern = gemm_skinny_kernel<IN_KIND, MP, NT, TWO>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
@@ -308,8 +311,10 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -251,6 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (PAIR) cluster_sync_all();   // peer barriers initialised before any remote signal
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Prologue done: let the next kernel's prologue start, then wait for the
+    // previous kernel's writes before the first global-memory access.
+    if (threadIdx.x == 0) grid_launch_dependents();
+    grid_dependency_wait();
 
     const int total = p.tiles_m * p.tiles_n * p.splits;
 
@@ -425,6 +429,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+}  // namespace
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device.
+cudaError_t set_smem_once(const void *kern, int bytes) {
+    static std::mutex mu;
+    static const void *done[256][2];
+    static int count = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < count; ++i)
+        if (done[i][0] == kern && done[i][1] == reinterpret_cast<const void *>(static_cast<intptr_t>(dev)))
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && count < 256) {
+        done[count][0] = kern;
+        done[count][1] = reinterpret_cast<const void *>(static_cast<intptr_t>(dev));
+        ++count;
+    }
+    return e;
+}
+
+namespace {
+
 struct ClusterCache {
     std::mutex mu;
     int max_clusters[64] = {0};
@@ -435,21 +464,23 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
                         int ctas, cudaStream_t stream) {
     using Cfg = TcCfg<IN_KIND, BN, PAIR>;
     auto kern = gemm_tc_kernel<IN_KIND, BN, PAIR>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         // Cap the persistent grid at the clusters that fit at once.
         static ClusterCache cache;
         int dev = 0;
@@ -471,8 +502,6 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
         cfg.gridDim = dim3(2 * pairs, 1, 1);
     } else {
         cfg.gridDim = dim3(ctas, 1, 1);
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
     }
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
     if (e != cudaSuccess) return e;

@@ -67,6 +67,7 @@ cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, const CUtensorMa
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);
 cudaError_t status_word_address(int **out);
+cudaError_t set_smem_once(const void *kernel, int bytes);
 
 // aux_kernels.cu
 cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,

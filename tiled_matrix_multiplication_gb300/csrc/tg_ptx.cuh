@@ -105,6 +105,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel in the stream is still running.  Everything before
+// grid_dependency_wait() must not touch global memory; the wait returns once
+// the preceding grid has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled (its prologue overlaps this
+// kernel's remaining work; it still waits for this grid to finish before
+// touching memory).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- cluster
 
 __device__ __forceinline__ uint32_t cluster_cta_rank() {
