@@ -112,6 +112,8 @@ typedef struct tg_plan {
     int32_t kernels;       /* kernel launches per call */
     int64_t tiles;         /* output tiles */
     int64_t workspace_bytes;
+    int32_t tail_tiles;    /* last tiles split over K to balance the last wave */
+    int32_t tail_splits;   /* K ranges per tail tile (partials summed in-kernel) */
 } tg_plan;
 
 /*

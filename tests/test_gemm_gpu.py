@@ -163,3 +163,31 @@ def test_skinny_two_ctas_per_sm_exact(M):
     a, b, c = run_gemm(M, N, K, "bf16", "bf16", dist="int", path=3, block_n=128, splits=4,
                        max_ctas=16)
     compare(a, b, c, M, N, K, "bf16", "bf16", exact=True)
+
+
+
+@pytest.mark.parametrize("path,block_n,max_ctas", [(1, 128, 10), (1, 256, 7), (2, 256, 14),
+                                                   (2, 128, 10), (2, 224, 6)])
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 2048), (1000, 700, 1500), (777, 1500, 4100)])
+def test_tail_split_exact(path, block_n, max_ctas, M, N, K):
+    """A short last wave split over K: partial tiles, last-arriving range sums
+    them (forced by a small CTA budget so that the tail is a few tiles)."""
+    import tiled_matrix_multiplication_gb300 as tg
+    p = tg.plan(M, N, K, "f16", "f16", num_sms=152, path=path, block_n=block_n, max_ctas=max_ctas)
+    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=path, block_n=block_n,
+                       max_ctas=max_ctas)
+    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
+    a, b, c = run_gemm(M, N, K, "bf16", "f32", dist="uniform", path=path, block_n=block_n,
+                       max_ctas=max_ctas, ldc=N + 4)
+    compare(a, b, c, M, N, K, "bf16", "f32")
+    assert padding_untouched(c, N, "f32")
+    return p
+
+
+def test_tail_split_is_exercised():
+    """The forced configurations above really do split a tail."""
+    import tiled_matrix_multiplication_gb300 as tg
+    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=1, block_n=128, max_ctas=10)
+    assert p["tail_tiles"] == 64 % 10 and p["tail_splits"] >= 2
+    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=2, block_n=256, max_ctas=14)
+    assert p["tail_tiles"] == 16 % 7 and p["tail_splits"] >= 2

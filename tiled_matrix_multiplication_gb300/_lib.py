@@ -49,7 +49,8 @@ class tg_plan(ctypes.Structure):
                 ("group_m", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
                 ("c_vector", ctypes.c_int32), ("kernels", ctypes.c_int32),
-                ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+                ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("tail_tiles", ctypes.c_int32), ("tail_splits", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

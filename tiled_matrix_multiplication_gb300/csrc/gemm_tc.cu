@@ -116,12 +116,27 @@ struct TcCfg {
 
 struct Work {
     int tm, tn, split, kt0, kt1;
+    int tail;   // index among the tail-split tiles, or -1
 };
+
+__device__ __forceinline__ int total_units(const TcParams &p) {
+    return p.tail_tiles > 0 ? p.tail_start + p.tail_tiles * p.tail_splits
+                            : p.tiles_m * p.tiles_n * p.splits;
+}
 
 __device__ __forceinline__ Work decode_work(const TcParams &p, int w) {
     Work r;
-    const int t = w / p.splits;
-    r.split = w - t * p.splits;
+    int t;
+    if (p.tail_tiles > 0 && w >= p.tail_start) {
+        const int u = w - p.tail_start;
+        r.tail = u / p.tail_splits;
+        r.split = u - r.tail * p.tail_splits;
+        t = p.tail_start + r.tail;
+    } else {
+        t = w / p.splits;
+        r.split = w - t * p.splits;
+        r.tail = -1;
+    }
     const int per_group = p.group_m * p.tiles_n;
     const int g = t / per_group;
     const int first_m = g * p.group_m;
@@ -129,9 +144,14 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, int w) {
     const int q = t - g * per_group;
     r.tm = first_m + q % size_m;
     r.tn = q / size_m;
-    r.kt0 = r.split * p.k_tiles_per_split;
-    r.kt1 = min(r.kt0 + p.k_tiles_per_split, p.k_tiles);
+    const int kps = r.tail >= 0 ? p.tail_kps : p.k_tiles_per_split;
+    r.kt0 = r.split * kps;
+    r.kt1 = min(r.kt0 + kps, p.k_tiles);
     return r;
+}
+
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
 }
 
 // Store 32 consecutive accumulator values (columns col .. col+31 of `row`).
@@ -216,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ int never_abort;
+    __shared__ int tail_last;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -256,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) grid_launch_dependents();
     grid_dependency_wait();
 
-    const int total = p.tiles_m * p.tiles_n * p.splits;
+    const int total = total_units(p);
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -397,16 +418,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int row =
-                wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M + quad * 32 + lane;
+            const int trow = static_cast<int>(rank) * Cfg::CTA_M + quad * 32 + lane;  // in tile
+            const int row = wk.tm * Cfg::TILE_M + trow;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_STRIDE;
+            // tail-split unit: this range's FP32 partial row of the tile
+            float *prow = nullptr;
+            if (wk.tail >= 0)
+                prow = p.tail_partial +
+                       ((static_cast<int64_t>(wk.tail) * p.tail_splits + wk.split) * Cfg::TILE_M +
+                        trow) * BN;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;
-                if (row < p.M && col < p.N) store_chunk(p, wk.split, row, col, r);
+                if (prow != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<uint4 *>(prow + c0 + j) =
+                            make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                } else if (row < p.M && col < p.N) {
+                    store_chunk(p, wk.split, row, col, r);
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -415,6 +449,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_cluster(tempty_bar(buf), 0);
                 else
                     mbar_arrive(tempty_bar(buf));
+            }
+            if (wk.tail >= 0) {
+                // The range that completes the tile last sums all ranges'
+                // partials, in range order, and writes C.  No range waits for
+                // another, so the order in which ranges run does not matter.
+                epilogue_bar_sync();                 // this CTA's partial rows written
+                if (threadIdx.x == 64) {
+                    __threadfence();
+                    const unsigned int old =
+                        atomicAdd(p.tail_count + wk.tail * Cfg::CTA_GROUP + rank, 1u);
+                    tail_last = (old == static_cast<unsigned int>(p.tail_splits - 1)) ? 1 : 0;
+                    __threadfence();
+                }
+                epilogue_bar_sync();
+                if (tail_last && row < p.M) {
+                    const float *base = p.tail_partial +
+                                        (static_cast<int64_t>(wk.tail) * p.tail_splits * Cfg::TILE_M +
+                                         trow) * BN;
+                    const int64_t split_stride = static_cast<int64_t>(Cfg::TILE_M) * BN;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        const int col = wk.tn * BN + c0;
+                        if (col >= p.N) break;
+                        float acc[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+                        for (int sidx = 0; sidx < p.tail_splits; ++sidx) {
+                            const float *src = base + sidx * split_stride + c0;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + j));
+                                acc[j] += v.x;
+                                acc[j + 1] += v.y;
+                                acc[j + 2] += v.z;
+                                acc[j + 3] += v.w;
+                            }
+                        }
+                        uint32_t r[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+                        store_chunk(p, 0, row, col, r);
+                    }
+                }
+                epilogue_bar_sync();                 // tail_last is reused by the next unit
             }
             ++acc_count;
         }

@@ -73,6 +73,8 @@ struct Plan {
     int64_t k_tiles = 0, k_per_split = 0, tiles_m = 0, tiles_n = 0;
     int64_t lda_p = 0, ldb_p = 0;              // pitches after packing
     int64_t off_a = 0, off_b = 0, off_p = 0;   // workspace offsets
+    int64_t off_tail = 0, off_cnt = 0;         // tail-split partials and counters
+    int64_t tail_start = 0, tail_kps = 0;
     bool skinny_two = false;                   // small-M kernel: two CTAs per SM
     uint64_t timeout_ns = 0;
 };
@@ -135,6 +137,17 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
     return TG_OK;
 }
 
+// K ranges for each tile of a short last wave (1 = no tail split): enough to
+// fill the idle slots, at most 8, and at least 8 K tiles per range.
+int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles) {
+    if (slots < 2) return 1;
+    const int64_t tail = tiles % slots;
+    if (tail == 0 || tail * 2 > slots) return 1;
+    int64_t ts = std::min<int64_t>(8, slots / tail);
+    ts = std::min<int64_t>(ts, k_tiles / 8);
+    return std::max<int64_t>(ts, 1);
+}
+
 void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
                const tg_options *opt, Plan *pl) {
@@ -185,7 +198,13 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             // at a quarter: fewer busy CTAs run faster (less contention for L2
             // bandwidth and power), so an idle slot costs less than a busy one.
             const double used = static_cast<double>(units) / static_cast<double>(std::max<int64_t>(1, std::min(units, slots)));
-            const double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
+            double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
+            // A split tail (below) turns a short last wave into 1/ts of a wave
+            // plus the partials' round trip.
+            if (se == 1 && !(opt && opt->splits)) {
+                const int64_t ts = tail_split_for(tiles, slots, pl->k_tiles);
+                if (ts > 1) waves = static_cast<double>(tiles / slots) + 1.15 / static_cast<double>(ts);
+            }
             const int64_t rows = std::min<int64_t>(M, kBlockM);
             const int64_t partial = se > 1 ? std::max<int64_t>(1, 24 * rows / kBlockM) : 0;
             const double cost =
@@ -287,6 +306,31 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         pl->off_p = ws;
         ws = round_up(ws + splits * M * N * 4, 256);
     }
+    // Tail split of the tensor-core paths (auto plans without a K split).
+    if (p.path != TG_PATH_SKINNY && splits == 1 && !(opt && opt->splits)) {
+        const int64_t slots = pair ? std::max<int64_t>(1, cap / 2) : std::max<int64_t>(1, cap);
+        const int64_t ts = tail_split_for(p.tiles, slots, pl->k_tiles);
+        if (ts > 1) {
+            p.tail_tiles = static_cast<int32_t>(p.tiles % slots);
+            pl->tail_start = p.tiles - p.tail_tiles;
+            pl->tail_kps = cdiv(pl->k_tiles, ts);
+            p.tail_splits = static_cast<int32_t>(cdiv(pl->k_tiles, pl->tail_kps));
+            const int64_t cta_group = pair ? 2 : 1;
+            pl->off_tail = ws;
+            ws = round_up(ws + static_cast<int64_t>(p.tail_tiles) * p.tail_splits * p.block_m *
+                                   p.block_n * 4, 256);
+            pl->off_cnt = ws;
+            ws = round_up(ws + static_cast<int64_t>(p.tail_tiles) * cta_group * 4, 256);
+            if (pair) {
+                const int64_t pairs = std::max<int64_t>(
+                    1, std::min<int64_t>(pl->tail_start + p.tail_tiles * p.tail_splits, cap / 2));
+                p.ctas = static_cast<int32_t>(2 * pairs);
+            } else {
+                p.ctas = static_cast<int32_t>(std::max<int64_t>(
+                    1, std::min<int64_t>(pl->tail_start + p.tail_tiles * p.tail_splits, cap)));
+            }
+        }
+    }
     p.workspace_bytes = ws;
     p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (global_partials ? 1 : 0);
     const int tmo = (opt && opt->timeout_ms) ? opt->timeout_ms : kDefaultTimeoutMs;
@@ -384,12 +428,11 @@ tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t l
     if (v != TG_OK) return v;
     Plan pl;
     make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, opt, &pl);
-    if (M == 0 || N == 0) {
+    if (M == 0 || N == 0 || K == 0) {   // nothing, or a memset of C: no kernel of the library
         pl.pub.kernels = 0;
         pl.pub.workspace_bytes = 0;
-    } else if (K == 0) {
-        pl.pub.kernels = 0;   // a memset, no kernel of the library
-        pl.pub.workspace_bytes = 0;
+        pl.pub.tail_tiles = 0;
+        pl.pub.tail_splits = 0;
     }
     *plan = pl.pub;
     return TG_OK;
@@ -490,6 +533,17 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
     tp.status = dev->status;
     tp.timeout_ns = pl.timeout_ns;
+    if (p.tail_tiles > 0) {
+        tp.tail_start = static_cast<int32_t>(pl.tail_start);
+        tp.tail_tiles = p.tail_tiles;
+        tp.tail_splits = p.tail_splits;
+        tp.tail_kps = static_cast<int32_t>(pl.tail_kps);
+        tp.tail_partial = reinterpret_cast<float *>(ws + pl.off_tail);
+        tp.tail_count = reinterpret_cast<unsigned int *>(ws + pl.off_cnt);
+        const size_t cnt_bytes = static_cast<size_t>(p.tail_tiles) * (pair ? 2 : 1) * 4;
+        st = cuda_status(cudaMemsetAsync(tp.tail_count, 0, cnt_bytes, s));
+        if (st != TG_OK) return fail(st);
+    }
     st = cuda_status(
         tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair, tmA, tmB, tp, p.ctas, s));
     if (st != TG_OK) return fail(st);

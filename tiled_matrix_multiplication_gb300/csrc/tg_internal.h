@@ -31,6 +31,15 @@ struct TcParams {
     float *partial;             // [splits][M][N] when splits > 1
     int *status;                // device status word (2 ints)
     uint64_t timeout_ns;
+    // Tail split (splits == 1 only): the last `tail_tiles` tiles in raster
+    // order are each split into `tail_splits` K ranges of `tail_kps` K tiles,
+    // addressed by unit indices >= tail_start.  Each range writes an FP32
+    // partial tile to `tail_partial` ([tail_tiles][tail_splits][TILE_M][BN]);
+    // the range that finishes a tile last (counted per tile and CTA of a pair
+    // in `tail_count`, zero before the launch) sums them in range order into C.
+    int32_t tail_start, tail_tiles, tail_splits, tail_kps;
+    float *tail_partial;
+    unsigned int *tail_count;
 };
 
 // Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with NT
