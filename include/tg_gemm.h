@@ -30,8 +30,9 @@
  *
  * Ownership.  a, b and c are DEVICE pointers owned by the caller and must stay
  * valid until the work enqueued on `stream` has finished.  The library owns only
- * temporary device workspace (stream-ordered, freed on the same stream) and
- * internal caches.  `stream` is a cudaStream_t passed as void*; NULL is the
+ * temporary device workspace (stream-ordered, taken from and returned to a
+ * memory pool of its own on the same stream; the pool keeps the memory for
+ * later calls) and internal caches.  `stream` is a cudaStream_t passed as void*; NULL is the
  * legacy default stream.
  *
  * Asynchrony and errors.  The GEMM calls validate their arguments on the host,

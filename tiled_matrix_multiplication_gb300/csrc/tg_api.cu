@@ -23,6 +23,11 @@ struct DeviceState {
     tg_status arch = TG_OK;
     int sms = 0;
     int *status = nullptr;
+    // The library's own stream-ordered memory pool for workspace.  Its release
+    // threshold is unlimited, so memory freed at the end of a call is kept for
+    // the next one instead of being unmapped and mapped again; the process's
+    // default pool is left untouched.
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -366,6 +371,16 @@ tg_status device_state(DeviceState **out) {
         if (d.arch == TG_OK) {
             if (tg::status_word_address(&d.status) != cudaSuccess) return TG_ERR_CUDA;
             if (init_encoder() != TG_OK) return TG_ERR_CUDA;
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) return TG_ERR_CUDA;
+            uint64_t keep = ~0ull;
+            if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+                return TG_ERR_CUDA;
         }
         d.init = true;
     }
@@ -459,7 +474,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
 
     uint8_t *ws = nullptr;
     if (p.workspace_bytes > 0) {
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), p.workspace_bytes, s);
+        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), p.workspace_bytes,
+                                                dev->pool, s);
         if (e != cudaSuccess) return cuda_status(e);
     }
     auto fail = [&](tg_status code) {
