@@ -95,7 +95,9 @@ typedef struct tg_options {
     int32_t group_m;      /* grouped raster height in tiles (default 8) */
     int32_t max_ctas;     /* cap on the persistent grid (default: one per SM) */
     int32_t timeout_ms;   /* bound on every device-side wait (default 2000) */
-    int32_t reserved[2];  /* must be zero */
+    int32_t tail_splits;  /* split each tile of a short last wave over this many K
+                             ranges (2..8; partials summed in the kernel); 0 = no */
+    int32_t reserved;     /* must be zero */
 } tg_options;
 
 /* What a call would launch (see tg_plan_gemm). */

@@ -96,22 +96,26 @@ def test_plan_square_4096(lib):
     assert p["tiles"] == (4096 // 256) * (4096 // p["block_n"])
     assert p["splits"] == 1 and p["ctas"] == 148
     assert p["pack_a"] == 0 and p["pack_b"] == 0 and p["c_vector"] == 1
-    assert p["kernels"] == 1
-    # 256 tiles on 74 pairs: the 34 tiles of the short last wave are split over K
-    assert p["tail_tiles"] == 256 % 74 and p["tail_splits"] == 2
-    assert p["workspace_bytes"] >= p["tail_tiles"] * 2 * 256 * p["block_n"] * 4
+    assert p["kernels"] == 1 and p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
 
 
 def test_plan_tail_split_rules(lib):
+    # 256 tiles on 74 pairs: the 34 tiles of the short last wave split over K
+    st, p = plan(4096, 4096, 4096, sms=148, tail_splits=2)
+    assert st == tg.TG_OK and p["tail_tiles"] == 256 % 74 and p["tail_splits"] == 2
+    assert p["workspace_bytes"] >= p["tail_tiles"] * 2 * 256 * p["block_n"] * 4
     # a full last wave: nothing to split
-    st, p = plan(8192, 4096, 4096, "bf16", sms=128)
+    st, p = plan(8192, 4096, 4096, "bf16", sms=128, tail_splits=4)
     assert st == tg.TG_OK and p["tiles"] % 64 == 0 and p["tail_tiles"] == 0
-    # forced K split replaces the tail split
-    st, p = plan(4096, 4096, 4096, sms=148, splits=2, path=tg.TG_PATH_TC_PAIR)
+    # a K split replaces the tail split
+    st, p = plan(4096, 4096, 4096, sms=148, splits=2, path=tg.TG_PATH_TC_PAIR, tail_splits=2)
     assert st == tg.TG_OK and p["tail_tiles"] == 0 and p["splits"] == 2
     # short K: ranges would be under 8 K tiles
-    st, p = plan(4096, 4096, 256, sms=148)
+    st, p = plan(4096, 4096, 256, sms=148, tail_splits=4)
     assert st == tg.TG_OK and p["tail_tiles"] == 0
+    for bad in (1, 9, -1):
+        st, _ = plan(512, 512, 512, tail_splits=bad)
+        assert st == tg.TG_ERR_INVALID_VALUE
 
 
 def test_plan_config1_needs_pack(lib):

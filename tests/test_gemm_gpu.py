@@ -173,12 +173,13 @@ def test_tail_split_exact(path, block_n, max_ctas, M, N, K):
     """A short last wave split over K: partial tiles, last-arriving range sums
     them (forced by a small CTA budget so that the tail is a few tiles)."""
     import tiled_matrix_multiplication_gb300 as tg
-    p = tg.plan(M, N, K, "f16", "f16", num_sms=152, path=path, block_n=block_n, max_ctas=max_ctas)
+    p = tg.plan(M, N, K, "f16", "f16", num_sms=152, path=path, block_n=block_n, max_ctas=max_ctas,
+                tail_splits=8)
     a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=path, block_n=block_n,
-                       max_ctas=max_ctas)
+                       max_ctas=max_ctas, tail_splits=8)
     compare(a, b, c, M, N, K, "f16", "f16", exact=True)
     a, b, c = run_gemm(M, N, K, "bf16", "f32", dist="uniform", path=path, block_n=block_n,
-                       max_ctas=max_ctas, ldc=N + 4)
+                       max_ctas=max_ctas, ldc=N + 4, tail_splits=3)
     compare(a, b, c, M, N, K, "bf16", "f32")
     assert padding_untouched(c, N, "f32")
     return p
@@ -187,7 +188,9 @@ def test_tail_split_exact(path, block_n, max_ctas, M, N, K):
 def test_tail_split_is_exercised():
     """The forced configurations above really do split a tail."""
     import tiled_matrix_multiplication_gb300 as tg
-    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=1, block_n=128, max_ctas=10)
+    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=1, block_n=128, max_ctas=10,
+                tail_splits=8)
     assert p["tail_tiles"] == 64 % 10 and p["tail_splits"] >= 2
-    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=2, block_n=256, max_ctas=14)
+    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=2, block_n=256, max_ctas=14,
+                tail_splits=8)
     assert p["tail_tiles"] == 16 % 7 and p["tail_splits"] >= 2

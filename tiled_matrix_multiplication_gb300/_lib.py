@@ -39,7 +39,7 @@ class tg_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("block_n", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("tail_splits", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class tg_plan(ctypes.Structure):
@@ -105,10 +105,11 @@ def _code(dtype) -> int:
     return DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
 
 
-def make_options(path=0, splits=0, block_n=0, group_m=0, max_ctas=0, timeout_ms=0):
+def make_options(path=0, splits=0, block_n=0, group_m=0, max_ctas=0, timeout_ms=0,
+                 tail_splits=0):
     o = tg_options()
     o.path, o.splits, o.block_n, o.group_m = path, splits, block_n, group_m
-    o.max_ctas, o.timeout_ms = max_ctas, timeout_ms
+    o.max_ctas, o.timeout_ms, o.tail_splits = max_ctas, timeout_ms, tail_splits
     return o
 
 

@@ -98,7 +98,9 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
     if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36) || ldc > (int64_t(1) << 36))
         return TG_ERR_UNSUPPORTED;
     if (opt) {
-        if (opt->reserved[0] || opt->reserved[1]) return TG_ERR_INVALID_VALUE;
+        if (opt->reserved) return TG_ERR_INVALID_VALUE;
+        if (opt->tail_splits < 0 || opt->tail_splits == 1 || opt->tail_splits > 8)
+            return TG_ERR_INVALID_VALUE;
         if (opt->path < TG_PATH_AUTO || opt->path > TG_PATH_SKINNY) return TG_ERR_INVALID_VALUE;
         if (opt->splits < 0 || opt->block_n < 0 || opt->group_m < 0 || opt->max_ctas < 0 ||
             opt->timeout_ms < 0)
@@ -142,13 +144,15 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
     return TG_OK;
 }
 
-// K ranges for each tile of a short last wave (1 = no tail split): enough to
-// fill the idle slots, at most 8, and at least 8 K tiles per range.
-int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles) {
-    if (slots < 2) return 1;
+// K ranges for each tile of a short last wave (1 = no tail split): at most
+// `want`, no more than fill the idle slots, and at least 8 K tiles per range.
+// (On GB300 the in-kernel sum of the partials currently costs more than the
+// balanced wave saves, so the planner only splits a tail when asked to.)
+int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles, int64_t want) {
+    if (slots < 2 || want < 2) return 1;
     const int64_t tail = tiles % slots;
     if (tail == 0 || tail * 2 > slots) return 1;
-    int64_t ts = std::min<int64_t>(8, slots / tail);
+    int64_t ts = std::min<int64_t>(want, slots / tail);
     ts = std::min<int64_t>(ts, k_tiles / 8);
     return std::max<int64_t>(ts, 1);
 }
@@ -204,10 +208,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             // bandwidth and power), so an idle slot costs less than a busy one.
             const double used = static_cast<double>(units) / static_cast<double>(std::max<int64_t>(1, std::min(units, slots)));
             double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
-            // A split tail (below) turns a short last wave into 1/ts of a wave
-            // plus the partials' round trip.
-            if (se == 1 && !(opt && opt->splits)) {
-                const int64_t ts = tail_split_for(tiles, slots, pl->k_tiles);
+            // A requested tail split (below) turns a short last wave into 1/ts
+            // of a wave plus the partials' round trip.
+            if (se == 1 && opt && opt->tail_splits && !opt->splits) {
+                const int64_t ts = tail_split_for(tiles, slots, pl->k_tiles, opt->tail_splits);
                 if (ts > 1) waves = static_cast<double>(tiles / slots) + 1.15 / static_cast<double>(ts);
             }
             const int64_t rows = std::min<int64_t>(M, kBlockM);
@@ -312,9 +316,9 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         ws = round_up(ws + splits * M * N * 4, 256);
     }
     // Tail split of the tensor-core paths (auto plans without a K split).
-    if (p.path != TG_PATH_SKINNY && splits == 1 && !(opt && opt->splits)) {
+    if (p.path != TG_PATH_SKINNY && splits == 1 && opt && opt->tail_splits && !opt->splits) {
         const int64_t slots = pair ? std::max<int64_t>(1, cap / 2) : std::max<int64_t>(1, cap);
-        const int64_t ts = tail_split_for(p.tiles, slots, pl->k_tiles);
+        const int64_t ts = tail_split_for(p.tiles, slots, pl->k_tiles, opt->tail_splits);
         if (ts > 1) {
             p.tail_tiles = static_cast<int32_t>(p.tiles % slots);
             pl->tail_start = p.tiles - p.tail_tiles;
