@@ -97,7 +97,8 @@ typedef struct tg_options {
     int32_t timeout_ms;   /* bound on every device-side wait (default 2000) */
     int32_t tail_splits;  /* split each tile of a short last wave over this many K
                              ranges (2..8; partials summed in the kernel); 0 = no */
-    int32_t reserved;     /* must be zero */
+    int32_t multicast;    /* CTA pairs only: 2 = clusters of two pairs that share A
+                             tiles by TMA multicast, 1 = no sharing, 0 = planner */
 } tg_options;
 
 /* What a call would launch (see tg_plan_gemm). */
@@ -117,6 +118,8 @@ typedef struct tg_plan {
     int64_t workspace_bytes;
     int32_t tail_tiles;    /* last tiles split over K to balance the last wave */
     int32_t tail_splits;   /* K ranges per tail tile (partials summed in-kernel) */
+    int32_t multicast;     /* tiles per cluster sharing A (1 or 2) */
+    int32_t reserved;
 } tg_plan;
 
 /*

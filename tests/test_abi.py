@@ -93,7 +93,8 @@ def test_plan_square_4096(lib):
     st, p = plan(4096, 4096, 4096, sms=148)
     assert st == tg.TG_OK
     assert p["path"] == tg.TG_PATH_TC_PAIR and p["block_m"] == 256 and p["block_k"] == 64
-    assert p["tiles"] == (4096 // 256) * (4096 // p["block_n"])
+    # work units: tiles, or pairs of adjacent tiles sharing A by multicast
+    assert p["tiles"] == (4096 // 256) * -(-(4096 // p["block_n"]) // p["multicast"])
     assert p["splits"] == 1 and p["ctas"] == 148
     assert p["pack_a"] == 0 and p["pack_b"] == 0 and p["c_vector"] == 1
     assert p["kernels"] == 1 and p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
@@ -182,6 +183,19 @@ def test_plan_forced_options(lib):
     st, p = plan(1024, 1024, 512, path=tg.TG_PATH_TC_PAIR, block_n=128, max_ctas=10)
     assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR and p["block_m"] == 256
     assert p["ctas"] == 10 and p["tiles"] == 4 * 8
+
+
+def test_plan_multicast_rules(lib):
+    st, p = plan(4096, 4096, 4096, multicast=2, block_n=256, sms=148)
+    assert st == tg.TG_OK and p["multicast"] == 2 and p["ctas"] % 4 == 0
+    st, p = plan(4096, 4096, 4096, multicast=1, sms=148)
+    assert st == tg.TG_OK and p["multicast"] == 1
+    for bad in (dict(multicast=2, path=tg.TG_PATH_TC), dict(multicast=2, splits=2),
+                dict(multicast=2, block_n=128), dict(multicast=2, tail_splits=2)):
+        st, _ = plan(4096, 4096, 4096, **bad)
+        assert st == tg.TG_ERR_UNSUPPORTED, bad
+    st, _ = plan(4096, 4096, 4096, multicast=3)
+    assert st == tg.TG_ERR_INVALID_VALUE
 
 
 def test_plan_width_limits(lib):

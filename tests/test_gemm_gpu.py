@@ -194,3 +194,26 @@ def test_tail_split_is_exercised():
     p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=2, block_n=256, max_ctas=14,
                 tail_splits=8)
     assert p["tail_tiles"] == 16 % 7 and p["tail_splits"] >= 2
+
+
+
+@pytest.mark.parametrize("block_n", [192, 224, 256])
+@pytest.mark.parametrize("M,N,K,max_ctas", [(1024, 1024, 1024, 0), (1000, 1500, 700, 0),
+                                            (700, 300, 2000, 8), (2048, 2048, 512, 8),
+                                            (300, 5000, 300, 12)])
+def test_multicast_pairs_exact(block_n, M, N, K, max_ctas):
+    """Clusters of two CTA pairs sharing A tiles by TMA multicast: ragged M, an odd
+    number of column tiles (the second tile of the last unit lies beyond N), and
+    small grids that walk many units."""
+    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=2, block_n=block_n, multicast=2,
+                       max_ctas=max_ctas)
+    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
+
+
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f16", "f32")])
+def test_multicast_pairs_uniform(din, dout):
+    M, N, K = 1536, 2560, 1200
+    a, b, c = run_gemm(M, N, K, din, dout, dist="uniform", path=2, block_n=256, multicast=2,
+                       ldc=N + 8)
+    compare(a, b, c, M, N, K, din, dout)
+    assert padding_untouched(c, N, dout)

@@ -43,6 +43,12 @@
 //       empty[s]  in both CTAs: the leader's MMA commit, multicast to both;
 //       tfull[b]  in both CTAs: the leader's commit after a tile's last MMA;
 //       tempty[b] leader's only: one arrive per epilogue warp of both CTAs.
+//   MC = 2 (with PAIR): a cluster of two pairs works on two horizontally
+//     adjacent tiles, which read the same A rows.  Each CTA loads half of its
+//     128 rows of A and multicasts them to the CTA in the same position of the
+//     other pair, so A is read from L2 once per two pairs.  A stage may then
+//     be refilled only after both pairs' MMAs are done with it: empty[s]
+//     counts one commit from each pair leader.
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = epilogue (warp w may read TMEM lanes 32*(w%4) .. +31).
@@ -75,7 +81,7 @@ constexpr int kThreads = 192;
 // the alignment slack and the barriers.
 constexpr int kSmemBudget = 232448 - 1024 - 256;
 
-template <int IN_KIND, int BN, bool PAIR>
+template <int IN_KIND, int BN, bool PAIR, int MC = 1>
 struct TcCfg {
     static constexpr int ESIZE = IN_KIND == IN_TF32 ? 4 : 2;
     static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
@@ -83,6 +89,7 @@ struct TcCfg {
     static constexpr int CHUNK_N = 128 / ESIZE;   // N elements in one 128-byte B row
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
     static constexpr int CTA_GROUP = PAIR ? 2 : 1;
+    static constexpr int CLUSTER = CTA_GROUP * MC;      // CTAs per cluster
     static constexpr int CTA_M = 128;             // accumulator rows held by one CTA
     static constexpr int TILE_M = PAIR ? 256 : 128;
     static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
@@ -112,6 +119,7 @@ struct TcCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(MC == 1 || (MC == 2 && PAIR), "A multicast pairs CTA pairs");
 };
 
 struct Work {
@@ -119,12 +127,18 @@ struct Work {
     int tail;   // index among the tail-split tiles, or -1
 };
 
-__device__ __forceinline__ int total_units(const TcParams &p) {
-    return p.tail_tiles > 0 ? p.tail_start + p.tail_tiles * p.tail_splits
-                            : p.tiles_m * p.tiles_n * p.splits;
+// Columns of work units: with A multicast one unit is two adjacent tiles.
+__device__ __forceinline__ int unit_cols(const TcParams &p) {
+    return (p.tiles_n + p.mc - 1) / p.mc;
 }
 
-__device__ __forceinline__ Work decode_work(const TcParams &p, int w) {
+__device__ __forceinline__ int total_units(const TcParams &p) {
+    return p.tail_tiles > 0 ? p.tail_start + p.tail_tiles * p.tail_splits
+                            : p.tiles_m * unit_cols(p) * p.splits;
+}
+
+// `q`: which tile of a multicast unit this CTA's pair works on.
+__device__ __forceinline__ Work decode_work(const TcParams &p, int w, int q = 0) {
     Work r;
     int t;
     if (p.tail_tiles > 0 && w >= p.tail_start) {
@@ -137,13 +151,13 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, int w) {
         r.split = w - t * p.splits;
         r.tail = -1;
     }
-    const int per_group = p.group_m * p.tiles_n;
+    const int per_group = p.group_m * unit_cols(p);
     const int g = t / per_group;
     const int first_m = g * p.group_m;
     const int size_m = min(p.tiles_m - first_m, p.group_m);
-    const int q = t - g * per_group;
-    r.tm = first_m + q % size_m;
-    r.tn = q / size_m;
+    const int pos = t - g * per_group;
+    r.tm = first_m + pos % size_m;
+    r.tn = (pos / size_m) * p.mc + q;
     const int kps = r.tail >= 0 ? p.tail_kps : p.k_tiles_per_split;
     r.kt0 = r.split * kps;
     r.kt1 = min(r.kt0 + kps, p.k_tiles);
@@ -212,11 +226,11 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
     }
 }
 
-template <int IN_KIND, int BN, bool PAIR>
+template <int IN_KIND, int BN, bool PAIR, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
-    using Cfg = TcCfg<IN_KIND, BN, PAIR>;
+    using Cfg = TcCfg<IN_KIND, BN, PAIR, MC>;
     constexpr int S = Cfg::STAGES;
     constexpr int CG = Cfg::CTA_GROUP;
 
@@ -240,15 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
+    const uint32_t crank = PAIR ? cluster_cta_rank() : 0u;       // rank in the cluster
+    const uint32_t rank = crank % CG;                             // position in the pair
+    const int q = static_cast<int>(crank / CG);                   // pair within the cluster
+    const uint32_t pair_leader = static_cast<uint32_t>(q * CG);   // cluster rank of my leader
     const bool leader = rank == 0;
-    const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int unit0 = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
+    const int unit_step = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC);   // one MMA commit per pair sharing the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -287,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int w = unit0; w < total && ok; w += unit_step) {
-                const Work wk = decode_work(p, w);
+                const Work wk = decode_work(p, w, q);
                 const int row0 = wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M;
                 const int col0 = wk.tn * BN + static_cast<int>(rank) * Cfg::BN_CTA;
                 for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
@@ -296,14 +313,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
-                    const uint32_t fb = PAIR ? map_to_cta(full_bar(stage), 0) : full_bar(stage);
+                    const uint32_t fb =
+                        PAIR ? map_to_cta(full_bar(stage), pair_leader) : full_bar(stage);
                     auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
                         if constexpr (PAIR)
                             tma_load_2d_pair(dst, map, fb, x, y);
                         else
                             tma_load_2d(dst, map, fb, x, y);
                     };
-                    load(sA + stage * Cfg::A_STAGE, &tmA, kt * Cfg::BK, row0);
+                    if constexpr (MC == 2) {
+                        // my half (q) of this CTA's A rows, to me and my counterpart
+                        const uint16_t mask =
+                            static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
+                        tma_load_2d_pair_mc(sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2),
+                                            &tmA, fb, kt * Cfg::BK, row0 + q * (Cfg::CTA_M / 2),
+                                            mask);
+                    } else {
+                        load(sA + stage * Cfg::A_STAGE, &tmA, kt * Cfg::BK, row0);
+                    }
                     if constexpr (Cfg::B_KMAJOR) {
                         // B^T tile [BN_CTA rows of N] x [BK of K], one box
                         load(sB + stage * Cfg::B_STAGE, &tmB, kt * Cfg::BK, col0);
@@ -347,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_count = 0;
             bool ok = true;
             for (int w = unit0; w < total && ok; w += unit_step) {
-                const Work wk = decode_work(p, w);
+                const Work wk = decode_work(p, w, q);
                 const uint32_t buf = acc_count & 1u;
                 const uint32_t acc_phase = (acc_count >> 1) & 1u;
                 if (!mbar_wait<PAIR>(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -374,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_ss<Cfg::KIND, CG>(d_tmem, ad, bd, Cfg::IDESC,
                                                (kt > wk.kt0 || kk > 0) ? 1u : 0u);
                     }
-                    if constexpr (PAIR)
-                        umma_commit_pair(empty_bar(stage), 0x3);
+                    if constexpr (PAIR)   // every CTA whose stage this pair read from
+                        umma_commit_pair(empty_bar(stage), MC == 2 ? 0xF : 0x3);
                     else
                         umma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -385,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 if constexpr (PAIR)
-                    umma_commit_pair(tfull_bar(buf), 0x3);
+                    umma_commit_pair(tfull_bar(buf), static_cast<uint16_t>(0x3u << pair_leader));
                 else
                     umma_commit(tfull_bar(buf));
                 ++acc_count;
@@ -396,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // All issued MMAs complete before tensor memory is released.
             if constexpr (PAIR)
-                umma_commit_pair(drain_bar, 0x1);
+                umma_commit_pair(drain_bar, static_cast<uint16_t>(1u << crank));
             else
                 umma_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, p.timeout_ns, &never_abort))
@@ -408,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         uint32_t acc_count = 0;
         for (int w = unit0; w < total; w += unit_step) {
-            const Work wk = decode_work(p, w);
+            const Work wk = decode_work(p, w, q);
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
             const bool got = mbar_wait<PAIR>(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
@@ -446,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if constexpr (PAIR)
-                    mbar_arrive_cluster(tempty_bar(buf), 0);
+                    mbar_arrive_cluster(tempty_bar(buf), pair_leader);
                 else
                     mbar_arrive(tempty_bar(buf));
             }
@@ -537,11 +564,11 @@ struct ClusterCache {
     int max_clusters[64] = {0};
 };
 
-template <int IN_KIND, int BN, bool PAIR>
+template <int IN_KIND, int BN, bool PAIR, int MC>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const TcParams &p,
                         int ctas, cudaStream_t stream) {
-    using Cfg = TcCfg<IN_KIND, BN, PAIR>;
-    auto kern = gemm_tc_kernel<IN_KIND, BN, PAIR>;
+    using Cfg = TcCfg<IN_KIND, BN, PAIR, MC>;
+    auto kern = gemm_tc_kernel<IN_KIND, BN, PAIR, MC>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -555,7 +582,7 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
     cfg.numAttrs = 1;
     if constexpr (PAIR) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.x = Cfg::CLUSTER;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
@@ -569,15 +596,15 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
             maxc = (dev >= 0 && dev < 64) ? cache.max_clusters[dev] : 0;
         }
         if (maxc == 0) {
-            cfg.gridDim = dim3(2, 1, 1);
+            cfg.gridDim = dim3(Cfg::CLUSTER, 1, 1);
             if ((e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg)) != cudaSuccess) return e;
             if (maxc < 1) return cudaErrorInvalidConfiguration;
             std::lock_guard<std::mutex> lk(cache.mu);
             if (dev >= 0 && dev < 64) cache.max_clusters[dev] = maxc;
         }
-        int pairs = (ctas + 1) / 2;
-        if (pairs > maxc) pairs = maxc;
-        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        int clusters = (ctas + Cfg::CLUSTER - 1) / Cfg::CLUSTER;
+        if (clusters > maxc) clusters = maxc;
+        cfg.gridDim = dim3(Cfg::CLUSTER * clusters, 1, 1);
     } else {
         cfg.gridDim = dim3(ctas, 1, 1);
     }
@@ -586,23 +613,30 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
     return cudaGetLastError();
 }
 
-template <int IN_KIND, bool PAIR>
+template <int IN_KIND, bool PAIR, int MC>
 cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const TcParams &p, int ctas, cudaStream_t stream) {
-    if constexpr (PAIR) {
+    if constexpr (MC == 2) {
         switch (block_n) {
-        case 128: return launch_impl<IN_KIND, 128, true>(tmA, tmB, p, ctas, stream);
-        case 192: return launch_impl<IN_KIND, 192, true>(tmA, tmB, p, ctas, stream);
-        case 224: return launch_impl<IN_KIND, 224, true>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, true>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, true, 2>(tmA, tmB, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, true, 2>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, true, 2>(tmA, tmB, p, ctas, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    } else if constexpr (PAIR) {
+        switch (block_n) {
+        case 128: return launch_impl<IN_KIND, 128, true, 1>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, true, 1>(tmA, tmB, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, true, 1>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, true, 1>(tmA, tmB, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
     } else {
         switch (block_n) {
-        case 128: return launch_impl<IN_KIND, 128, false>(tmA, tmB, p, ctas, stream);
-        case 192: return launch_impl<IN_KIND, 192, false>(tmA, tmB, p, ctas, stream);
-        case 224: return launch_impl<IN_KIND, 224, false>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, false>(tmA, tmB, p, ctas, stream);
+        case 128: return launch_impl<IN_KIND, 128, false, 1>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, false, 1>(tmA, tmB, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, false, 1>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, false, 1>(tmA, tmB, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
     }
@@ -638,19 +672,27 @@ int tc_stages(int in_kind, int block_n, bool pair) {
     }
 }
 
-cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, const CUtensorMap &tmA,
+bool tc_supported_mc(int block_n, int mc) {
+    return mc == 1 || (mc == 2 && (block_n == 192 || block_n == 224 || block_n == 256));
+}
+
+cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream) {
+    if (mc == 2 && !pair) return cudaErrorInvalidValue;
     switch (in_kind) {
     case IN_F16:
-        return pair ? launch_kind<IN_F16, true>(block_n, tmA, tmB, p, ctas, stream)
-                    : launch_kind<IN_F16, false>(block_n, tmA, tmB, p, ctas, stream);
+        return mc == 2 ? launch_kind<IN_F16, true, 2>(block_n, tmA, tmB, p, ctas, stream)
+               : pair  ? launch_kind<IN_F16, true, 1>(block_n, tmA, tmB, p, ctas, stream)
+                       : launch_kind<IN_F16, false, 1>(block_n, tmA, tmB, p, ctas, stream);
     case IN_BF16:
-        return pair ? launch_kind<IN_BF16, true>(block_n, tmA, tmB, p, ctas, stream)
-                    : launch_kind<IN_BF16, false>(block_n, tmA, tmB, p, ctas, stream);
+        return mc == 2 ? launch_kind<IN_BF16, true, 2>(block_n, tmA, tmB, p, ctas, stream)
+               : pair  ? launch_kind<IN_BF16, true, 1>(block_n, tmA, tmB, p, ctas, stream)
+                       : launch_kind<IN_BF16, false, 1>(block_n, tmA, tmB, p, ctas, stream);
     case IN_TF32:
-        return pair ? launch_kind<IN_TF32, true>(block_n, tmA, tmB, p, ctas, stream)
-                    : launch_kind<IN_TF32, false>(block_n, tmA, tmB, p, ctas, stream);
+        return mc == 2 ? launch_kind<IN_TF32, true, 2>(block_n, tmA, tmB, p, ctas, stream)
+               : pair  ? launch_kind<IN_TF32, true, 1>(block_n, tmA, tmB, p, ctas, stream)
+                       : launch_kind<IN_TF32, false, 1>(block_n, tmA, tmB, p, ctas, stream);
     default: return cudaErrorInvalidValue;
     }
 }

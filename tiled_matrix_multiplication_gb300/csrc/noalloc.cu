@@ -159,13 +159,14 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     tp.group_m = plan.group_m;
     tp.out_kind = dtype_out == TG_F16 ? tg::OUT_F16 : (dtype_out == TG_BF16 ? tg::OUT_BF16 : tg::OUT_F32);
     tp.c_vector = plan.c_vector;
+    tp.mc = 1;
     tp.ldc = ldc;
     tp.c = c;
     tp.partial = plan.splits > 1 ? dev->scratch : nullptr;
     tp.status = dev->status;
     tp.timeout_ns = 2000ull * 1000000ull;
     const int in_kind = dtype_in == TG_F16 ? tg::IN_F16 : tg::IN_BF16;
-    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
+    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, 1, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
         return TG_ERR_CUDA;
     if (plan.splits > 1 &&
         tg::launch_splitk_reduce(dev->scratch, plan.splits, M, N, c, ldc, tp.out_kind,

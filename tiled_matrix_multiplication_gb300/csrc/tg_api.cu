@@ -98,7 +98,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
     if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36) || ldc > (int64_t(1) << 36))
         return TG_ERR_UNSUPPORTED;
     if (opt) {
-        if (opt->reserved) return TG_ERR_INVALID_VALUE;
+        if (opt->multicast < 0 || opt->multicast > 2) return TG_ERR_INVALID_VALUE;
+        if (opt->multicast == 2 &&
+            (opt->path == TG_PATH_TC || opt->path == TG_PATH_SKINNY || opt->splits > 1 ||
+             opt->tail_splits || (opt->block_n && !tg::tc_supported_mc(opt->block_n, 2))))
+            return TG_ERR_UNSUPPORTED;
         if (opt->tail_splits < 0 || opt->tail_splits == 1 || opt->tail_splits > 8)
             return TG_ERR_INVALID_VALUE;
         if (opt->path < TG_PATH_AUTO || opt->path > TG_PATH_SKINNY) return TG_ERR_INVALID_VALUE;
@@ -179,23 +183,29 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // for 128 rows, less for fewer rows).  Ties go to the earlier candidate.
     // Relative efficiencies (percent of the best variant) measured on GB300 at
     // 8192^3 and on the prefill shapes.
-    struct Cand { bool pair; int bn; int eff; };
+    // mc = 2: clusters of two pairs sharing A by multicast (two tiles per unit).
+    struct Cand { bool pair; int mc; int bn; int eff; };
     static const Cand kCands[] = {
-        {true, 256, 100}, {true, 224, 94}, {true, 192, 90}, {false, 256, 91},
-        {false, 192, 85}, {false, 224, 82}, {true, 128, 65}, {false, 128, 66}};
+        {true, 2, 256, 106}, {true, 2, 224, 100}, {true, 2, 192, 96},
+        {true, 1, 256, 100}, {true, 1, 224, 94}, {true, 1, 192, 90}, {false, 1, 256, 91},
+        {false, 1, 192, 85}, {false, 1, 224, 82}, {true, 1, 128, 65}, {false, 1, 128, 66}};
     double best_cost = -1.0;
     for (const Cand &cd : kCands) {
         if (opt && opt->path == TG_PATH_TC && cd.pair) continue;
         if (opt && opt->path == TG_PATH_TC_PAIR && !cd.pair) continue;
         if (opt && opt->block_n && opt->block_n != cd.bn) continue;
-        if (cd.pair && cap < 2) continue;
+        if (cd.pair && cap < 2 * cd.mc) continue;
+        if (opt && opt->multicast && opt->multicast != cd.mc) continue;
+        if (cd.mc == 2 && ((opt && (opt->splits > 1 || opt->tail_splits)) || din == TG_F32))
+            continue;
         const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
-        const int64_t slots = std::max<int64_t>(1, cd.pair ? cap / 2 : cap);
-        const int64_t tiles = cdiv(M, tile_m) * cdiv(N, cd.bn);
+        const int64_t slots = std::max<int64_t>(1, cd.pair ? cap / (2 * cd.mc) : cap);
+        // work units: tiles, or pairs of horizontally adjacent tiles
+        const int64_t tiles = cdiv(M, tile_m) * cdiv(cdiv(N, cd.bn), cd.mc);
         int64_t s_lo = 1, s_hi = 1;
         if (opt && opt->splits) {
             s_lo = s_hi = opt->splits;
-        } else if (tiles < slots / 2) {
+        } else if (tiles < slots / 2 && cd.mc == 1) {
             s_hi = std::min<int64_t>(pl->k_tiles, 16);   // too few tiles: consider split K
         }
         for (int64_t s = s_lo; s <= s_hi; ++s) {
@@ -223,6 +233,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
                 p.path = cd.pair ? TG_PATH_TC_PAIR : TG_PATH_TC;
                 p.block_m = static_cast<int32_t>(tile_m);
                 p.block_n = cd.bn;
+                p.multicast = cd.mc;
                 pl->k_per_split = kps;
                 p.splits = static_cast<int32_t>(se);
                 p.tiles = tiles;
@@ -285,12 +296,14 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     pl->tiles_m = cdiv(M, p.block_m);
     pl->tiles_n = cdiv(N, p.block_n);
     const int64_t splits = p.splits;
-    const int64_t units = p.tiles * splits;
+    const int64_t units = p.tiles * splits;   // (tiles = work units: tile pairs when mc = 2)
     if (p.path == TG_PATH_SKINNY) {
         p.ctas = static_cast<int32_t>(units);   // not persistent: one CTA per unit
+        p.multicast = 1;
     } else if (pair) {
-        const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(units, cap / 2));
-        p.ctas = static_cast<int32_t>(2 * pairs);
+        const int64_t cl = 2 * std::max(p.multicast, 1);
+        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, cap / cl));
+        p.ctas = static_cast<int32_t>(cl * clusters);
     } else {
         p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
     }
@@ -532,7 +545,9 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     const tg_status sb = p.pack_b == 2
                              ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
                              : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k);
-    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, kBlockM) != TG_OK || sb != TG_OK)
+    // with A multicast each CTA loads half of its 128 rows of A
+    const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
+    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_rows) != TG_OK || sb != TG_OK)
         return fail(TG_ERR_CUDA);
 
     tg::TcParams tp;
@@ -548,6 +563,7 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     tp.group_m = p.group_m;
     tp.out_kind = out_kind_of(dtype_out);
     tp.c_vector = p.c_vector;
+    tp.mc = std::max(p.multicast, 1);
     tp.ldc = ldc;
     tp.c = c;
     tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
@@ -564,8 +580,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         st = cuda_status(cudaMemsetAsync(tp.tail_count, 0, cnt_bytes, s));
         if (st != TG_OK) return fail(st);
     }
-    st = cuda_status(
-        tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair, tmA, tmB, tp, p.ctas, s));
+    st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair,
+                                        std::max(p.multicast, 1), tmA, tmB, tp, p.ctas, s));
     if (st != TG_OK) return fail(st);
     if (p.splits > 1) {
         st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,

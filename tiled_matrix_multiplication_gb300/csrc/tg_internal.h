@@ -25,7 +25,7 @@ struct TcParams {
     int32_t group_m;            // grouped raster height (tiles)
     int32_t out_kind;           // OutKind of C
     int32_t c_vector;           // C base and row pitch allow 16-byte stores
-    int32_t pad_;
+    int32_t mc;                 // tiles per work unit (2: two pairs share A by multicast)
     int64_t ldc;                // elements
     void *c;
     float *partial;             // [splits][M][N] when splits > 1
@@ -69,10 +69,12 @@ cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &t
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream);
 
 // gemm_tc.cu
-// `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `ctas` counts CTAs.
+// `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `mc` = 2: clusters
+// of two pairs sharing A by multicast (pair only); `ctas` counts CTAs.
 int tc_stages(int in_kind, int block_n, bool pair);
 bool tc_supported_block_n(int block_n, bool pair);
-cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, const CUtensorMap &tmA,
+bool tc_supported_mc(int block_n, int mc);
+cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);
 cudaError_t status_word_address(int **out);
