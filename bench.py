@@ -316,10 +316,20 @@ def run_ours(args, world, rank, local):
     plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count)
     code_in, code_out = tg.dtype_code(din), tg.dtype_code(dout)
 
+    opts = dict(kv.split("=") for kv in args.opt)
+    opts = {k: int(v) for k, v in opts.items()}
+    topt = tg.make_options(**opts) if opts else None
+    if opts:
+        plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count, **opts)
+
     def step(i):
         a, b, c = sets[i % R]
-        st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
-                        code_in, code_out, sh)
+        if topt is None:
+            st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                            code_in, code_out, sh)
+        else:
+            st = tg.tg_gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                               code_in, code_out, sh, topt)
         if st != tg.TG_OK:
             raise tg.TgError(st, "tg_gemm")
 
@@ -422,7 +432,8 @@ def run_ours(args, world, rank, local):
                    "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2 {l2 / 1e6:.0f} MB)",
                    "tile": f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}",
-                   "splits": plan["splits"], "ctas": plan["ctas"]},
+                   "splits": plan["splits"], "ctas": plan["ctas"],
+                   "multicast": plan["multicast"], "options": opts or None},
         "pct_of_peak": round(100.0 * value / world / peak, 2) if not skinny else None,
         "clocks": clocks,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -451,6 +462,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
+                    help="planner override passed to tg_gemm_ex (tg_options field), e.g. "
+                         "multicast=1; repeatable")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
