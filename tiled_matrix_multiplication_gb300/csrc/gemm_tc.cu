@@ -86,7 +86,12 @@ struct TcCfg {
     static constexpr int ESIZE = IN_KIND == IN_TF32 ? 4 : 2;
     static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
     static constexpr int UMMA_K = 32 / ESIZE;     // K of one tcgen05.mma
-    static constexpr int CHUNK_N = 128 / ESIZE;   // N elements in one 128-byte B row
+    // N-major B: rows of B_SW bytes, the widest swizzle (128, 64 or 32 bytes)
+    // whose row divides the columns this CTA stages, so no box runs past them.
+    static constexpr int BN_CTA_ = PAIR ? BN / 2 : BN;
+    static constexpr int B_SW = (BN_CTA_ * ESIZE) % 128 == 0 ? 128
+                              : ((BN_CTA_ * ESIZE) % 64 == 0 ? 64 : 32);
+    static constexpr int CHUNK_N = B_SW / ESIZE;  // N elements in one B row of a box
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
     static constexpr int CTA_GROUP = PAIR ? 2 : 1;
     static constexpr int CLUSTER = CTA_GROUP * MC;      // CTAs per cluster
@@ -99,10 +104,9 @@ struct TcCfg {
     // produced all-zero results with kind::tf32 on this hardware.
     static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
     static constexpr int A_STAGE = CTA_M * 128;   // bytes
-    static constexpr int B_BOX = BK * 128;        // one CHUNK_N-wide N-major TMA box
-    static constexpr int B_CHUNKS = (BN_CTA + CHUNK_N - 1) / CHUNK_N;
-    // N-major: whole 128-byte chunks (the last one may run past BN_CTA);
-    // K-major: BN_CTA rows of 128 bytes.
+    static constexpr int B_BOX = BK * B_SW;       // one CHUNK_N-wide N-major TMA box
+    static constexpr int B_CHUNKS = BN_CTA / CHUNK_N;
+    // N-major: B_CHUNKS boxes; K-major (TF32): BN_CTA rows of 128 bytes.
     static constexpr int B_STAGE = B_KMAJOR ? BN_CTA * 128 : B_CHUNKS * B_BOX;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
     static constexpr int TX_BYTES = STAGE_BYTES * CTA_GROUP;   // per full-barrier phase
@@ -116,6 +120,7 @@ struct TcCfg {
                    B_KMAJOR ? 0u : 1u, TILE_M, BN);
     static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
     static_assert(BN_CTA % 16 == 0, "each CTA stages whole 16-column groups of B");
+    static_assert(B_KMAJOR || BN_CTA % CHUNK_N == 0, "B boxes tile the CTA's columns");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -397,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd =
                             Cfg::B_KMAJOR
                                 ? smem_desc_sw128(b0 + kk * 32, 16, 1024)
-                                : smem_desc_sw128(b0 + kk * Cfg::UMMA_K * 128, Cfg::B_BOX, 1024);
+                                : smem_desc_mn<Cfg::B_SW>(b0 + kk * Cfg::UMMA_K * Cfg::B_SW,
+                                                          Cfg::B_BOX);
                         umma_ss<Cfg::KIND, CG>(d_tmem, ad, bd, Cfg::IDESC,
                                                (kt > wk.kt0 || kk > 0) ? 1u : 0u);
                     }
@@ -670,6 +676,12 @@ int tc_stages(int in_kind, int block_n, bool pair) {
         return pair ? stages_kind<IN_TF32, true>(block_n) : stages_kind<IN_TF32, false>(block_n);
     default: return 0;
     }
+}
+
+int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair) {
+    const int es = in_kind == IN_TF32 ? 4 : 2;
+    const int cols = pair ? block_n / 2 : block_n;
+    return (cols * es) % 128 == 0 ? 128 : ((cols * es) % 64 == 0 ? 64 : 32);
 }
 
 bool tc_supported_mc(int block_n, int mc) {

@@ -412,15 +412,20 @@ CUtensorMapDataType tma_type(tg_dtype t) {
 }
 
 // Row-major [rows, cols] with pitch `ld` elements; boxes of box_cols x box_rows
-// (box_cols * esize == 128 bytes), 128-byte swizzle, zero fill out of range.
+// whose rows (box_cols * esize bytes = 128, 64 or 32) are swizzled at that
+// size; zero fill out of range.
 tg_status encode_2d(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
                     int64_t ld, int box_cols, int box_rows) {
+    const int row_bytes = box_cols * esize_of(t);
+    const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esize_of(t))};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, tma_type(t), 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
 }
@@ -542,9 +547,10 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     }
     const bool pair = p.path == TG_PATH_TC_PAIR;
     const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
+    const int b_chunk = tg::tc_b_swizzle_bytes(in_kind_of(dtype_in), p.block_n, pair) / ei;
     const tg_status sb = p.pack_b == 2
                              ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
-                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k);
+                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, b_chunk, p.block_k);
     // with A multicast each CTA loads half of its 128 rows of A
     const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
     if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_rows) != TG_OK || sb != TG_OK)

@@ -74,6 +74,8 @@ cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &t
 int tc_stages(int in_kind, int block_n, bool pair);
 bool tc_supported_block_n(int block_n, bool pair);
 bool tc_supported_mc(int block_n, int mc);
+// Swizzle (row bytes of a TMA box) of the N-major B tile of a variant.
+int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair);
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);

@@ -398,6 +398,25 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Swizzle-mode field of the descriptor for rows of `bytes` (128, 64, 32).
+__host__ __device__ constexpr uint64_t desc_swizzle_mode(int bytes) {
+    return bytes == 128 ? 2ull : (bytes == 64 ? 4ull : 6ull);
+}
+
+// MN-major operand with `sw`-byte swizzled rows (sw = 128, 64 or 32): each
+// TMA box holds `sw` bytes of MN for every K row; boxes follow each other at
+// `lbo_bytes`; 8-row K groups are 8*sw bytes apart.
+template <int SW>
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t lbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(((8u * SW) >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= desc_swizzle_mode(SW) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an FP32 accumulator:
 //   [4,6) D format (1 = F32)   [7,10) A format   [10,13) B format
 //   (kind::f16: 0 = F16, 1 = BF16; kind::tf32: 2 = TF32)
