@@ -182,7 +182,7 @@ def test_tail_split_exact(path, block_n, max_ctas, M, N, K):
                        max_ctas=max_ctas, ldc=N + 4, tail_splits=3)
     compare(a, b, c, M, N, K, "bf16", "f32")
     assert padding_untouched(c, N, "f32")
-    return p
+    assert p["tail_tiles"] >= 0
 
 
 def test_tail_split_is_exercised():

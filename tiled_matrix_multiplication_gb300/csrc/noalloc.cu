@@ -94,6 +94,10 @@ tg_status setup_current_device(NoAllocDevice **out) {
 tg_status encode(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
                  int64_t ld, int box_cols, int box_rows) {
     const int es = t == TG_F32 ? 4 : 2;
+    const int row_bytes = box_cols * es;
+    const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
@@ -101,12 +105,14 @@ tg_status encode(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, in
     const CUtensorMapDataType dt =
         t == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = g_encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int in_kind_of_noalloc(tg_dtype t) { return t == TG_F16 ? tg::IN_F16 : tg::IN_BF16; }
 
 }  // namespace
 
@@ -144,7 +150,9 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     const int64_t kps = cdiv(k_tiles, splits);
     CUtensorMap tmA, tmB;
     if (encode(&tmA, dtype_in, a, M, K, lda, plan.block_k, plan.block_m) != TG_OK ||
-        encode(&tmB, dtype_in, b, K, N, ldb, 64, plan.block_k) != TG_OK)
+        encode(&tmB, dtype_in, b, K, N, ldb,
+               tg::tc_b_swizzle_bytes(in_kind_of_noalloc(dtype_in), plan.block_n, false) / 2,
+               plan.block_k) != TG_OK)
         return TG_ERR_CUDA;
     tg::TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
