@@ -86,11 +86,11 @@ struct TcCfg {
     static constexpr int ESIZE = IN_KIND == IN_TF32 ? 4 : 2;
     static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
     static constexpr int UMMA_K = 32 / ESIZE;     // K of one tcgen05.mma
-    // N-major B: rows of B_SW bytes, the widest swizzle (128, 64 or 32 bytes)
-    // whose row divides the columns this CTA stages, so no box runs past them.
+    // N-major B: 128-byte swizzled rows, or 64-byte ones when those tile the
+    // CTA's columns exactly and 128-byte ones do not (96 columns per CTA); 32-byte
+    // rows measured much slower than loading a partly unused 128-byte box.
     static constexpr int BN_CTA_ = PAIR ? BN / 2 : BN;
-    static constexpr int B_SW = (BN_CTA_ * ESIZE) % 128 == 0 ? 128
-                              : ((BN_CTA_ * ESIZE) % 64 == 0 ? 64 : 32);
+    static constexpr int B_SW = ((BN_CTA_ * ESIZE) % 128 != 0 && (BN_CTA_ * ESIZE) % 64 == 0) ? 64 : 128;
     static constexpr int CHUNK_N = B_SW / ESIZE;  // N elements in one B row of a box
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : 0;
     static constexpr int CTA_GROUP = PAIR ? 2 : 1;
@@ -105,7 +105,7 @@ struct TcCfg {
     static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
     static constexpr int A_STAGE = CTA_M * 128;   // bytes
     static constexpr int B_BOX = BK * B_SW;       // one CHUNK_N-wide N-major TMA box
-    static constexpr int B_CHUNKS = BN_CTA / CHUNK_N;
+    static constexpr int B_CHUNKS = (BN_CTA + CHUNK_N - 1) / CHUNK_N;   // last may run past
     // N-major: B_CHUNKS boxes; K-major (TF32): BN_CTA rows of 128 bytes.
     static constexpr int B_STAGE = B_KMAJOR ? BN_CTA * 128 : B_CHUNKS * B_BOX;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
@@ -120,7 +120,6 @@ struct TcCfg {
                    B_KMAJOR ? 0u : 1u, TILE_M, BN);
     static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
     static_assert(BN_CTA % 16 == 0, "each CTA stages whole 16-column groups of B");
-    static_assert(B_KMAJOR || BN_CTA % CHUNK_N == 0, "B boxes tile the CTA's columns");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -681,7 +680,49 @@ int tc_stages(int in_kind, int block_n, bool pair) {
 int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair) {
     const int es = in_kind == IN_TF32 ? 4 : 2;
     const int cols = pair ? block_n / 2 : block_n;
-    return (cols * es) % 128 == 0 ? 128 : ((cols * es) % 64 == 0 ? 64 : 32);
+    return ((cols * es) % 128 != 0 && (cols * es) % 64 == 0) ? 64 : 128;
+}
+
+int tc_max_clusters(int cluster_size) {
+    // Clusters of 2 or 4 CTAs of the widest-stage kernel that fit at once
+    // (every variant of the kernel takes one CTA per SM, so the count is the
+    // same for all of them).
+    static std::mutex mu;
+    static int cache[64][2];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int slot = cluster_size == 4 ? 1 : 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev][slot] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(cluster_size, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        int n = 0;
+        if (cluster_size == 4) {
+            using Cfg = TcCfg<IN_F16, 256, true, 2>;
+            auto kern = gemm_tc_kernel<IN_F16, 256, true, 2>;
+            cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            if (set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES) != cudaSuccess ||
+                cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+                return 0;
+        } else {
+            using Cfg = TcCfg<IN_F16, 256, true, 1>;
+            auto kern = gemm_tc_kernel<IN_F16, 256, true, 1>;
+            cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            if (set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES) != cudaSuccess ||
+                cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+                return 0;
+        }
+        cache[dev][slot] = n;
+    }
+    return cache[dev][slot];
 }
 
 bool tc_supported_mc(int block_n, int mc) {

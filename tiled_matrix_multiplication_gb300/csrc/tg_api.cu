@@ -28,6 +28,7 @@ struct DeviceState {
     // the next one instead of being unmapped and mapped again; the process's
     // default pool is left untouched.
     cudaMemPool_t pool = nullptr;
+    int pair_slots = 0, quad_slots = 0;   // resident clusters of 2 / 4 CTAs
 };
 
 std::mutex g_mu;
@@ -161,9 +162,11 @@ int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles, int64_t wa
     return std::max<int64_t>(ts, 1);
 }
 
+// `pair_slots` / `quad_slots`: clusters of 2 / 4 CTAs resident at once
+// (0: estimate from the SM count).
 void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
-               const tg_options *opt, Plan *pl) {
+               const tg_options *opt, Plan *pl, int pair_slots = 0, int quad_slots = 0) {
     tg_plan &p = pl->pub;
     std::memset(&p, 0, sizeof(p));
     const int ei = esize_of(din), eo = esize_of(dout);
@@ -186,9 +189,9 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // mc = 2: clusters of two pairs sharing A by multicast (two tiles per unit).
     struct Cand { bool pair; int mc; int bn; int eff; };
     static const Cand kCands[] = {
-        {true, 2, 256, 106}, {true, 2, 224, 100}, {true, 2, 192, 96},
-        {true, 1, 256, 100}, {true, 1, 224, 94}, {true, 1, 192, 90}, {false, 1, 256, 91},
-        {false, 1, 192, 85}, {false, 1, 224, 82}, {true, 1, 128, 65}, {false, 1, 128, 66}};
+        {true, 2, 256, 105}, {true, 1, 256, 100}, {true, 2, 224, 90}, {true, 2, 192, 86},
+        {true, 1, 224, 92}, {true, 1, 192, 84}, {false, 1, 256, 90},
+        {false, 1, 192, 82}, {false, 1, 224, 80}, {true, 1, 128, 62}, {false, 1, 128, 62}};
     double best_cost = -1.0;
     for (const Cand &cd : kCands) {
         if (opt && opt->path == TG_PATH_TC && cd.pair) continue;
@@ -199,7 +202,15 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         if (cd.mc == 2 && ((opt && (opt->splits > 1 || opt->tail_splits)) || din == TG_F32))
             continue;
         const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
-        const int64_t slots = std::max<int64_t>(1, cd.pair ? cap / (2 * cd.mc) : cap);
+        // resident clusters: 4-CTA clusters can leave SMs of a GPC unused
+        int64_t resident = cap;
+        if (cd.pair) {
+            // without a device: 4-CTA clusters measured at 36 on 152 SMs
+            const int64_t est = cd.mc == 2 ? (quad_slots ? quad_slots : num_sms * 19 / 80)
+                                           : (pair_slots ? pair_slots : num_sms / 2);
+            resident = std::min<int64_t>(cap / (2 * cd.mc), est);
+        }
+        const int64_t slots = std::max<int64_t>(1, resident);
         // work units: tiles, or pairs of horizontally adjacent tiles
         const int64_t tiles = cdiv(M, tile_m) * cdiv(cdiv(N, cd.bn), cd.mc);
         int64_t s_lo = 1, s_hi = 1;
@@ -398,6 +409,8 @@ tg_status device_state(DeviceState **out) {
             uint64_t keep = ~0ull;
             if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
                 return TG_ERR_CUDA;
+            d.pair_slots = tg::tc_max_clusters(2);
+            d.quad_slots = tg::tc_max_clusters(4);
         }
         d.init = true;
     }
@@ -490,7 +503,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         return cuda_status(cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s));
 
     Plan pl;
-    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl);
+    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl,
+              dev->pair_slots, dev->quad_slots);
     const tg_plan &p = pl.pub;
     const int ei = esize_of(dtype_in);
 

@@ -76,6 +76,9 @@ bool tc_supported_block_n(int block_n, bool pair);
 bool tc_supported_mc(int block_n, int mc);
 // Swizzle (row bytes of a TMA box) of the N-major B tile of a variant.
 int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair);
+// Clusters of `cluster_size` (2 or 4) CTAs of the pair kernel resident at
+// once on the current device (0 if the query fails).
+int tc_max_clusters(int cluster_size);
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);
