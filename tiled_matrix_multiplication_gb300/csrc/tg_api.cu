@@ -313,7 +313,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         p.multicast = 1;
     } else if (pair) {
         const int64_t cl = 2 * std::max(p.multicast, 1);
-        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, cap / cl));
+        int64_t resident = cap / cl;
+        if (p.multicast == 2) resident = std::min<int64_t>(resident, quad_slots ? quad_slots : num_sms * 19 / 80);
+        else resident = std::min<int64_t>(resident, pair_slots ? pair_slots : num_sms / 2);
+        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, resident));
         p.ctas = static_cast<int32_t>(cl * clusters);
     } else {
         p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(units, cap)));
