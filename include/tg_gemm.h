@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 1
+#define TG_ABI_VERSION 2
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -119,7 +119,9 @@ typedef struct tg_plan {
     int32_t tail_tiles;    /* last tiles split over K to balance the last wave */
     int32_t tail_splits;   /* K ranges per tail tile (partials summed in-kernel) */
     int32_t multicast;     /* tiles per cluster sharing A (1 or 2) */
-    int32_t reserved;
+    int32_t per_batch;     /* strided batches only: 1 if each product of the batch
+                              is run as its own call (kernels counts them all), 0
+                              if one launch covers every product */
 } tg_plan;
 
 /*
@@ -160,6 +162,59 @@ tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K,
                        const void *c, int64_t ldc,
                        tg_dtype dtype_in, tg_dtype dtype_out,
                        int32_t num_sms, const tg_options *opt, tg_plan *plan);
+
+/*
+ * tg_gemm_strided_batched -- `batch` independent products
+ *
+ *     C_z = A_z * B_z,   A_z = a + z*stride_a,  B_z = b + z*stride_b,
+ *                        C_z = c + z*stride_c,  0 <= z < batch
+ *
+ * each of them exactly the operation of tg_gemm (same sizes M, N, K, leading
+ * dimensions, types and rounding).  This is the batched extension of the tiled
+ * multiply with a third grid axis over the batch ("Triton tiled matmul",
+ * llm-systems-cookbook, section "Exercises", item 3): the kernels treat the
+ * batch index as the slowest dimension of their work list, and A / B are read
+ * through rank-3 TMA tensor maps.
+ *
+ *   batch              number of products (>= 0; 0 does nothing)
+ *   stride_a/b/c       distance in ELEMENTS between consecutive products' A, B,
+ *                      C (>= 0).  stride_a == 0 (or stride_b == 0) uses one A
+ *                      (one B) for every product.  C of different products
+ *                      must not overlap: stride_c >= (M-1)*ldc + N (stacked
+ *                      products), or stride_c >= N with
+ *                      (batch-1)*stride_c + N <= ldc (products interleaved
+ *                      along a row, C stored [M][batch][N]); else
+ *                      TG_ERR_INVALID_VALUE.  The whole of C (all products)
+ *                      must not overlap the whole of A or of B.
+ *   opt                as for tg_gemm_ex; with batch > 1, opt->splits > 1 is
+ *                      only accepted with opt->path == TG_PATH_SKINNY (the
+ *                      on-chip K split), and opt->tail_splits is unsupported.
+ *
+ * One launch covers every product when the operands are 16-bit, A and B are
+ * 16-byte aligned with 16-byte row pitches and 16-byte batch strides.
+ * Otherwise (TF32 operands, misaligned A or B) each product is run as its own
+ * tg_gemm_ex call on `stream`, in order of z.  Ownership, asynchrony and error
+ * behaviour as for tg_gemm; batch > 2^31-1 or more than 2^30 output tiles in
+ * all return TG_ERR_UNSUPPORTED.
+ */
+tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                  const void *a, int64_t lda, int64_t stride_a,
+                                  const void *b, int64_t ldb, int64_t stride_b,
+                                  void *c, int64_t ldc, int64_t stride_c,
+                                  tg_dtype dtype_in, tg_dtype dtype_out,
+                                  void *stream, const tg_options *opt);
+
+/*
+ * tg_plan_gemm_strided_batched -- host only, like tg_plan_gemm: validates as
+ * tg_gemm_strided_batched does and fills *plan with what it would launch on a
+ * device with `num_sms` SMs (tiles counts the tiles of all products).
+ */
+tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                       const void *a, int64_t lda, int64_t stride_a,
+                                       const void *b, int64_t ldb, int64_t stride_b,
+                                       const void *c, int64_t ldc, int64_t stride_c,
+                                       tg_dtype dtype_in, tg_dtype dtype_out,
+                                       int32_t num_sms, const tg_options *opt, tg_plan *plan);
 
 /* Static, human-readable name of a status code. */
 const char *tg_status_string(tg_status status);

@@ -9,8 +9,9 @@ streams: every step of the multiply runs in the library's CUDA kernels.
     c = tg.gemm(a, b, out_dtype=torch.float32)
 
 The raw C entry points are re-exported under their C names (``tg_gemm``,
-``tg_gemm_ex``, ``tg_plan_gemm``, ``tg_status_string``, ``tg_last_device_error``,
-``tg_abi_version``) with pointers and streams passed as integers.
+``tg_gemm_ex``, ``tg_plan_gemm``, ``tg_gemm_strided_batched``, ...) with pointers
+and streams passed as integers.  ``bmm`` runs a batch of products
+([B, M, K] @ [B, K, N], either side may be a shared 2-D matrix).
 """
 from __future__ import annotations
 
@@ -19,13 +20,15 @@ from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_ERR_ARCH, TG_ERR_
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
                    TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, NOALLOC_SCRATCH_BYTES, TgError,
                    load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
-                   tg_gemm_splitk_noalloc, tg_last_device_error, tg_options, tg_plan,
-                   tg_plan_gemm, tg_status_string)
+                   tg_gemm_splitk_noalloc, tg_gemm_strided_batched, tg_last_device_error,
+                   tg_options, tg_plan, tg_plan_gemm, tg_plan_gemm_strided_batched,
+                   tg_status_string)
 
 __all__ = [
-    "gemm", "plan", "check_device_error", "dtype_code", "TgError", "load", "make_options",
+    "gemm", "bmm", "plan", "plan_batched", "check_device_error", "dtype_code", "TgError", "load", "make_options",
     "tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string", "tg_last_device_error",
-    "tg_abi_version", "tg_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
+    "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",
+    "tg_plan_gemm_strided_batched", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
     "EXPORTS", "LIB_PATH",
     "TG_F16", "TG_BF16", "TG_F32", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
     "TG_ERR_OUT_OF_MEMORY", "TG_ERR_CUDA", "TG_ERR_ARCH", "TG_ERR_TIMEOUT",
@@ -87,6 +90,77 @@ def gemm(a, b, out_dtype=None, out=None, stream=None, **options):
     if st != TG_OK:
         raise TgError(st, f"tg_gemm_ex(M={M}, N={N}, K={K})")
     return out
+
+
+def _batch_stride(t, dims: int) -> int:
+    """Element stride between the products of a [B, rows, cols] tensor (0 for 2-D)."""
+    return 0 if t.dim() == dims - 1 else (t.stride(0) if t.shape[0] > 1 else 0)
+
+
+def bmm(a, b, out_dtype=None, out=None, stream=None, **options):
+    """C[z] = A[z] @ B[z] through ``tg_gemm_strided_batched``.
+
+    ``a`` is [B, M, K] or a shared [M, K]; ``b`` is [B, K, N] or a shared
+    [K, N] (at least one of them 3-D), same dtype, unit column stride.  The
+    result is a new [B, M, N] tensor of ``out_dtype`` (default: the input
+    dtype), or ``out`` with unit column stride.  Raises ``ValueError`` on a
+    shape mismatch and ``TgError`` on any status other than TG_OK.
+    """
+    import torch
+    if a.dim() not in (2, 3) or b.dim() not in (2, 3) or (a.dim() == 2 and b.dim() == 2):
+        raise ValueError("bmm expects [B, M, K] or [M, K] times [B, K, N] or [K, N]")
+    if a.dtype != b.dtype:
+        raise ValueError("A and B must have the same dtype")
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    batch = a.shape[0] if a.dim() == 3 else b.shape[0]
+    if (a.dim() == 3 and a.shape[0] != batch) or (b.dim() == 3 and b.shape[0] != batch):
+        raise ValueError("batch sizes differ")
+    M, K = a.shape[-2], a.shape[-1]
+    N = b.shape[-1]
+    if b.shape[-2] != K:
+        raise ValueError("inner dimensions differ")
+    if (a.stride(-1) != 1 and K > 1) or (b.stride(-1) != 1 and N > 1):
+        raise ValueError("A and B need unit column stride")
+    out_dtype = a.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=out_dtype, device=a.device)
+    elif (out.shape != (batch, M, N) or out.dtype != out_dtype or
+          (out.stride(-1) != 1 and N > 1)):
+        raise ValueError("out must be [B, M, N] of out_dtype with unit column stride")
+    lda = a.stride(-2) if M > 1 else max(K, 1)
+    ldb = b.stride(-2) if K > 1 else max(N, 1)
+    ldc = out.stride(-2) if M > 1 else max(N, 1)
+    sc = out.stride(0) if batch > 1 else (M - 1) * ldc + N
+    opt = make_options(**options) if options else None
+    with torch.cuda.device(a.device):
+        st = tg_gemm_strided_batched(batch, M, N, K, a.data_ptr(), lda, _batch_stride(a, 3),
+                                     b.data_ptr(), ldb, _batch_stride(b, 3), out.data_ptr(), ldc,
+                                     sc, dtype_code(a.dtype), dtype_code(out_dtype),
+                                     _stream_handle(stream), opt)
+    if st != TG_OK:
+        raise TgError(st, f"tg_gemm_strided_batched(batch={batch}, M={M}, N={N}, K={K})")
+    return out
+
+
+def plan_batched(batch, M, N, K, dtype_in="f16", dtype_out=None, num_sms=148, stride_a=None,
+                 stride_b=None, stride_c=None, lda=None, ldb=None, ldc=None, a=0x1000,
+                 b=0x10000000000, c=0x20000000000, **options) -> dict:
+    """What ``tg_gemm_strided_batched`` would launch (host only, no GPU); the
+    default strides are those of contiguous [B, rows, cols] operands."""
+    dtype_out = dtype_in if dtype_out is None else dtype_out
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    sa = M * lda if stride_a is None else stride_a
+    sb = K * ldb if stride_b is None else stride_b
+    sc = M * ldc if stride_c is None else stride_c
+    opt = make_options(**options) if options else None
+    st, p = tg_plan_gemm_strided_batched(batch, M, N, K, a, lda, sa, b, ldb, sb, c, ldc, sc,
+                                         dtype_in, dtype_out, num_sms, opt)
+    if st != TG_OK:
+        raise TgError(st, "tg_plan_gemm_strided_batched")
+    return p
 
 
 def plan(M, N, K, dtype_in="f16", dtype_out=None, num_sms=148, lda=None, ldb=None, ldc=None,

@@ -29,7 +29,8 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 
 # Every extern "C" symbol the header declares.
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
-           "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc")
+           "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
+           "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched")
 
 # Bytes of the library-owned partial-tile array of tg_gemm_splitk_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -51,7 +52,7 @@ class tg_plan(ctypes.Structure):
                 ("c_vector", ctypes.c_int32), ("kernels", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("tail_tiles", ctypes.c_int32), ("tail_splits", ctypes.c_int32),
-                ("multicast", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("multicast", ctypes.c_int32), ("per_batch", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -97,6 +98,13 @@ def load(path: str | None = None):
         lib.tg_abi_version.restype = i32
         lib.tg_gemm_splitk_noalloc.argtypes = gemm_args[:-1] + [i32, vp]
         lib.tg_gemm_splitk_noalloc.restype = ctypes.c_int
+        batched = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, ctypes.c_int,
+                   ctypes.c_int]
+        lib.tg_gemm_strided_batched.argtypes = batched + [vp, ctypes.POINTER(tg_options)]
+        lib.tg_gemm_strided_batched.restype = ctypes.c_int
+        lib.tg_plan_gemm_strided_batched.argtypes = batched + [i32, ctypes.POINTER(tg_options),
+                                                               ctypes.POINTER(tg_plan)]
+        lib.tg_plan_gemm_strided_batched.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -163,3 +171,25 @@ def tg_gemm_splitk_noalloc(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out,
     splits * M * N * 4 exceeds the array, for misaligned operands or TF32)."""
     return int(load().tg_gemm_splitk_noalloc(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
                                              _code(dtype_out), splits, stream))
+
+
+def tg_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc, stride_c,
+                            dtype_in, dtype_out, stream, options=None) -> int:
+    """``batch`` products C_z = A_z B_z whose operands start ``stride_*`` elements
+    apart (0 = one operand shared by all).  Returns the tg_status."""
+    opt = ctypes.byref(options) if options is not None else None
+    return int(load().tg_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b,
+                                              c, ldc, stride_c, _code(dtype_in),
+                                              _code(dtype_out), stream, opt))
+
+
+def tg_plan_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc,
+                                 stride_c, dtype_in, dtype_out, num_sms, options=None):
+    """Returns ``(status, plan_dict)``; host only, needs no GPU."""
+    plan = tg_plan()
+    opt = ctypes.byref(options) if options is not None else None
+    st = int(load().tg_plan_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb,
+                                                 stride_b, c, ldc, stride_c, _code(dtype_in),
+                                                 _code(dtype_out), num_sms, opt,
+                                                 ctypes.byref(plan)))
+    return st, plan.as_dict()

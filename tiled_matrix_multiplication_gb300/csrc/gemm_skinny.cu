@@ -76,7 +76,8 @@ struct SkCfg {
 };
 
 __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float v) {
-    const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+    const int64_t off = static_cast<int64_t>(blockIdx.y) * p.stride_c +   // batch
+                        static_cast<int64_t>(m) * p.ldc + n;
     if (p.out_kind == OUT_F32)
         static_cast<float *>(p.c)[off] = v;
     else if (p.out_kind == OUT_F16)
@@ -157,11 +158,19 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                 }
                 mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
                 const uint32_t fb = full_bar(stage);
-                tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
+                const int z = static_cast<int>(blockIdx.y);   // batch
+                if (p.a_batched)
+                    tma_load_3d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0, z);
+                else
+                    tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
 #pragma unroll
-                for (int j = 0; j < NT / Cfg::CHUNK_N; ++j)
-                    tma_load_2d(sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX, &tmB, fb,
-                                tn * NT + j * Cfg::CHUNK_N, kt * Cfg::BK);
+                for (int j = 0; j < NT / Cfg::CHUNK_N; ++j) {
+                    const uint32_t dst = sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX;
+                    if (p.b_batched)
+                        tma_load_3d(dst, &tmB, fb, tn * NT + j * Cfg::CHUNK_N, kt * Cfg::BK, z);
+                    else
+                        tma_load_2d(dst, &tmB, fb, tn * NT + j * Cfg::CHUNK_N, kt * Cfg::BK);
+                }
                 ++issued;
                 if (++stage == S) {
                     stage = 0;
@@ -303,7 +312,8 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits),
+                       static_cast<unsigned>(p.batch > 0 ? p.batch : 1), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;

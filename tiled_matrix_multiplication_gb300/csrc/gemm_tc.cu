@@ -129,6 +129,7 @@ struct TcCfg {
 struct Work {
     int tm, tn, split, kt0, kt1;
     int tail;   // index among the tail-split tiles, or -1
+    int z;      // batch index
 };
 
 // Columns of work units: with A multicast one unit is two adjacent tiles.
@@ -136,15 +137,25 @@ __device__ __forceinline__ int unit_cols(const TcParams &p) {
     return (p.tiles_n + p.mc - 1) / p.mc;
 }
 
+__device__ __forceinline__ int units_per_batch(const TcParams &p) {
+    return p.tiles_m * unit_cols(p) * p.splits;
+}
+
 __device__ __forceinline__ int total_units(const TcParams &p) {
     return p.tail_tiles > 0 ? p.tail_start + p.tail_tiles * p.tail_splits
-                            : p.tiles_m * unit_cols(p) * p.splits;
+                            : units_per_batch(p) * p.batch;
 }
 
 // `q`: which tile of a multicast unit this CTA's pair works on.
 __device__ __forceinline__ Work decode_work(const TcParams &p, int w, int q = 0) {
     Work r;
     int t;
+    r.z = 0;
+    if (p.batch > 1) {   // batches are the slowest dimension (no tail split)
+        const int per = units_per_batch(p);
+        r.z = w / per;
+        w -= r.z * per;
+    }
     if (p.tail_tiles > 0 && w >= p.tail_start) {
         const int u = w - p.tail_start;
         r.tail = u / p.tail_splits;
@@ -174,7 +185,7 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 
 // Store 32 consecutive accumulator values (columns col .. col+31 of `row`).
 __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int row, int col,
-                                            const uint32_t (&r)[32]) {
+                                            const uint32_t (&r)[32], int z = 0) {
     const int ncols = min(32, p.N - col);
     if (p.splits > 1) {
         float *dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
@@ -189,7 +200,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
         }
         return;
     }
-    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
+    const int64_t off = static_cast<int64_t>(z) * p.stride_c + static_cast<int64_t>(row) * p.ldc + col;
     if (p.out_kind == OUT_F32) {
         float *dst = static_cast<float *>(p.c) + off;
         if (ncols == 32 && p.c_vector) {
@@ -319,29 +330,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
                     const uint32_t fb =
                         PAIR ? map_to_cta(full_bar(stage), pair_leader) : full_bar(stage);
-                    auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
-                        if constexpr (PAIR)
-                            tma_load_2d_pair(dst, map, fb, x, y);
-                        else
-                            tma_load_2d(dst, map, fb, x, y);
+                    // rank-3 maps for batched operands (z = batch), 2-D otherwise
+                    auto load = [&](uint32_t dst, const CUtensorMap *map, bool batched, int x,
+                                    int y) {
+                        if constexpr (PAIR) {
+                            if (batched)
+                                tma_load_3d_pair(dst, map, fb, x, y, wk.z);
+                            else
+                                tma_load_2d_pair(dst, map, fb, x, y);
+                        } else {
+                            if (batched)
+                                tma_load_3d(dst, map, fb, x, y, wk.z);
+                            else
+                                tma_load_2d(dst, map, fb, x, y);
+                        }
                     };
                     if constexpr (MC == 2) {
                         // my half (q) of this CTA's A rows, to me and my counterpart
                         const uint16_t mask =
                             static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
-                        tma_load_2d_pair_mc(sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2),
-                                            &tmA, fb, kt * Cfg::BK, row0 + q * (Cfg::CTA_M / 2),
-                                            mask);
+                        const uint32_t dst = sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2);
+                        const int ya = row0 + q * (Cfg::CTA_M / 2);
+                        if (p.a_batched)
+                            tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
+                        else
+                            tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
                     } else {
-                        load(sA + stage * Cfg::A_STAGE, &tmA, kt * Cfg::BK, row0);
+                        load(sA + stage * Cfg::A_STAGE, &tmA, p.a_batched, kt * Cfg::BK, row0);
                     }
                     if constexpr (Cfg::B_KMAJOR) {
                         // B^T tile [BN_CTA rows of N] x [BK of K], one box
-                        load(sB + stage * Cfg::B_STAGE, &tmB, kt * Cfg::BK, col0);
+                        load(sB + stage * Cfg::B_STAGE, &tmB, p.b_batched, kt * Cfg::BK, col0);
                     } else {
 #pragma unroll
                         for (int j = 0; j < Cfg::B_CHUNKS; ++j)
-                            load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB,
+                            load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB, p.b_batched,
                                  col0 + j * Cfg::CHUNK_N, kt * Cfg::BK);
                     }
                     ++issued;
@@ -471,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(prow + c0 + j) =
                             make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
                 } else if (row < p.M && col < p.N) {
-                    store_chunk(p, wk.split, row, col, r);
+                    store_chunk(p, wk.split, row, col, r, wk.z);
                 }
             }
             tc_fence_before_sync();

@@ -173,6 +173,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     tp.partial = plan.splits > 1 ? dev->scratch : nullptr;
     tp.status = dev->status;
     tp.timeout_ns = 2000ull * 1000000ull;
+    tp.batch = 1;
     const int in_kind = dtype_in == TG_F16 ? tg::IN_F16 : tg::IN_BF16;
     if (tg::launch_gemm_tc(in_kind, plan.block_n, false, 1, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
         return TG_ERR_CUDA;

@@ -83,7 +83,10 @@ struct Plan {
     int64_t tail_start = 0, tail_kps = 0;
     bool skinny_two = false;                   // small-M kernel: two CTAs per SM
     uint64_t timeout_ns = 0;
+    int64_t stride_c = 0;                      // C batch stride (set before make_plan)
 };
+
+constexpr int64_t kMaxGridY = 65535;           // gridDim.y: one row per product (small M)
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -164,9 +167,13 @@ int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles, int64_t wa
 
 // `pair_slots` / `quad_slots`: clusters of 2 / 4 CTAs resident at once
 // (0: estimate from the SM count).
+// `batch` > 1: that many products with 16-byte aligned operands (no packing,
+// no K split across kernels, no tail split) in one launch; the batch index is
+// the slowest dimension of the work list.
 void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
-               const tg_options *opt, Plan *pl, int pair_slots = 0, int quad_slots = 0) {
+               const tg_options *opt, Plan *pl, int pair_slots = 0, int quad_slots = 0,
+               int64_t batch = 1) {
     tg_plan &p = pl->pub;
     std::memset(&p, 0, sizeof(p));
     const int ei = esize_of(din), eo = esize_of(dout);
@@ -212,11 +219,11 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         }
         const int64_t slots = std::max<int64_t>(1, resident);
         // work units: tiles, or pairs of horizontally adjacent tiles
-        const int64_t tiles = cdiv(M, tile_m) * cdiv(cdiv(N, cd.bn), cd.mc);
+        const int64_t tiles = cdiv(M, tile_m) * cdiv(cdiv(N, cd.bn), cd.mc) * batch;
         int64_t s_lo = 1, s_hi = 1;
-        if (opt && opt->splits) {
+        if (opt && opt->splits && batch == 1) {
             s_lo = s_hi = opt->splits;
-        } else if (tiles < slots / 2 && cd.mc == 1) {
+        } else if (tiles < slots / 2 && cd.mc == 1 && batch == 1) {
             s_hi = std::min<int64_t>(pl->k_tiles, 16);   // too few tiles: consider split K
         }
         for (int64_t s = s_lo; s <= s_hi; ++s) {
@@ -231,7 +238,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
             // A requested tail split (below) turns a short last wave into 1/ts
             // of a wave plus the partials' round trip.
-            if (se == 1 && opt && opt->tail_splits && !opt->splits) {
+            if (se == 1 && opt && opt->tail_splits && !opt->splits && batch == 1) {
                 const int64_t ts = tail_split_for(tiles, slots, pl->k_tiles, opt->tail_splits);
                 if (ts > 1) waves = static_cast<double>(tiles / slots) + 1.15 / static_cast<double>(ts);
             }
@@ -255,7 +262,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // holds all rows; work is spread over 128-column tiles and K splits).
     const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
     const bool skinny_ok = din != TG_F32 && M <= 128 && (forced_skinny || !(opt && opt->block_n)) &&
-                           !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR));
+                           !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&
+                           batch <= kMaxGridY;
     if (skinny_ok) {
         // One CTA per (128-column tile, K range); the K ranges of a tile form a
         // cluster of 1, 2, 4 or 8 CTAs that sums its partials on chip.  Take the
@@ -268,9 +276,11 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         // contiguous runs of B, fewer re-reads of A) measured no faster at
         // M <= 64 and slower at M = 128; they remain selectable.
         const int nt = (opt && opt->block_n) ? opt->block_n : 128;
-        const int64_t tiles = cdiv(N, nt);
+        // (with a batch, one grid row of tiles x K ranges per product)
+        const int64_t tiles = cdiv(N, nt) * batch;
         int64_t best_s = 1;
-        bool two = false;
+        // a batch with more CTAs than SMs even unsplit: two CTAs per SM
+        bool two = batch > 1 && nt == 128 && tiles > cap;
         for (int64_t sc : {2, 4, 8}) {
             const int64_t kps = cdiv(ktiles, sc);
             if ((sc - 1) * kps >= ktiles) continue;          // a K range would be empty
@@ -324,7 +334,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
     p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
     if (din == TG_F32) p.pack_b = 2;   // kind::tf32 reads B K-major: B^T into the workspace
-    p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0;
+    p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0 && (batch == 1 || (pl->stride_c * eo) % 16 == 0);
     pl->lda_p = p.pack_a ? round_up(K, align_elems) : lda;
     pl->ldb_p = p.pack_b == 2 ? round_up(K, align_elems)
                               : (p.pack_b ? round_up(N, align_elems) : ldb);
@@ -343,7 +353,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         ws = round_up(ws + splits * M * N * 4, 256);
     }
     // Tail split of the tensor-core paths (auto plans without a K split).
-    if (p.path != TG_PATH_SKINNY && splits == 1 && opt && opt->tail_splits && !opt->splits) {
+    if (p.path != TG_PATH_SKINNY && splits == 1 && opt && opt->tail_splits && !opt->splits &&
+        batch == 1) {
         const int64_t slots = pair ? std::max<int64_t>(1, cap / 2) : std::max<int64_t>(1, cap);
         const int64_t ts = tail_split_for(p.tiles, slots, pl->k_tiles, opt->tail_splits);
         if (ts > 1) {
@@ -429,19 +440,24 @@ CUtensorMapDataType tma_type(tg_dtype t) {
 
 // Row-major [rows, cols] with pitch `ld` elements; boxes of box_cols x box_rows
 // whose rows (box_cols * esize bytes = 128, 64 or 32) are swizzled at that
-// size; zero fill out of range.
+// size; zero fill out of range.  With nb > 1 the map has a third dimension of
+// nb matrices `stride` elements apart (boxes one matrix deep).
 tg_status encode_2d(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
-                    int64_t ld, int box_cols, int box_rows) {
+                    int64_t ld, int box_cols, int box_rows, int64_t nb = 1, int64_t stride = 0) {
     const int row_bytes = box_cols * esize_of(t);
     const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                                                    : CU_TENSOR_MAP_SWIZZLE_32B;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esize_of(t))};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, tma_type(t), 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+    const cuuint32_t rank = nb > 1 ? 3 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(nb)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * esize_of(t)),
+                                   static_cast<cuuint64_t>(stride * esize_of(t))};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows),
+                               1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, tma_type(t), rank, const_cast<void *>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
 }
@@ -450,6 +466,204 @@ tg_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return TG_OK;
     if (e == cudaErrorMemoryAllocation) return TG_ERR_OUT_OF_MEMORY;
     return TG_ERR_CUDA;
+}
+
+// Products of one launch: `count` of them, whose A / B / C start sa / sb / sc
+// elements apart (sa or sb == 0: one operand shared by every product).
+struct Batch {
+    int64_t count = 1, sa = 0, sb = 0, sc = 0;
+};
+
+// Enqueues one validated product with M, N, K > 0 -- or, with bt.count > 1,
+// that many products in one launch (16-bit operands that need no packing).
+// A tensor map the driver rejects for a batch sets *map_failed before
+// anything is enqueued, so the caller can run the products one by one.
+tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+                  int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
+                  cudaStream_t s, const tg_options *opt, DeviceState *dev, const Batch &bt,
+                  bool *map_failed) {
+    tg_status st = TG_OK;
+    Plan pl;
+    pl.stride_c = bt.sc;
+    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl,
+              dev->pair_slots, dev->quad_slots, bt.count);
+    const tg_plan &p = pl.pub;
+    const int ei = esize_of(dtype_in);
+    const bool batched = bt.count > 1;
+    // operands that differ per product get a rank-3 map; a shared one (stride 0) stays 2-D
+    const int64_t nb_a = batched && bt.sa ? bt.count : 1;
+    const int64_t nb_b = batched && bt.sb ? bt.count : 1;
+    auto map_error = [&]() {
+        if (batched && map_failed) *map_failed = true;
+        return TG_ERR_CUDA;
+    };
+
+    uint8_t *ws = nullptr;
+    if (p.workspace_bytes > 0) {
+        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), p.workspace_bytes,
+                                                dev->pool, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    auto fail = [&](tg_status code) {
+        if (ws) cudaFreeAsync(ws, s);
+        return code;
+    };
+    const void *A = a;
+    const void *B = b;
+    if (p.pack_a) {
+        A = ws + pl.off_a;
+        st = cuda_status(tg::launch_pack_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, ei, s));
+        if (st != TG_OK) return fail(st);
+    }
+    if (p.pack_b) {
+        B = ws + pl.off_b;
+        st = cuda_status(p.pack_b == 2
+                             ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
+                             : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
+        if (st != TG_OK) return fail(st);
+    }
+    CUtensorMap tmA, tmB;
+    const int chunk = 128 / ei;
+    if (p.path == TG_PATH_SKINNY) {
+        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, p.block_m, nb_a, bt.sa) != TG_OK ||
+            encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k, nb_b, bt.sb) != TG_OK)
+            return fail(map_error());
+        tg::SkParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.M = static_cast<int32_t>(M);
+        sp.N = static_cast<int32_t>(N);
+        sp.K = static_cast<int32_t>(K);
+        sp.tiles_n = static_cast<int32_t>(pl.tiles_n);
+        sp.k_tiles = static_cast<int32_t>(pl.k_tiles);
+        sp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
+        sp.splits = p.splits;
+        sp.out_kind = out_kind_of(dtype_out);
+        sp.ldc = ldc;
+        sp.c = c;
+        sp.status = dev->status;
+        sp.timeout_ns = pl.timeout_ns;
+        sp.two_per_sm = pl.skinny_two ? 1 : 0;
+        sp.batch = static_cast<int32_t>(bt.count);
+        sp.a_batched = nb_a > 1;
+        sp.b_batched = nb_b > 1;
+        sp.stride_c = bt.sc;
+        st = cuda_status(
+            tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));
+        if (st != TG_OK) return fail(st);
+        if (ws && cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
+        return TG_OK;
+    }
+    const bool pair = p.path == TG_PATH_TC_PAIR;
+    const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
+    const int b_chunk = tg::tc_b_swizzle_bytes(in_kind_of(dtype_in), p.block_n, pair) / ei;
+    const tg_status sb = p.pack_b == 2
+                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
+                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, b_chunk, p.block_k,
+                                         nb_b, bt.sb);
+    // with A multicast each CTA loads half of its 128 rows of A
+    const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
+    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_rows, nb_a, bt.sa) != TG_OK ||
+        sb != TG_OK)
+        return fail(map_error());
+
+    tg::TcParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    tp.M = static_cast<int32_t>(M);
+    tp.N = static_cast<int32_t>(N);
+    tp.K = static_cast<int32_t>(K);
+    tp.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    tp.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    tp.k_tiles = static_cast<int32_t>(pl.k_tiles);
+    tp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
+    tp.splits = p.splits;
+    tp.group_m = p.group_m;
+    tp.out_kind = out_kind_of(dtype_out);
+    tp.c_vector = p.c_vector;
+    tp.mc = std::max(p.multicast, 1);
+    tp.ldc = ldc;
+    tp.c = c;
+    tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
+    tp.status = dev->status;
+    tp.timeout_ns = pl.timeout_ns;
+    tp.batch = static_cast<int32_t>(bt.count);
+    tp.a_batched = nb_a > 1;
+    tp.b_batched = nb_b > 1;
+    tp.stride_c = bt.sc;
+    if (p.tail_tiles > 0) {
+        tp.tail_start = static_cast<int32_t>(pl.tail_start);
+        tp.tail_tiles = p.tail_tiles;
+        tp.tail_splits = p.tail_splits;
+        tp.tail_kps = static_cast<int32_t>(pl.tail_kps);
+        tp.tail_partial = reinterpret_cast<float *>(ws + pl.off_tail);
+        tp.tail_count = reinterpret_cast<unsigned int *>(ws + pl.off_cnt);
+        const size_t cnt_bytes = static_cast<size_t>(p.tail_tiles) * (pair ? 2 : 1) * 4;
+        st = cuda_status(cudaMemsetAsync(tp.tail_count, 0, cnt_bytes, s));
+        if (st != TG_OK) return fail(st);
+    }
+    st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair,
+                                        std::max(p.multicast, 1), tmA, tmB, tp, p.ctas, s));
+    if (st != TG_OK) return fail(st);
+    if (p.splits > 1) {
+        st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,
+                                                  tp.out_kind, p.c_vector, s));
+        if (st != TG_OK) return fail(st);
+    }
+    if (ws) {
+        if (cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
+    }
+    return TG_OK;
+}
+
+// Argument rules of tg_gemm_strided_batched on top of those of one product.
+tg_status validate_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void *a,
+                           int64_t lda, int64_t sa, const void *b, int64_t ldb, int64_t sb,
+                           const void *c, int64_t ldc, int64_t sc, int din, int dout,
+                           const tg_options *opt) {
+    if (batch < 0 || sa < 0 || sb < 0 || sc < 0) return TG_ERR_INVALID_VALUE;
+    const tg_status v = validate(M, N, K, a, lda, b, ldb, c, ldc, din, dout, opt);
+    if (v != TG_OK) return v;
+    if (batch > kMaxDim) return TG_ERR_UNSUPPORTED;
+    if (batch > 1 && opt) {
+        if (opt->tail_splits) return TG_ERR_UNSUPPORTED;
+        if (opt->splits > 1 && opt->path != TG_PATH_SKINNY) return TG_ERR_UNSUPPORTED;
+    }
+    if (batch <= 1 || M == 0 || N == 0) return TG_OK;
+    const int64_t lim = int64_t(1) << 46;   // elements spanned by the batch strides
+    for (const int64_t st : {sa, sb, sc})
+        if (st > 0 && batch - 1 > lim / st) return TG_ERR_UNSUPPORTED;
+    if (cdiv(M, 128) * cdiv(N, 128) > (int64_t(1) << 30) / batch) return TG_ERR_UNSUPPORTED;
+    // the products' C blocks must be disjoint: stacked, or interleaved along rows
+    const int64_t span_c = (M - 1) * ldc + N;
+    const bool stacked = sc >= span_c;
+    const bool interleaved = sc >= N && (batch - 1) * sc + N <= ldc;
+    if (!stacked && !interleaved) return TG_ERR_INVALID_VALUE;
+    if (K > 0) {
+        const int ei = esize_of(static_cast<tg_dtype>(din));
+        const int eo = esize_of(static_cast<tg_dtype>(dout));
+        auto range = [](const void *p, int64_t elems, int es, uintptr_t *lo, uintptr_t *hi) {
+            *lo = reinterpret_cast<uintptr_t>(p);
+            *hi = *lo + static_cast<uintptr_t>(elems * es);
+        };
+        uintptr_t a0, a1, b0, b1, c0, c1;
+        range(a, (batch - 1) * sa + (M - 1) * lda + K, ei, &a0, &a1);
+        range(b, (batch - 1) * sb + (K - 1) * ldb + N, ei, &b0, &b1);
+        range(c, (batch - 1) * sc + span_c, eo, &c0, &c1);
+        if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+// One launch for the whole batch: 16-bit operands read in place (16-byte
+// aligned base, row pitch and batch stride; strides within the TMA limit).
+bool batch_in_one_launch(tg_dtype din, const void *a, int64_t lda, int64_t sa, const void *b,
+                         int64_t ldb, int64_t sb) {
+    if (din == TG_F32) return false;
+    const int ei = esize_of(din);
+    auto ok = [&](const void *p, int64_t ld, int64_t st) {
+        return aligned16(p) && (ld * ei) % 16 == 0 && (st * ei) % 16 == 0 &&
+               st * ei < (int64_t(1) << 40);
+    };
+    return ok(a, lda, sa) && ok(b, ldb, sb);
 }
 
 }  // namespace
@@ -504,123 +718,85 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     const int eo = esize_of(dtype_out);
     if (K == 0)
         return cuda_status(cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s));
-
-    Plan pl;
-    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl,
-              dev->pair_slots, dev->quad_slots);
-    const tg_plan &p = pl.pub;
-    const int ei = esize_of(dtype_in);
-
-    uint8_t *ws = nullptr;
-    if (p.workspace_bytes > 0) {
-        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), p.workspace_bytes,
-                                                dev->pool, s);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    auto fail = [&](tg_status code) {
-        if (ws) cudaFreeAsync(ws, s);
-        return code;
-    };
-    const void *A = a;
-    const void *B = b;
-    if (p.pack_a) {
-        A = ws + pl.off_a;
-        st = cuda_status(tg::launch_pack_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, ei, s));
-        if (st != TG_OK) return fail(st);
-    }
-    if (p.pack_b) {
-        B = ws + pl.off_b;
-        st = cuda_status(p.pack_b == 2
-                             ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
-                             : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
-        if (st != TG_OK) return fail(st);
-    }
-    CUtensorMap tmA, tmB;
-    const int chunk = 128 / ei;
-    if (p.path == TG_PATH_SKINNY) {
-        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, p.block_m) != TG_OK ||
-            encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k) != TG_OK)
-            return fail(TG_ERR_CUDA);
-        tg::SkParams sp;
-        std::memset(&sp, 0, sizeof(sp));
-        sp.M = static_cast<int32_t>(M);
-        sp.N = static_cast<int32_t>(N);
-        sp.K = static_cast<int32_t>(K);
-        sp.tiles_n = static_cast<int32_t>(p.tiles);
-        sp.k_tiles = static_cast<int32_t>(pl.k_tiles);
-        sp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
-        sp.splits = p.splits;
-        sp.out_kind = out_kind_of(dtype_out);
-        sp.ldc = ldc;
-        sp.c = c;
-        sp.status = dev->status;
-        sp.timeout_ns = pl.timeout_ns;
-        sp.two_per_sm = pl.skinny_two ? 1 : 0;
-        st = cuda_status(
-            tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));
-        if (st != TG_OK) return fail(st);
-        if (ws && cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
-        return TG_OK;
-    }
-    const bool pair = p.path == TG_PATH_TC_PAIR;
-    const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
-    const int b_chunk = tg::tc_b_swizzle_bytes(in_kind_of(dtype_in), p.block_n, pair) / ei;
-    const tg_status sb = p.pack_b == 2
-                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
-                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, b_chunk, p.block_k);
-    // with A multicast each CTA loads half of its 128 rows of A
-    const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
-    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_rows) != TG_OK || sb != TG_OK)
-        return fail(TG_ERR_CUDA);
-
-    tg::TcParams tp;
-    std::memset(&tp, 0, sizeof(tp));
-    tp.M = static_cast<int32_t>(M);
-    tp.N = static_cast<int32_t>(N);
-    tp.K = static_cast<int32_t>(K);
-    tp.tiles_m = static_cast<int32_t>(pl.tiles_m);
-    tp.tiles_n = static_cast<int32_t>(pl.tiles_n);
-    tp.k_tiles = static_cast<int32_t>(pl.k_tiles);
-    tp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
-    tp.splits = p.splits;
-    tp.group_m = p.group_m;
-    tp.out_kind = out_kind_of(dtype_out);
-    tp.c_vector = p.c_vector;
-    tp.mc = std::max(p.multicast, 1);
-    tp.ldc = ldc;
-    tp.c = c;
-    tp.partial = p.splits > 1 ? reinterpret_cast<float *>(ws + pl.off_p) : nullptr;
-    tp.status = dev->status;
-    tp.timeout_ns = pl.timeout_ns;
-    if (p.tail_tiles > 0) {
-        tp.tail_start = static_cast<int32_t>(pl.tail_start);
-        tp.tail_tiles = p.tail_tiles;
-        tp.tail_splits = p.tail_splits;
-        tp.tail_kps = static_cast<int32_t>(pl.tail_kps);
-        tp.tail_partial = reinterpret_cast<float *>(ws + pl.off_tail);
-        tp.tail_count = reinterpret_cast<unsigned int *>(ws + pl.off_cnt);
-        const size_t cnt_bytes = static_cast<size_t>(p.tail_tiles) * (pair ? 2 : 1) * 4;
-        st = cuda_status(cudaMemsetAsync(tp.tail_count, 0, cnt_bytes, s));
-        if (st != TG_OK) return fail(st);
-    }
-    st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair,
-                                        std::max(p.multicast, 1), tmA, tmB, tp, p.ctas, s));
-    if (st != TG_OK) return fail(st);
-    if (p.splits > 1) {
-        st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,
-                                                  tp.out_kind, p.c_vector, s));
-        if (st != TG_OK) return fail(st);
-    }
-    if (ws) {
-        if (cudaFreeAsync(ws, s) != cudaSuccess) return TG_ERR_CUDA;
-    }
-    return TG_OK;
+    return enqueue(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, s, opt, dev, Batch{},
+                   nullptr);
 }
 
 tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                   int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
                   void *stream) {
     return tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, nullptr);
+}
+
+tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                       const void *a, int64_t lda, int64_t stride_a,
+                                       const void *b, int64_t ldb, int64_t stride_b,
+                                       const void *c, int64_t ldc, int64_t stride_c,
+                                       tg_dtype dtype_in, tg_dtype dtype_out, int32_t num_sms,
+                                       const tg_options *opt, tg_plan *plan) {
+    if (plan == nullptr) return TG_ERR_INVALID_VALUE;
+    const tg_status v = validate_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c,
+                                         ldc, stride_c, dtype_in, dtype_out, opt);
+    if (v != TG_OK) return v;
+    Plan pl;
+    const bool one = batch > 1 &&
+                     batch_in_one_launch(dtype_in, a, lda, stride_a, b, ldb, stride_b);
+    pl.stride_c = stride_c;
+    make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, opt, &pl, 0, 0,
+              one ? batch : 1);
+    if (batch > 1 && !one) {   // one call per product
+        pl.pub.per_batch = 1;
+        pl.pub.kernels *= static_cast<int32_t>(std::min<int64_t>(batch, 1 << 24));
+        pl.pub.tiles *= batch;
+    }
+    if (batch == 0 || M == 0 || N == 0 || K == 0) {
+        pl.pub.kernels = 0;
+        pl.pub.workspace_bytes = 0;
+        pl.pub.tail_tiles = 0;
+        pl.pub.tail_splits = 0;
+    }
+    *plan = pl.pub;
+    return TG_OK;
+}
+
+tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void *a,
+                                  int64_t lda, int64_t stride_a, const void *b, int64_t ldb,
+                                  int64_t stride_b, void *c, int64_t ldc, int64_t stride_c,
+                                  tg_dtype dtype_in, tg_dtype dtype_out, void *stream,
+                                  const tg_options *opt) {
+    tg_status st = validate_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc,
+                                    stride_c, dtype_in, dtype_out, opt);
+    if (st != TG_OK) return st;
+    if (batch == 0 || M == 0 || N == 0) return TG_OK;
+    if (batch == 1)
+        return tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, opt);
+    DeviceState *dev = nullptr;
+    st = device_state(&dev);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int ei = esize_of(dtype_in), eo = esize_of(dtype_out);
+    auto c_of = [&](int64_t z) { return static_cast<uint8_t *>(c) + z * stride_c * eo; };
+    if (K == 0) {
+        for (int64_t z = 0; z < batch; ++z) {
+            st = cuda_status(cudaMemset2DAsync(c_of(z), ldc * eo, 0, N * eo, M, s));
+            if (st != TG_OK) return st;
+        }
+        return TG_OK;
+    }
+    if (batch_in_one_launch(dtype_in, a, lda, stride_a, b, ldb, stride_b)) {
+        bool map_failed = false;
+        st = enqueue(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, s, opt, dev,
+                     Batch{batch, stride_a, stride_b, stride_c}, &map_failed);
+        if (!map_failed) return st;
+    }
+    // one call per product, in order of z
+    for (int64_t z = 0; z < batch; ++z) {
+        st = tg_gemm_ex(M, N, K, static_cast<const uint8_t *>(a) + z * stride_a * ei, lda,
+                        static_cast<const uint8_t *>(b) + z * stride_b * ei, ldb, c_of(z), ldc,
+                        dtype_in, dtype_out, stream, opt);
+        if (st != TG_OK) return st;
+    }
+    return TG_OK;
 }
 
 tg_status tg_last_device_error(void *stream) {

@@ -40,6 +40,11 @@ struct TcParams {
     int32_t tail_start, tail_tiles, tail_splits, tail_kps;
     float *tail_partial;
     unsigned int *tail_count;
+    // Strided batch: `batch` independent products; A / B use rank-3 tensor maps
+    // (z = batch index) when a_batched / b_batched, else one 2-D map shared by
+    // every batch (stride 0); C of batch z starts at c + z * stride_c.
+    int32_t batch, a_batched, b_batched, pad2_;
+    int64_t stride_c;           // elements
 };
 
 // Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with NT
@@ -53,7 +58,9 @@ struct SkParams {
     int32_t splits;             // cluster size: 1, 2, 4 or 8
     int32_t out_kind;
     int32_t two_per_sm;         // half-size ring, two CTAs per SM
-    int32_t pad_;
+    int32_t batch;              // gridDim.y; A / B rank-3 when a_batched / b_batched
+    int32_t a_batched, b_batched;
+    int64_t stride_c;           // elements between the C of consecutive batches
     int64_t ldc;
     void *c;
     int *status;
