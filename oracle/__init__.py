@@ -11,6 +11,8 @@ Contents:
   * ``tiled_model`` -- the pages' CPU tiled model: tile ranges, grouped raster,
                        per-K-chunk partial sums and the global-load counter.
   * ``compare``     -- the tolerance rule and ulp of the output format.
+  * ``epilogue``    -- the fused epilogue act(alpha*scale*C + bias) + beta*R in
+                       FP64 and its tolerance.
 
 Every pin that ties these functions to the pages or to mathematics lives in
 ``tests/test_oracle_*.py``.
@@ -18,10 +20,10 @@ Every pin that ties these functions to the pages or to mathematics lives in
 from .ref import (F16, BF16, F32, FORMATS, build, decode, encode, gemm_ref,
                   gemm_ref_bits, num_threads, lib_path)
 from .compare import ulp, tolerance, check_close, rel_tol_for
-from . import tiled_model
+from . import epilogue, tiled_model
 
 __all__ = [
     "F16", "BF16", "F32", "FORMATS", "build", "decode", "encode", "gemm_ref",
     "gemm_ref_bits", "num_threads", "lib_path", "ulp", "tolerance", "check_close",
-    "rel_tol_for", "tiled_model",
+    "rel_tol_for", "tiled_model", "epilogue",
 ]
