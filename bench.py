@@ -70,7 +70,16 @@ WORKLOADS = {
     "skinny16_f16": (16, 8192, 8192, "f16", "f16", "uniform", "skinny M=16, N=K=8192 FP16"),
     "skinny64_f16": (64, 8192, 8192, "f16", "f16", "uniform", "skinny M=64, N=K=8192 FP16"),
     "skinny128_f16": (128, 8192, 8192, "f16", "f16", "uniform", "skinny M=128, N=K=8192 FP16"),
+    # strided batches (one tg_gemm_strided_batched call; contiguous [batch, rows, cols])
+    "batched16x2048_f16": (2048, 2048, 2048, "f16", "f16", "uniform",
+                           "strided batch of 16 GEMMs 2048^3, FP16 in U[-1,1), FP16 out"),
+    "batched64x1024_bf16": (1024, 1024, 1024, "bf16", "bf16", "normal",
+                            "strided batch of 64 GEMMs 1024^3, BF16 N(0,0.02)"),
+    "batched32x64x8192_f16": (64, 8192, 8192, "f16", "f16", "uniform",
+                              "strided batch of 32 small-M GEMMs 64x8192x8192, FP16"),
 }
+# products per call of the batched workloads (1 for every other workload)
+BATCH = {"batched16x2048_f16": 16, "batched64x1024_bf16": 64, "batched32x64x8192_f16": 32}
 DEFAULT_WORKLOAD = "square4096_f16"
 ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -268,8 +277,9 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "M": M, "N": N, "K": K, "dtype_in": din,
-                   "dtype_out": dout, "step": f"{rows} sampled output rows of the problem"},
+        "config": {"workload": desc, "M": M, "N": N, "K": K, "batch": BATCH.get(args.workload, 1),
+                   "dtype_in": din, "dtype_out": dout,
+                   "step": f"{rows} sampled output rows of the problem"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                          "sample": f"{rows} seeded output rows x {N} columns per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -299,37 +309,46 @@ def run_ours(args, world, rank, local):
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     iview = {"f16": np.int16, "bf16": np.int16, "f32": np.int32}
 
-    a_bits = inputs.matrix_bits(M, K, din, dist, inputs.SEED_A)
-    b_bits = inputs.matrix_bits(K, N, din, dist, inputs.SEED_B)
+    nb = BATCH.get(args.workload, 1)
+    a_bits = np.stack([inputs.matrix_bits(M, K, din, dist, inputs.SEED_A + z) for z in range(nb)])
+    b_bits = np.stack([inputs.matrix_bits(K, N, din, dist, inputs.SEED_B + z) for z in range(nb)])
     a_host = torch.from_numpy(a_bits.view(iview[din])).view(tdt[din])
     b_host = torch.from_numpy(b_bits.view(iview[din])).view(tdt[din])
-    set_bytes = (M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout]
+    set_bytes = nb * ((M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout])
     R = max(2, -(-2 * l2 // set_bytes) + 1)
     A0 = a_host.cuda()
     B0 = b_host.cuda()
     sets = []
     for i in range(R):
         sets.append((A0 if i == 0 else A0.clone(), B0 if i == 0 else B0.clone(),
-                     torch.empty((M, N), dtype=tdt[dout], device="cuda")))
+                     torch.empty((nb, M, N), dtype=tdt[dout], device="cuda")))
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count)
     code_in, code_out = tg.dtype_code(din), tg.dtype_code(dout)
 
     opts = dict(kv.split("=") for kv in args.opt)
     opts = {k: int(v) for k, v in opts.items()}
     topt = tg.make_options(**opts) if opts else None
-    if opts:
+    if nb > 1:
+        plan = tg.plan_batched(nb, M, N, K, din, dout, num_sms=props.multi_processor_count,
+                               **opts)
+    else:
         plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count, **opts)
+
+    def call(a, b, c):
+        if nb > 1:
+            return tg.tg_gemm_strided_batched(nb, M, N, K, a.data_ptr(), K, M * K, b.data_ptr(),
+                                              N, K * N, c.data_ptr(), N, M * N, code_in,
+                                              code_out, sh, topt)
+        if topt is None:
+            return tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                              code_in, code_out, sh)
+        return tg.tg_gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                             code_in, code_out, sh, topt)
 
     def step(i):
         a, b, c = sets[i % R]
-        if topt is None:
-            st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
-                            code_in, code_out, sh)
-        else:
-            st = tg.tg_gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
-                               code_in, code_out, sh, topt)
+        st = call(a, b, c)
         if st != tg.TG_OK:
             raise tg.TgError(st, "tg_gemm")
 
@@ -362,7 +381,7 @@ def run_ours(args, world, rank, local):
     region_ms = max_over_ranks(region_ms, dist_on)
     kernel_ms = max_over_ranks(kernel_ms, dist_on)
 
-    flops = 2.0 * M * N * K
+    flops = 2.0 * M * N * K * nb
     ms_per_step = region_ms / K_steps
     value = world * flops / (ms_per_step * 1e-3) / 1e12
 
@@ -370,14 +389,13 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(3, min(K_steps, 50))
     a_pin = a_host.pin_memory()
     b_pin = b_host.pin_memory()
-    c_pin = torch.empty((M, N), dtype=tdt[dout]).pin_memory()
+    c_pin = torch.empty((nb, M, N), dtype=tdt[dout]).pin_memory()
     a_d, b_d, c_d = sets[0]
 
     def e2e_step():
         a_d.copy_(a_pin, non_blocking=True)
         b_d.copy_(b_pin, non_blocking=True)
-        st = tg.tg_gemm(M, N, K, a_d.data_ptr(), K, b_d.data_ptr(), N, c_d.data_ptr(), N,
-                        code_in, code_out, sh)
+        st = call(a_d, b_d, c_d)
         if st != tg.TG_OK:
             raise tg.TgError(st, "tg_gemm")
         c_pin.copy_(c_d, non_blocking=True)
@@ -395,8 +413,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist_on)
     tg.check_device_error()
-    h2d = (M * K + K * N) * ESIZE[din]
-    d2h = M * N * ESIZE[dout]
+    h2d = nb * (M * K + K * N) * ESIZE[din]
+    d2h = nb * M * N * ESIZE[dout]
 
     if rank != 0:
         if dist_on:
@@ -408,7 +426,7 @@ def run_ours(args, world, rank, local):
     skinny = M <= 128
     if skinny:
         bound, unit = "hbm", "GB/s"
-        alg = (M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout]
+        alg = nb * ((M * K + K * N) * ESIZE[din] + M * N * ESIZE[dout])
         achieved = alg / (kernel_ms * 1e-3) / 1e9
         peak = float(pk["hbm_gbs"])
     else:
@@ -427,8 +445,8 @@ def run_ours(args, world, rank, local):
         "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": din,
         "data": "synthetic",
-        "config": {"workload": desc, "M": M, "N": N, "K": K, "dtype_in": din, "dtype_out": dout,
-                   "accumulate": "f32", "parallelism": "replicas" if world > 1 else "single",
+        "config": {"workload": desc, "M": M, "N": N, "K": K, "batch": nb, "dtype_in": din,
+                   "dtype_out": dout, "accumulate": "f32", "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2 {l2 / 1e6:.0f} MB)",
                    "tile": f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}",

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 2
+#define TG_ABI_VERSION 3
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -162,6 +162,57 @@ tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K,
                        const void *c, int64_t ldc,
                        tg_dtype dtype_in, tg_dtype dtype_out,
                        int32_t num_sms, const tg_options *opt, tg_plan *plan);
+
+/* Activation of the fused epilogue (see tg_gemm_fused). */
+typedef enum tg_activation {
+    TG_ACT_NONE = 0,       /* x */
+    TG_ACT_RELU = 1,       /* x if x > 0, else 0 */
+    TG_ACT_SILU = 2,       /* x / (1 + exp(-x)) */
+    TG_ACT_GELU_TANH = 3   /* x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))) */
+} tg_activation;
+
+/* Fused epilogue of tg_gemm_fused. */
+typedef struct tg_epilogue {
+    float alpha;            /* multiplies the product */
+    float beta;             /* multiplies the residual */
+    const float *scale;     /* N per-column FP32 factors on the device, or NULL (1) */
+    const float *bias;      /* N per-column FP32 offsets on the device, or NULL (0) */
+    const void *residual;   /* R: [M, ldr] of dtype_out on the device, or NULL */
+    int64_t ldr;            /* leading dimension of R in elements (>= N) */
+    int32_t activation;     /* tg_activation */
+    int32_t reserved;       /* must be 0 */
+} tg_epilogue;
+
+/*
+ * tg_gemm_fused -- the product with a fused epilogue, applied to each FP32
+ * accumulator value where the kernel writes C, before its one rounding to
+ * dtype_out:
+ *
+ *     C[m,n] = act(alpha * scale[n] * sum_k A[m,k] B[k,n] + bias[n]) + beta * R[m,n]
+ *
+ * The work done "while the data is already in registers" that "Matrix
+ * Multiplication" (teenygrad docs, closing section) hands on to the next
+ * chapter, "Fusing an Epilogue"; the same book's fused kernel applies a
+ * per-channel scale and shift (batch norm) and a SiLU to a GEMM this way.
+ *
+ *   M .. dtype_out, stream, opt   as for tg_gemm_ex
+ *   epilogue   NULL: exactly tg_gemm_ex.  Otherwise: activation out of range
+ *              or reserved != 0 -> TG_ERR_INVALID_VALUE; a residual needs
+ *              ldr >= N and dtype_out alignment, and may be C itself (same
+ *              pointer and ldr == ldc: C = act(...) + beta * C) but must not
+ *              otherwise overlap C; scale / bias must be 4-byte aligned and
+ *              not overlap C -> else TG_ERR_INVALID_VALUE.
+ *
+ * K == 0 writes act(bias[n]) + beta * R[m,n] (the epilogue of the empty sum).
+ * With a K split the epilogue runs in the kernel that sums the partials.
+ */
+tg_status tg_gemm_fused(int64_t M, int64_t N, int64_t K,
+                        const void *a, int64_t lda,
+                        const void *b, int64_t ldb,
+                        void *c, int64_t ldc,
+                        tg_dtype dtype_in, tg_dtype dtype_out,
+                        const tg_epilogue *epilogue,
+                        void *stream, const tg_options *opt);
 
 /*
  * tg_gemm_strided_batched -- `batch` independent products

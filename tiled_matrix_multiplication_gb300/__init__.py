@@ -20,12 +20,16 @@ from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_ERR_ARCH, TG_ERR_
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
                    TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, NOALLOC_SCRATCH_BYTES, TgError,
                    load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
+                   ACT_CODES, TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU,
+                   make_epilogue, tg_epilogue, tg_gemm_fused,
                    tg_gemm_splitk_noalloc, tg_gemm_strided_batched, tg_last_device_error,
                    tg_options, tg_plan, tg_plan_gemm, tg_plan_gemm_strided_batched,
                    tg_status_string)
 
 __all__ = [
-    "gemm", "bmm", "plan", "plan_batched", "check_device_error", "dtype_code", "TgError", "load", "make_options",
+    "gemm", "gemm_fused", "bmm", "plan", "plan_batched", "check_device_error",
+    "tg_gemm_fused", "tg_epilogue", "make_epilogue", "ACT_CODES", "TG_ACT_NONE", "TG_ACT_RELU",
+    "TG_ACT_SILU", "TG_ACT_GELU_TANH", "dtype_code", "TgError", "load", "make_options",
     "tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string", "tg_last_device_error",
     "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",
     "tg_plan_gemm_strided_batched", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
@@ -89,6 +93,59 @@ def gemm(a, b, out_dtype=None, out=None, stream=None, **options):
                         dtype_code(a.dtype), dtype_code(out_dtype), _stream_handle(stream), opt)
     if st != TG_OK:
         raise TgError(st, f"tg_gemm_ex(M={M}, N={N}, K={K})")
+    return out
+
+
+def gemm_fused(a, b, out_dtype=None, out=None, stream=None, alpha=1.0, scale=None, bias=None,
+               activation="none", beta=0.0, residual=None, **options):
+    """C = act(alpha * scale * (A @ B) + bias) + beta * residual, through
+    ``tg_gemm_fused``; the epilogue runs on the FP32 accumulator before the
+    one rounding to ``out_dtype``.
+
+    ``scale`` and ``bias`` are optional float32 CUDA vectors of length N;
+    ``residual`` an optional [M, N] CUDA tensor of ``out_dtype`` with unit
+    column stride (it may be ``out`` itself).  ``activation``: "none", "relu",
+    "silu" or "gelu_tanh".  Other arguments as for ``gemm``.
+    """
+    import torch
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("gemm_fused expects [M, K] @ [K, N]")
+    if a.dtype != b.dtype or not (a.is_cuda and b.is_cuda):
+        raise ValueError("A and B must be CUDA tensors of the same dtype")
+    M, K = a.shape
+    N = b.shape[1]
+    if (a.stride(1) != 1 and K > 1) or (b.stride(1) != 1 and N > 1):
+        raise ValueError("A and B need unit column stride")
+    out_dtype = a.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    elif out.shape != (M, N) or out.dtype != out_dtype or (out.stride(1) != 1 and N > 1):
+        raise ValueError("out must be [M, N] of out_dtype with unit column stride")
+    for name, v in (("scale", scale), ("bias", bias)):
+        if v is not None and (v.dtype != torch.float32 or v.shape != (N,) or not v.is_cuda
+                              or (v.stride(0) != 1 and N > 1)):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA vector of length N")
+    ldr = 0
+    if residual is not None:
+        if (residual.shape != (M, N) or residual.dtype != out_dtype or not residual.is_cuda
+                or (residual.stride(1) != 1 and N > 1)):
+            raise ValueError("residual must be [M, N] of out_dtype with unit column stride")
+        ldr = residual.stride(0) if M > 1 else max(N, 1)
+    lda = a.stride(0) if M > 1 else max(K, 1)
+    ldb = b.stride(0) if K > 1 else max(N, 1)
+    ldc = out.stride(0) if M > 1 else max(N, 1)
+    ep = make_epilogue(alpha=alpha, beta=beta,
+                       scale=scale.data_ptr() if scale is not None else 0,
+                       bias=bias.data_ptr() if bias is not None else 0,
+                       residual=residual.data_ptr() if residual is not None else 0, ldr=ldr,
+                       activation=activation)
+    opt = make_options(**options) if options else None
+    with torch.cuda.device(a.device):
+        st = tg_gemm_fused(M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
+                           dtype_code(a.dtype), dtype_code(out_dtype), ep,
+                           _stream_handle(stream), opt)
+    if st != TG_OK:
+        raise TgError(st, f"tg_gemm_fused(M={M}, N={N}, K={K})")
     return out
 
 

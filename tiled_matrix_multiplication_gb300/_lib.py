@@ -30,7 +30,11 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 # Every extern "C" symbol the header declares.
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
            "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
-           "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched")
+           "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused")
+
+TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_ACT_GELU_TANH = 0, 1, 2, 3
+ACT_CODES = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "silu": TG_ACT_SILU,
+             "gelu_tanh": TG_ACT_GELU_TANH}
 
 # Bytes of the library-owned partial-tile array of tg_gemm_splitk_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -41,6 +45,13 @@ class tg_options(ctypes.Structure):
                 ("block_n", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("tail_splits", ctypes.c_int32), ("multicast", ctypes.c_int32)]
+
+
+class tg_epilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("ldr", ctypes.c_int64),
+                ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class tg_plan(ctypes.Structure):
@@ -105,6 +116,9 @@ def load(path: str | None = None):
         lib.tg_plan_gemm_strided_batched.argtypes = batched + [i32, ctypes.POINTER(tg_options),
                                                                ctypes.POINTER(tg_plan)]
         lib.tg_plan_gemm_strided_batched.restype = ctypes.c_int
+        lib.tg_gemm_fused.argtypes = gemm_args[:-1] + [ctypes.POINTER(tg_epilogue), vp,
+                                                        ctypes.POINTER(tg_options)]
+        lib.tg_gemm_fused.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -193,3 +207,24 @@ def tg_plan_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb, strid
                                                  _code(dtype_out), num_sms, opt,
                                                  ctypes.byref(plan)))
     return st, plan.as_dict()
+
+
+def make_epilogue(alpha=1.0, beta=0.0, scale=0, bias=0, residual=0, ldr=0, activation="none"):
+    """tg_epilogue from plain values; pointers are integers (0 = NULL)."""
+    e = tg_epilogue()
+    e.alpha, e.beta = alpha, beta
+    e.scale, e.bias, e.residual = scale or None, bias or None, residual or None
+    e.ldr = ldr
+    e.activation = ACT_CODES[activation] if isinstance(activation, str) else int(activation)
+    e.reserved = 0
+    return e
+
+
+def tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, epilogue, stream,
+                  options=None) -> int:
+    """C = act(alpha * scale * (A B) + bias) + beta * R; ``epilogue`` is a
+    tg_epilogue or None.  Returns the tg_status."""
+    ep = ctypes.byref(epilogue) if epilogue is not None else None
+    opt = ctypes.byref(options) if options is not None else None
+    return int(load().tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                                    _code(dtype_out), ep, stream, opt))

@@ -8,12 +8,13 @@
 //   the descriptor's logical width stays the original one.
 // pack_transpose: writes B^T ([N, K], K contiguous) into the workspace for
 //   operand types whose MMA wants B K-major.
-// splitk_reduce: C[m,n] = round(sum_{s=0}^{S-1} P[s,m,n]) in increasing s --
+// splitk_reduce: C[m,n] = round(epilogue(sum_{s=0}^{S-1} P[s,m,n])) in increasing s --
 //   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
 //   both steps"), finished across work units instead of inside one.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "tg_epilogue.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -68,7 +69,7 @@ __device__ __forceinline__ void store_out(void *c, int64_t off, int out_kind, fl
 // One thread per 4 consecutive columns of one row.
 __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, int64_t M,
                                      int64_t N, void *c, int64_t ldc, int out_kind,
-                                     int vec_ok) {
+                                     int vec_ok, const EpiParams epi) {
     const int64_t groups_per_row = (N + 3) / 4;
     const int64_t total = M * groups_per_row;
     const int64_t plane = M * N;
@@ -92,6 +93,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int spli
                 for (int j = 0; j < nv; ++j) acc[j] += partial[s * plane + src + j];
         }
         const int nv = static_cast<int>(N - n0 < 4 ? N - n0 : 4);
+        if (epi.on)
+            for (int j = 0; j < nv; ++j) acc[j] = epi_one(epi, out_kind, m, n0 + j, acc[j]);
         for (int j = 0; j < nv; ++j) store_out(c, m * ldc + n0 + j, out_kind, acc[j]);
     }
 }
@@ -145,14 +148,17 @@ cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, in
 }
 
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N, void *c,
-                                 int64_t ldc, int out_kind, int c_vector, cudaStream_t stream) {
+                                 int64_t ldc, int out_kind, int c_vector, cudaStream_t stream,
+                                 const EpiParams *epi) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     (void)c_vector;
     const int threads = 256;
     const int64_t work = M * ((N + 3) / 4);
     const int vec_ok = (N % 4) == 0;
+    EpiParams e{};
+    if (epi) e = *epi;
     splitk_reduce_kernel<<<grid_for(work, threads), threads, 0, stream>>>(partial, splits, M, N, c,
-                                                                          ldc, out_kind, vec_ok);
+                                                                          ldc, out_kind, vec_ok, e);
     return cudaGetLastError();
 }
 

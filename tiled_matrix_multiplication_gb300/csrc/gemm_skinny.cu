@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "tg_epilogue.cuh"
 #include "tg_internal.h"
 #include "tg_kernel_common.cuh"
 #include "tg_ptx.cuh"
@@ -78,6 +79,7 @@ struct SkCfg {
 __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float v) {
     const int64_t off = static_cast<int64_t>(blockIdx.y) * p.stride_c +   // batch
                         static_cast<int64_t>(m) * p.ldc + n;
+    if (p.epi.on) v = epi_one(p.epi, p.out_kind, m, n, v);
     if (p.out_kind == OUT_F32)
         static_cast<float *>(p.c)[off] = v;
     else if (p.out_kind == OUT_F16)

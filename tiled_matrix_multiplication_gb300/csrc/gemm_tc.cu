@@ -62,6 +62,7 @@
 
 #include <mutex>
 
+#include "tg_epilogue.cuh"
 #include "tg_internal.h"
 #include "tg_kernel_common.cuh"
 #include "tg_ptx.cuh"
@@ -185,7 +186,7 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 
 // Store 32 consecutive accumulator values (columns col .. col+31 of `row`).
 __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int row, int col,
-                                            const uint32_t (&r)[32], int z = 0) {
+                                            uint32_t (&r)[32], int z = 0) {
     const int ncols = min(32, p.N - col);
     if (p.splits > 1) {
         float *dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
@@ -200,6 +201,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
         }
         return;
     }
+    if (p.epi.on) epi_chunk32(p.epi, p.out_kind, row, col, ncols, r);
     const int64_t off = static_cast<int64_t>(z) * p.stride_c + static_cast<int64_t>(row) * p.ldc + col;
     if (p.out_kind == OUT_F32) {
         float *dst = static_cast<float *>(p.c) + off;

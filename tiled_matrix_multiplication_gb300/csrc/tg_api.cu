@@ -481,7 +481,7 @@ struct Batch {
 tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                   int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
                   cudaStream_t s, const tg_options *opt, DeviceState *dev, const Batch &bt,
-                  bool *map_failed) {
+                  bool *map_failed, const tg::EpiParams *epi = nullptr) {
     tg_status st = TG_OK;
     Plan pl;
     pl.stride_c = bt.sc;
@@ -547,6 +547,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         sp.a_batched = nb_a > 1;
         sp.b_batched = nb_b > 1;
         sp.stride_c = bt.sc;
+        if (epi) sp.epi = *epi;
         st = cuda_status(
             tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));
         if (st != TG_OK) return fail(st);
@@ -589,6 +590,8 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     tp.a_batched = nb_a > 1;
     tp.b_batched = nb_b > 1;
     tp.stride_c = bt.sc;
+    // with a K split the epilogue runs where the partials are summed
+    if (epi && p.splits == 1) tp.epi = *epi;
     if (p.tail_tiles > 0) {
         tp.tail_start = static_cast<int32_t>(pl.tail_start);
         tp.tail_tiles = p.tail_tiles;
@@ -605,7 +608,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     if (st != TG_OK) return fail(st);
     if (p.splits > 1) {
         st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,
-                                                  tp.out_kind, p.c_vector, s));
+                                                  tp.out_kind, p.c_vector, s, epi));
         if (st != TG_OK) return fail(st);
     }
     if (ws) {
@@ -666,6 +669,45 @@ bool batch_in_one_launch(tg_dtype din, const void *a, int64_t lda, int64_t sa, c
     return ok(a, lda, sa) && ok(b, ldb, sb);
 }
 
+// Argument rules of the fused epilogue (on top of those of the product);
+// fills *e for the kernels.
+tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg_dtype dout,
+                            const tg_epilogue *ep, tg::EpiParams *e) {
+    std::memset(e, 0, sizeof(*e));
+    if (ep == nullptr) return TG_OK;
+    if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_GELU_TANH || ep->reserved != 0)
+        return TG_ERR_INVALID_VALUE;
+    const int eo = esize_of(dout);
+    e->on = 1;
+    e->act = ep->activation;
+    e->alpha = ep->alpha;
+    e->beta = ep->beta;
+    e->scale = ep->scale;
+    e->bias = ep->bias;
+    e->res = ep->residual;
+    e->ldr = ep->residual ? ep->ldr : 0;
+    if (M == 0 || N == 0) return TG_OK;
+    uintptr_t c0, c1;
+    span(c, M, N, ldc, eo, &c0, &c1);
+    for (const float *v : {ep->scale, ep->bias}) {
+        if (v == nullptr) continue;
+        if (reinterpret_cast<uintptr_t>(v) % 4) return TG_ERR_INVALID_VALUE;
+        const uintptr_t v0 = reinterpret_cast<uintptr_t>(v);
+        if (overlaps(c0, c1, v0, v0 + static_cast<uintptr_t>(N) * 4)) return TG_ERR_INVALID_VALUE;
+    }
+    if (ep->residual) {
+        if (ep->ldr < N || ep->ldr > (int64_t(1) << 36)) return TG_ERR_INVALID_VALUE;
+        if (reinterpret_cast<uintptr_t>(ep->residual) % eo) return TG_ERR_INVALID_VALUE;
+        const bool in_place = ep->residual == c && ep->ldr == ldc;
+        uintptr_t r0, r1;
+        span(ep->residual, M, N, ep->ldr, eo, &r0, &r1);
+        if (!in_place && overlaps(c0, c1, r0, r1)) return TG_ERR_INVALID_VALUE;
+        e->res_vector = aligned16(ep->residual) && (ep->ldr * eo) % 16 == 0;
+    }
+    e->sb_vector = (!ep->scale || aligned16(ep->scale)) && (!ep->bias || aligned16(ep->bias));
+    return TG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -720,6 +762,29 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
         return cuda_status(cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s));
     return enqueue(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, s, opt, dev, Batch{},
                    nullptr);
+}
+
+tg_status tg_gemm_fused(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda,
+                        const void *b, int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in,
+                        tg_dtype dtype_out, const tg_epilogue *epilogue, void *stream,
+                        const tg_options *opt) {
+    tg_status st = validate(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, opt);
+    if (st != TG_OK) return st;
+    tg::EpiParams e;
+    st = validate_epilogue(M, N, c, ldc, dtype_out, epilogue, &e);
+    if (st != TG_OK) return st;
+    if (epilogue == nullptr)
+        return tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, opt);
+    if (M == 0 || N == 0) return TG_OK;
+    DeviceState *dev = nullptr;
+    st = device_state(&dev);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)   // the epilogue of the empty sum
+        return cuda_status(tg::launch_splitk_reduce(nullptr, 0, M, N, c, ldc,
+                                                    out_kind_of(dtype_out), 0, s, &e));
+    return enqueue(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, s, opt, dev, Batch{},
+                   nullptr, &e);
 }
 
 tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,

@@ -15,6 +15,22 @@ enum OutKind : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
 // was recorded (role << 16 | detail).
 enum FailRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
 
+enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
+
+// Fused epilogue, applied to each FP32 accumulator value before its single
+// rounding to the output type:  D = act(alpha * scale[n] * acc + bias[n]) +
+// beta * R[m, n].  With on == 0 no other field is read.
+struct EpiParams {
+    int32_t on, act;
+    float alpha, beta;
+    const float *scale;         // [N] or null (1)
+    const float *bias;          // [N] or null (0)
+    const void *res;            // [M][ldr] in the output type, or null
+    int64_t ldr;                // elements
+    int32_t res_vector;         // res base and pitch allow 16-byte loads
+    int32_t sb_vector;          // scale and bias allow 16-byte loads
+};
+
 // Parameters of the tensor-core GEMM kernel (one persistent launch).
 struct TcParams {
     int32_t M, N, K;
@@ -45,6 +61,7 @@ struct TcParams {
     // every batch (stride 0); C of batch z starts at c + z * stride_c.
     int32_t batch, a_batched, b_batched, pad2_;
     int64_t stride_c;           // elements
+    EpiParams epi;              // applied where C is written (splits == 1)
 };
 
 // Parameters of the small-M kernel (gemm_skinny.cu): C^T = B^T A^T with NT
@@ -65,6 +82,7 @@ struct SkParams {
     void *c;
     int *status;
     uint64_t timeout_ns;
+    EpiParams epi;
 };
 
 // gemm_skinny.cu -- mp: MMA N used for the M rows (16, 32, 64, 128); nt: output
@@ -97,8 +115,10 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
                              int64_t rows, int64_t cols, int esize, cudaStream_t stream);
 cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                                   int64_t rows, int64_t cols, int esize, cudaStream_t stream);
+// C = the sum of the `splits` partial planes, through the epilogue `epi`
+// (splits == 0: the empty sum, i.e. the epilogue of zero).
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N,
                                  void *c, int64_t ldc, int out_kind, int c_vector,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const EpiParams *epi = nullptr);
 
 }  // namespace tg
