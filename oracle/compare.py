@@ -3,12 +3,12 @@
 TEST INFRASTRUCTURE (see the package docstring).
 
 Rule, per element (C_ref and S from ``gemm_ref``):
-  * f16 / bf16 operands:  |C - C_ref| <= 2e-3 * S + ulp_out(C_ref)
+  * f16 / bf16 / FP8 (e4m3, e5m2) operands:  |C - C_ref| <= 2e-3 * S + ulp_out(C_ref)
   * f32 operands contracted at TF32:  |C - C_ref| <= 1e-2 * S + ulp_out(C_ref)
 where S = sum_k |A[m,k] * B[k,n]| and ulp_out(x) is the spacing of the output
 format at |x| (the subnormal spacing below the smallest normal).
 
-Why these hold with margin: the products of f16/bf16 operands are exact in the
+Why these hold with margin: the products of f16/bf16 (and FP8) operands are exact in the
 FP32 accumulator, so the accumulated error is at most about K * 2^-24 * S
 (2.4e-4 * S at K = 4096, 9.8e-4 * S at K = 16384), plus half an ulp for the final
 rounding to the output format.  TF32 rounds each f32 operand to 10 fraction
@@ -22,7 +22,7 @@ import numpy as np
 # (exponent of the smallest normal, fraction bits) per output format
 _FORMAT = {"f16": (-14, 10), "bf16": (-126, 7), "f32": (-126, 23)}
 
-REL_TOL = {"f16": 2e-3, "bf16": 2e-3, "f32": 1e-2}
+REL_TOL = {"f16": 2e-3, "bf16": 2e-3, "f32": 1e-2, "e4m3": 2e-3, "e5m2": 2e-3}
 
 
 def rel_tol_for(dtype_in: str) -> float:

@@ -14,8 +14,9 @@
  * C[row,col] is the sum over `inner` of A[row,inner]*B[inner,col], computed
  * first as a plain three-loop CPU version.  Here the sum is carried in IEEE
  * double, term by term in increasing `inner` (k) order, starting from zero.
- * Every product of two f16, bf16 or f32 values is exact in double (at most
- * 24+24 significand bits), so the only rounding is the double addition.
+ * Every product of two f16, bf16, f32 or FP8 (E4M3 / E5M2) values is exact in
+ * double (at most 24+24 significand bits), so the only rounding is the double
+ * addition.
  *
  * Alongside C the oracle returns S[m,n] = sum_k |A[m,k]*B[k,n]|, the scale that
  * the floating-point tolerance is stated against.
@@ -31,7 +32,17 @@
 #endif
 
 /* Operand / result format tags (the oracle's own numbering). */
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
+
+static int fmt_bytes(int fmt)
+{
+    switch (fmt) {
+    case ORC_F16: case ORC_BF16: return 2;
+    case ORC_F32: return 4;
+    case ORC_E4M3: case ORC_E5M2: return 1;
+    default: return 0;
+    }
+}
 
 int orc_num_threads(void)
 {
@@ -67,13 +78,48 @@ static double decode_bits(uint32_t w, int exp_bits, int frac_bits)
     return sign ? -v : v;
 }
 
+/* 8-bit floating point, the OCP FP8 formats (OCP 8-bit Floating Point
+ * Specification, 2023):
+ *   E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits, IEEE-like (an
+ *         all-ones exponent is Inf or NaN) -- decode_bits applies as is.
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits, NO infinities:
+ *         the all-ones exponent is an ordinary binade except for fraction 111,
+ *         the only NaN (S.1111.111), so the largest finite value is
+ *         1.75 * 2^8 = 448.
+ */
+static double decode_e4m3(uint32_t w)
+{
+    const int sign = (int)((w >> 7) & 1u);
+    const uint32_t e = (w >> 3) & 0xFu;
+    const uint32_t f = w & 7u;
+    double v;
+    if (e == 0xFu && f == 7u)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, 1 - 7 - 3);
+    else
+        v = ldexp((double)(f | 8u), (int)e - 7 - 3);
+    return sign ? -v : v;
+}
+
 double orc_decode_one(int fmt, uint32_t bits)
 {
     switch (fmt) {
     case ORC_F16: return decode_bits(bits & 0xFFFFu, 5, 10);
     case ORC_BF16: return decode_bits(bits & 0xFFFFu, 8, 7);
     case ORC_F32: return decode_bits(bits, 8, 23);
+    case ORC_E4M3: return decode_e4m3(bits & 0xFFu);
+    case ORC_E5M2: return decode_bits(bits & 0xFFu, 5, 2);
     default: return NAN;
+    }
+}
+
+static uint32_t load_bits(int fmt, const void *src, int64_t i)
+{
+    switch (fmt_bytes(fmt)) {
+    case 1: return ((const uint8_t *)src)[i];
+    case 2: return ((const uint16_t *)src)[i];
+    default: return ((const uint32_t *)src)[i];
     }
 }
 
@@ -81,15 +127,12 @@ double orc_decode_one(int fmt, uint32_t bits)
  * dense rows x cols double array.  Returns 0, or -1 on an unknown format. */
 int orc_decode(int fmt, const void *src, int64_t rows, int64_t cols, int64_t ld, double *dst)
 {
-    if (fmt != ORC_F16 && fmt != ORC_BF16 && fmt != ORC_F32)
+    if (fmt_bytes(fmt) == 0)
         return -1;
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
-        for (int64_t c = 0; c < cols; ++c) {
-            uint32_t w = (fmt == ORC_F32) ? ((const uint32_t *)src)[r * ld + c]
-                                          : ((const uint16_t *)src)[r * ld + c];
-            dst[r * cols + c] = orc_decode_one(fmt, w);
-        }
+        for (int64_t c = 0; c < cols; ++c)
+            dst[r * cols + c] = orc_decode_one(fmt, load_bits(fmt, src, r * ld + c));
     }
     return 0;
 }
@@ -130,12 +173,45 @@ static uint32_t encode_bits(double x, int exp_bits, int frac_bits)
     return sign | ((uint32_t)(e + bias) << frac_bits) | frac;
 }
 
+/* E4M3 round to nearest, ties to even.  Rounding works as in encode_bits
+ * with the top binade (2^8) ordinary; a magnitude that rounds to 480 or more
+ * (the would-be code S.1111.111) has no finite encoding and becomes the NaN
+ * S.1111.111 (there is no Inf). */
+static uint32_t encode_e4m3(double x)
+{
+    const uint32_t sign = signbit(x) ? 0x80u : 0u;
+    if (isnan(x))
+        return sign | 0x7Fu;
+    const double ax = fabs(x);
+    if (isinf(ax))
+        return sign | 0x7Fu;
+    if (ax == 0.0)
+        return sign;
+    int E;
+    (void)frexp(ax, &E);
+    int e = E - 1;
+    if (e < -6)
+        e = -6;                            /* subnormal range: quantum 2^-9 */
+    const double quantum = ldexp(1.0, e - 3);
+    const double v = rint(ax / quantum) * quantum;
+    if (v >= 480.0)
+        return sign | 0x7Fu;
+    if (v < ldexp(1.0, -6))
+        return sign | (uint32_t)(v / ldexp(1.0, -9));
+    (void)frexp(v, &E);
+    e = E - 1;
+    const uint32_t frac = (uint32_t)(v / ldexp(1.0, e - 3)) - 8u;
+    return sign | ((uint32_t)(e + 7) << 3) | frac;
+}
+
 uint32_t orc_encode_one(int fmt, double x)
 {
     switch (fmt) {
     case ORC_F16: return encode_bits(x, 5, 10);
     case ORC_BF16: return encode_bits(x, 8, 7);
     case ORC_F32: return encode_bits(x, 8, 23);
+    case ORC_E4M3: return encode_e4m3(x);
+    case ORC_E5M2: return encode_bits(x, 5, 2);
     default: return 0;
     }
 }
@@ -143,15 +219,18 @@ uint32_t orc_encode_one(int fmt, double x)
 /* Encode n doubles into the bit patterns of `fmt` (uint16 or uint32 elements). */
 int orc_encode(int fmt, const double *src, int64_t n, void *dst)
 {
-    if (fmt != ORC_F16 && fmt != ORC_BF16 && fmt != ORC_F32)
+    const int nb = fmt_bytes(fmt);
+    if (nb == 0)
         return -1;
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         uint32_t w = orc_encode_one(fmt, src[i]);
-        if (fmt == ORC_F32)
+        if (nb == 4)
             ((uint32_t *)dst)[i] = w;
-        else
+        else if (nb == 2)
             ((uint16_t *)dst)[i] = (uint16_t)w;
+        else
+            ((uint8_t *)dst)[i] = (uint8_t)w;
     }
     return 0;
 }

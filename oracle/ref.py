@@ -14,9 +14,9 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32 = 0, 1, 2
-FORMATS = {"f16": F16, "bf16": BF16, "f32": F32}
-_BITS = {F16: np.uint16, BF16: np.uint16, F32: np.uint32}
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+FORMATS = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "e5m2": E5M2}
+_BITS = {F16: np.uint16, BF16: np.uint16, F32: np.uint32, E4M3: np.uint8, E5M2: np.uint8}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")

@@ -30,6 +30,14 @@ MUTANTS = {
     "encode_bias": ("(uint32_t)(e + bias) << frac_bits", "(uint32_t)(e + bias - 1) << frac_bits"),
     "encode_no_overflow": ("if (v >= ldexp(1.0, emax + 1))", "if (0)"),
     "encode_late_overflow": ("if (v >= ldexp(1.0, emax + 1))", "if (v > ldexp(1.0, emax + 2))"),
+    "e4m3_ieee_top_binade": ("if (e == 0xFu && f == 7u)", "if (e == 0xFu)"),
+    "e4m3_bias": ("ldexp((double)(f | 8u), (int)e - 7 - 3)", "ldexp((double)(f | 8u), (int)e - 8 - 3)"),
+    "e4m3_subnormal_scale": ("ldexp((double)f, 1 - 7 - 3)", "ldexp((double)f, -7 - 3)"),
+    "e4m3_encode_overflow_early": ("if (v >= 480.0)", "if (v >= 448.0)"),
+    "e4m3_encode_truncates": ("const double v = rint(ax / quantum) * quantum;\n    if (v >= 480.0)",
+                              "const double v = floor(ax / quantum) * quantum;\n    if (v >= 480.0)"),
+    "e5m2_as_e4m3": ("case ORC_E5M2: return decode_bits(bits & 0xFFu, 5, 2);",
+                     "case ORC_E5M2: return decode_bits(bits & 0xFFu, 4, 3);"),
 }
 
 
@@ -84,6 +92,38 @@ def battery(lib) -> list[str]:
         want = x.astype(np.float16).view(np.uint16)
     if not np.array_equal(ref.encode(x, "f16", lib=lib), want):
         failed.append("encode_f16")
+    failed += fp8_pins(lib)
+    return failed
+
+
+def fp8_pins(lib) -> list[str]:
+    """FP8 decode of all 256 patterns and encode of random values against
+    torch's float8 types; the worked example exact in E4M3."""
+    import torch
+    failed = []
+    allp = np.arange(256, dtype=np.uint8)
+    for fmt, tdt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        want = torch.from_numpy(allp).view(tdt).to(torch.float64).numpy()
+        got = ref.decode(allp, fmt, lib=lib)[0]
+        if not ((got == want) | (np.isnan(got) & np.isnan(want))).all():
+            failed.append(f"decode_{fmt}")
+        top = 500.0 if fmt == "e4m3" else 60000.0
+        x = np.random.default_rng(5).uniform(-top, top, 20000)
+        x = np.concatenate([x, np.ldexp(np.random.default_rng(6).uniform(-1, 1, 5000), -8),
+                            [464.0, 470.0, 1 + 2.0 ** -4, 1 + 3 * 2.0 ** -4, 2.0 ** -10]])
+        if fmt == "e5m2":
+            x = x[np.abs(x) < 57344.0]
+        tw = torch.from_numpy(x).to(tdt).view(torch.uint8).numpy()
+        if not np.array_equal(ref.encode(x, fmt, lib=lib), tw):
+            failed.append(f"encode_{fmt}")
+    g = read_golden("worked_example.txt")
+    A = np.array(parse_matrix(g["A"]))
+    B = np.array(parse_matrix(g["B"]))
+    C = np.array(parse_matrix(g["C"]))
+    got, _ = ref.gemm_ref_bits(ref.encode(A, "e4m3", lib=lib), ref.encode(B, "e4m3", lib=lib),
+                               K=3, N=2, fmt="e4m3", lib=lib)
+    if not np.array_equal(got, C):
+        failed.append("worked_example_e4m3")
     return failed
 
 

@@ -17,7 +17,8 @@ Distributions (the workloads' value recipes):
   * ``int``      -- integers drawn uniformly from {-2, ..., 2}
 The float64 draw is then rounded to nearest-even into the operand dtype
 (``f16`` and ``f32`` by numpy's conversion; ``bf16`` by rounding the float32
-value's upper half).
+value's upper half; the 8-bit ``e4m3`` / ``e5m2`` by scaling to an integer
+multiple of the value's quantum, see ``_to_fp8``).
 """
 from __future__ import annotations
 
@@ -27,9 +28,15 @@ GOLDEN_GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-DTYPES = ("f16", "bf16", "f32")
-ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4}
-BITS_NP = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32}
+DTYPES = ("f16", "bf16", "f32", "e4m3", "e5m2")
+ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+BITS_NP = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32, "e4m3": np.uint8,
+           "e5m2": np.uint8}
+
+# (exponent bias, fraction bits, largest finite magnitude) of the 8-bit formats
+# of the OCP 8-bit Floating Point Specification: E4M3 has no infinities (its
+# only NaN is S.1111.111), E5M2 follows IEEE 754.
+_FP8 = {"e4m3": (7, 3, 448.0), "e5m2": (15, 2, 57344.0)}
 
 # Seeds used for the named workloads (A and B streams).
 SEED_A = 0x5EED0001
@@ -65,12 +72,37 @@ def draw_f64(dist: str, seed: int, start: int, count: int, sigma: float = 0.02) 
     raise ValueError(f"unknown distribution {dist!r}")
 
 
+def _to_fp8(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round to nearest-even into E4M3 / E5M2 bit patterns.  Draws here are
+    small (|x| <= 2 for the uniform and integer recipes), far from the
+    formats' overflow; larger magnitudes saturate to the largest finite value
+    (not used by any workload)."""
+    bias, frac, vmax = _FP8[dtype]
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    ax = np.minimum(np.abs(x), vmax)
+    emin = 1 - bias
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, emin)
+    q = np.rint(np.ldexp(ax, (frac - e).astype(np.int64)))       # ties to even
+    # q in [0, 2^(frac+1)]: q == 2^(frac+1) is the next binade's leading value
+    up = q >= 2 ** (frac + 1)
+    e = np.where(up, e + 1, e)
+    q = np.where(up, q / 2, q)
+    normal = q >= 2 ** frac
+    code = np.where(normal, (e + bias) * 2 ** frac + (q - 2 ** frac), q)
+    return sign | code.astype(np.uint8)
+
+
 def f64_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     """Round float64 draws to the operand dtype; returns the raw bit patterns."""
     if dtype == "f16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "f32":
         return x.astype(np.float32).view(np.uint32)
+    if dtype in _FP8:
+        return _to_fp8(x, dtype)
     if dtype == "bf16":
         w = x.astype(np.float32).view(np.uint32).astype(np.uint64)
         w = w + np.uint64(0x7FFF) + ((w >> np.uint64(16)) & np.uint64(1))
@@ -102,7 +134,7 @@ def matrix_bits(rows: int, cols: int, dtype: str, dist: str, seed: int,
 
 
 def nan_bits(dtype: str) -> int:
-    return {"f16": 0x7E00, "bf16": 0x7FC0, "f32": 0x7FC00000}[dtype]
+    return {"f16": 0x7E00, "bf16": 0x7FC0, "f32": 0x7FC00000, "e4m3": 0x7F, "e5m2": 0x7E}[dtype]
 
 
 def problem(M: int, N: int, K: int, dtype: str, dist: str = "uniform",
