@@ -26,6 +26,13 @@
  *     (TG_F32,  TG_F32)  -- FP32 operands contracted at TF32 precision (10
  *                           fraction bits), FP32 accumulate; the "TF32" input
  *                           precision of the teenygrad page, section "T::dot".
+ *     (TG_E4M3 or TG_E5M2, TG_F16 / TG_BF16 / TG_F32)
+ *                        -- 8-bit floating-point operands, FP32 accumulate: the
+ *                           FP8 input path of "Triton tiled matmul"
+ *                           (llm-systems-cookbook), section "Exercises", item 2.
+ *                           Row pitches (lda, ldb) and bases of A and B that are
+ *                           not multiples of 16 bytes are packed first; the
+ *                           small-M streaming kernel is not used for FP8.
  * Any other pair returns TG_ERR_UNSUPPORTED.
  *
  * Ownership.  a, b and c are DEVICE pointers owned by the caller and must stay
@@ -58,12 +65,14 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 3
+#define TG_ABI_VERSION 4
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
     TG_BF16 = 1,  /* bfloat16 */
-    TG_F32 = 2    /* IEEE 754 binary32 */
+    TG_F32 = 2,   /* IEEE 754 binary32 */
+    TG_E4M3 = 3,  /* OCP FP8 E4M3 (bias 7, 3 fraction bits, no Inf; max 448) */
+    TG_E5M2 = 4   /* OCP FP8 E5M2 (bias 15, 2 fraction bits, IEEE-like) */
 } tg_dtype;
 
 typedef enum tg_status {

@@ -8,12 +8,14 @@ import oracle
 import tiled_matrix_multiplication_gb300 as tg
 from tiled_matrix_multiplication_gb300 import inputs
 
-_INT_VIEW = {"f16": np.int16, "bf16": np.int16, "f32": np.int32}
+_INT_VIEW = {"f16": np.int16, "bf16": np.int16, "f32": np.int32, "e4m3": np.uint8,
+             "e5m2": np.uint8}
 
 
 def torch_dtype(name):
     import torch
-    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[name]
 
 
 def to_device(bits: np.ndarray, dtype: str):
@@ -25,7 +27,8 @@ def to_device(bits: np.ndarray, dtype: str):
 
 def to_bits(t, dtype: str) -> np.ndarray:
     import torch
-    ints = {"f16": torch.int16, "bf16": torch.int16, "f32": torch.int32}[dtype]
+    ints = {"f16": torch.int16, "bf16": torch.int16, "f32": torch.int32, "e4m3": torch.uint8,
+            "e5m2": torch.uint8}[dtype]
     host = t.detach().contiguous().view(ints).cpu().numpy()
     return host.view(inputs.BITS_NP[dtype])
 

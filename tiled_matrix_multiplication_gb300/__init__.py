@@ -15,7 +15,8 @@ and streams passed as integers.  ``bmm`` runs a batch of products
 """
 from __future__ import annotations
 
-from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_ERR_ARCH, TG_ERR_CUDA,
+from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_E4M3, TG_E5M2, TG_ERR_ARCH,
+                   TG_ERR_CUDA,
                    TG_ERR_INVALID_VALUE, TG_ERR_NOT_IMPLEMENTED, TG_ERR_OUT_OF_MEMORY,
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
                    TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, NOALLOC_SCRATCH_BYTES, TgError,
@@ -34,7 +35,7 @@ __all__ = [
     "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",
     "tg_plan_gemm_strided_batched", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
     "EXPORTS", "LIB_PATH",
-    "TG_F16", "TG_BF16", "TG_F32", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
+    "TG_F16", "TG_BF16", "TG_F32", "TG_E4M3", "TG_E5M2", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
     "TG_ERR_OUT_OF_MEMORY", "TG_ERR_CUDA", "TG_ERR_ARCH", "TG_ERR_TIMEOUT",
     "TG_ERR_NOT_IMPLEMENTED", "TG_PATH_AUTO", "TG_PATH_TC", "TG_PATH_TC_PAIR", "TG_PATH_SKINNY",
 ]
@@ -45,7 +46,8 @@ def dtype_code(dtype) -> int:
     if isinstance(dtype, str):
         return DTYPE_CODES[dtype]
     import torch
-    table = {torch.float16: TG_F16, torch.bfloat16: TG_BF16, torch.float32: TG_F32}
+    table = {torch.float16: TG_F16, torch.bfloat16: TG_BF16, torch.float32: TG_F32,
+             torch.float8_e4m3fn: TG_E4M3, torch.float8_e5m2: TG_E5M2}
     if dtype not in table:
         raise TgError(TG_ERR_UNSUPPORTED, f"dtype {dtype}")
     return table[dtype]

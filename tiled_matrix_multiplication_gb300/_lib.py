@@ -13,8 +13,8 @@ import threading
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
 
-TG_F16, TG_BF16, TG_F32 = 0, 1, 2
-DTYPE_CODES = {"f16": TG_F16, "bf16": TG_BF16, "f32": TG_F32}
+TG_F16, TG_BF16, TG_F32, TG_E4M3, TG_E5M2 = 0, 1, 2, 3, 4
+DTYPE_CODES = {"f16": TG_F16, "bf16": TG_BF16, "f32": TG_F32, "e4m3": TG_E4M3, "e5m2": TG_E5M2}
 
 TG_OK = 0
 TG_ERR_INVALID_VALUE = 1

@@ -115,7 +115,11 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
     if (rows <= 0 || cols <= 0) return cudaSuccess;
     const int threads = 256;
     const int blocks = grid_for(rows * cols, threads);
-    if (esize == 2)
+    if (esize == 1)
+        pack_rows_kernel<uint8_t><<<blocks, threads, 0, stream>>>(
+            static_cast<const uint8_t *>(src), ld_src, static_cast<uint8_t *>(dst), ld_dst, rows,
+            cols);
+    else if (esize == 2)
         pack_rows_kernel<uint16_t><<<blocks, threads, 0, stream>>>(
             static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst, rows,
             cols);

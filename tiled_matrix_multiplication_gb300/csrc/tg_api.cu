@@ -40,19 +40,28 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-int esize_of(tg_dtype t) { return t == TG_F32 ? 4 : 2; }
+int esize_of(tg_dtype t) { return t == TG_F32 ? 4 : (t == TG_E4M3 || t == TG_E5M2 ? 1 : 2); }
 
-bool valid_dtype(int t) { return t == TG_F16 || t == TG_BF16 || t == TG_F32; }
+bool is_fp8(int t) { return t == TG_E4M3 || t == TG_E5M2; }
+
+bool valid_dtype(int t) { return t == TG_F16 || t == TG_BF16 || t == TG_F32 || is_fp8(t); }
 
 bool supported_pair(tg_dtype in, tg_dtype out) {
     if (in == TG_F16) return out == TG_F16 || out == TG_F32;
     if (in == TG_BF16) return out == TG_BF16 || out == TG_F32;
     if (in == TG_F32) return out == TG_F32;
+    if (is_fp8(in)) return out == TG_F16 || out == TG_BF16 || out == TG_F32;
     return false;
 }
 
 int in_kind_of(tg_dtype t) {
-    return t == TG_F16 ? tg::IN_F16 : (t == TG_BF16 ? tg::IN_BF16 : tg::IN_TF32);
+    switch (t) {
+    case TG_F16: return tg::IN_F16;
+    case TG_BF16: return tg::IN_BF16;
+    case TG_E4M3: return tg::IN_E4M3;
+    case TG_E5M2: return tg::IN_E5M2;
+    default: return tg::IN_TF32;
+    }
 }
 
 int out_kind_of(tg_dtype t) {
@@ -117,7 +126,7 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128,
             // K split over a cluster of 1, 2, 4 or 8 CTAs (none of them empty),
             // 128, 256 or 512 columns per CTA
-            if (din == TG_F32 || M > 128) return TG_ERR_UNSUPPORTED;
+            if (din == TG_F32 || is_fp8(din) || M > 128) return TG_ERR_UNSUPPORTED;
             if (opt->block_n && !tg::skinny_supported(tg::skinny_rows(M), opt->block_n))
                 return TG_ERR_UNSUPPORTED;
             const int64_t s = opt->splits;
@@ -261,7 +270,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // Small M with 16-bit operands: the transposed streaming kernel (one tile
     // holds all rows; work is spread over 128-column tiles and K splits).
     const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
-    const bool skinny_ok = din != TG_F32 && M <= 128 && (forced_skinny || !(opt && opt->block_n)) &&
+    const bool skinny_ok = din != TG_F32 && !is_fp8(din) && M <= 128 &&
+                           (forced_skinny || !(opt && opt->block_n)) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&
                            batch <= kMaxGridY;
     if (skinny_ok) {
@@ -433,6 +443,7 @@ tg_status device_state(DeviceState **out) {
 }
 
 CUtensorMapDataType tma_type(tg_dtype t) {
+    if (is_fp8(t)) return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes moved as they are
     return t == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                        : (t == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);

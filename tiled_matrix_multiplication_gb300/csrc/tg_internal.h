@@ -8,7 +8,12 @@
 
 namespace tg {
 
-enum InKind : int { IN_F16 = 0, IN_BF16 = 1, IN_TF32 = 2 };
+enum InKind : int { IN_F16 = 0, IN_BF16 = 1, IN_TF32 = 2, IN_E4M3 = 3, IN_E5M2 = 4 };
+
+// Bytes of one operand element.
+__host__ __device__ constexpr int in_esize(int in_kind) {
+    return in_kind == IN_TF32 ? 4 : (in_kind == IN_E4M3 || in_kind == IN_E5M2 ? 1 : 2);
+}
 enum OutKind : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
 
 // Device status word layout: [0] first tg_status code recorded, [1] where it
@@ -107,6 +112,17 @@ int tc_max_clusters(int cluster_size);
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream);
+// The instantiations behind launch_gemm_tc, one translation unit per operand
+// type (gemm_tc_f16.cu, gemm_tc_tf32.cu, gemm_tc_fp8.cu).
+cudaError_t launch_gemm_tc_16bit(int in_kind, int block_n, bool pair, int mc,
+                                 const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                 const TcParams &p, int ctas, cudaStream_t stream);
+cudaError_t launch_gemm_tc_tf32(int block_n, bool pair, int mc, const CUtensorMap &tmA,
+                                const CUtensorMap &tmB, const TcParams &p, int ctas,
+                                cudaStream_t stream);
+cudaError_t launch_gemm_tc_fp8(int in_kind, int block_n, bool pair, int mc,
+                               const CUtensorMap &tmA, const CUtensorMap &tmB,
+                               const TcParams &p, int ctas, cudaStream_t stream);
 cudaError_t status_word_address(int **out);
 cudaError_t set_smem_once(const void *kernel, int bytes);
 

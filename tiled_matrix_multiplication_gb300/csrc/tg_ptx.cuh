@@ -328,31 +328,29 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem], both operands described by smem descriptors.
-// KIND 0: kind::f16 (f16 / bf16 operands), KIND 1: kind::tf32.
+// KIND 0: kind::f16 (f16 / bf16 operands), 1: kind::tf32, 2: kind::f8f6f4
+// (e4m3 / e5m2 operands).
+#define TG_UMMA_SS(KINDSTR, CGSTR)                                                          \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                       \
+                 "tcgen05.mma.cta_group::" CGSTR ".kind::" KINDSTR " [%0], %1, %2, %3, p;\n\t}" \
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate))
 template <int KIND, int CTA_GROUP>
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                         uint32_t idesc, uint32_t accumulate) {
     if constexpr (KIND == 0 && CTA_GROUP == 1)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+        TG_UMMA_SS("f16", "1");
     else if constexpr (KIND == 1 && CTA_GROUP == 1)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+        TG_UMMA_SS("tf32", "1");
+    else if constexpr (KIND == 2 && CTA_GROUP == 1)
+        TG_UMMA_SS("f8f6f4", "1");
     else if constexpr (KIND == 0 && CTA_GROUP == 2)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+        TG_UMMA_SS("f16", "2");
+    else if constexpr (KIND == 1 && CTA_GROUP == 2)
+        TG_UMMA_SS("tf32", "2");
     else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+        TG_UMMA_SS("f8f6f4", "2");
 }
+#undef TG_UMMA_SS
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
@@ -438,9 +436,10 @@ __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t lbo_by
     return d;
 }
 
-// Instruction descriptor for kind::f16 / kind::tf32 with an FP32 accumulator:
+// Instruction descriptor for kind::f16 / tf32 / f8f6f4 with an FP32 accumulator:
 //   [4,6) D format (1 = F32)   [7,10) A format   [10,13) B format
-//   (kind::f16: 0 = F16, 1 = BF16; kind::tf32: 2 = TF32)
+//   (kind::f16: 0 = F16, 1 = BF16; kind::tf32: 2 = TF32; kind::f8f6f4:
+//   0 = E4M3, 1 = E5M2)
 //   [15] A major (0 = K-major)  [16] B major (1 = MN-major)
 //   [17,23) N >> 3              [24,29) M >> 4
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t a_mn_major,
