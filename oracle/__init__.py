@@ -19,11 +19,11 @@ Every pin that ties these functions to the pages or to mathematics lives in
 """
 from .ref import (F16, BF16, F32, FORMATS, build, decode, encode, gemm_ref,
                   gemm_ref_bits, num_threads, lib_path)
-from .compare import ulp, tolerance, check_close, rel_tol_for
+from .compare import ulp, tolerance, check_close, rel_tol_for, rel_tol_3xtf32
 from . import epilogue, tiled_model
 
 __all__ = [
     "F16", "BF16", "F32", "FORMATS", "build", "decode", "encode", "gemm_ref",
     "gemm_ref_bits", "num_threads", "lib_path", "ulp", "tolerance", "check_close",
-    "rel_tol_for", "tiled_model", "epilogue",
+    "rel_tol_for", "rel_tol_3xtf32", "tiled_model", "epilogue",
 ]

@@ -43,11 +43,28 @@ def tolerance(C_ref: np.ndarray, S: np.ndarray, dtype_in: str, dtype_out: str) -
     return REL_TOL[dtype_in] * S + ulp(C_ref, dtype_out)
 
 
+def rel_tol_3xtf32(K: int) -> float:
+    """Relative bound (times S) for FP32 operands contracted as three TF32
+    products ("Matrix Multiplication", teenygrad docs, section "T::dot": TF32x3,
+    three TF32 products recovering most of FP32's precision).
+
+    Each operand x = hi + lo + r with hi, lo TF32 values and |r| <= 2^-22 |x|;
+    the three kept products hi*hi + lo*hi + hi*lo (each exact in FP32) miss
+    lo*lo and the r terms, at most about 3 * 2^-22 |a b| per product: 2^-20.
+    Their 3K terms are summed in FP32: at most 3K * 2^-24 * S for sequential
+    round-to-nearest addition, doubled (3K * 2^-23) for an accumulator that may
+    truncate.
+    """
+    return 2.0 ** -20 + 3.0 * K * 2.0 ** -23
+
+
 def check_close(C: np.ndarray, C_ref: np.ndarray, S: np.ndarray, dtype_in: str,
-                dtype_out: str):
-    """Returns ``(ok, report)``; ``report`` describes the worst element."""
+                dtype_out: str, rel: float | None = None):
+    """Returns ``(ok, report)``; ``report`` describes the worst element.
+    ``rel`` overrides the relative term of the rule (e.g. ``rel_tol_3xtf32``)."""
     C = np.asarray(C, dtype=np.float64)
-    tol = tolerance(C_ref, S, dtype_in, dtype_out)
+    tol = (tolerance(C_ref, S, dtype_in, dtype_out) if rel is None
+           else rel * np.asarray(S, dtype=np.float64) + ulp(C_ref, dtype_out))
     err = np.abs(C - C_ref)
     bad = ~(err <= tol)  # NaN in C counts as a failure
     ok = not bool(bad.any())
