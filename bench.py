@@ -64,6 +64,10 @@ WORKLOADS = {
                         "prefill MLP up/gate (each) 8192x14336x4096, BF16 N(0,0.02)"),
     "prefill_down_bf16": (8192, 4096, 14336, "bf16", "bf16", "normal",
                           "prefill MLP down 8192x4096x14336, BF16 N(0,0.02)"),
+    "square4096_e4m3": (4096, 4096, 4096, "e4m3", "f16", "uniform",
+                        "square GEMM 4096^3, FP8 E4M3 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square8192_e4m3": (8192, 8192, 8192, "e4m3", "f16", "uniform",
+                        "square GEMM 8192^3, FP8 E4M3 in U[-1,1), FP32 accumulate, FP16 out"),
     "tf32_2048": (2048, 2048, 2048, "f32", "f32", "uniform",
                   "FP32 operands at TF32 2048^3, FP32 out"),
     "skinny1_f16": (1, 8192, 8192, "f16", "f16", "uniform", "skinny M=1, N=K=8192 FP16"),
@@ -81,7 +85,10 @@ WORKLOADS = {
 # products per call of the batched workloads (1 for every other workload)
 BATCH = {"batched16x2048_f16": 16, "batched64x1024_bf16": 64, "batched32x64x8192_f16": 32}
 DEFAULT_WORKLOAD = "square4096_f16"
-ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+# dense tensor-core peak of an operand type relative to BF16 (nominal ratios of
+# 4.5 : 2.25 : 1.1 PFLOP/s for FP8 : BF16 : TF32)
+PEAK_RATIO = {"f16": 1.0, "bf16": 1.0, "f32": 0.5, "e4m3": 2.0, "e5m2": 2.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -306,8 +313,10 @@ def run_ours(args, world, rank, local):
     M, N, K, din, dout, dist, desc = WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    iview = {"f16": np.int16, "bf16": np.int16, "f32": np.int32}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+           "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    iview = {"f16": np.int16, "bf16": np.int16, "f32": np.int32, "e4m3": np.uint8,
+             "e5m2": np.uint8}
 
     nb = BATCH.get(args.workload, 1)
     a_bits = np.stack([inputs.matrix_bits(M, K, din, dist, inputs.SEED_A + z) for z in range(nb)])
@@ -432,11 +441,11 @@ def run_ours(args, world, rank, local):
     else:
         bound, unit = "tensor", "TFLOP/s"
         achieved = flops / (kernel_ms * 1e-3) / 1e12
-        peak = float(pk["bf16_tflops"]) * (0.5 if din == "f32" else 1.0)
+        peak = float(pk["bf16_tflops"]) * PEAK_RATIO[din]
     roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
             "peak_source": f"{pk_kind} ({'hbm_gbs' if skinny else 'bf16_tflops'} burst"
-                           f"{', x0.5 nominal TF32/BF16 ratio' if din == 'f32' and not skinny else ''})",
+                           f"{'' if skinny or PEAK_RATIO[din] == 1.0 else f', x{PEAK_RATIO[din]} nominal ratio to BF16'})",
             "kernel": ("gemm_skinny_kernel" if plan["path"] == tg.TG_PATH_SKINNY else "gemm_tc_kernel")
                       + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
             "launch_ms": round(kernel_ms, 5)}

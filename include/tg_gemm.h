@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 4
+#define TG_ABI_VERSION 5
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -108,7 +108,31 @@ typedef struct tg_options {
                              ranges (2..8; partials summed in the kernel); 0 = no */
     int32_t multicast;    /* CTA pairs only: 2 = clusters of two pairs that share A
                              tiles by TMA multicast, 1 = no sharing, 0 = planner */
+    int32_t f32_mode;     /* FP32 operands only (tg_f32_mode): TG_F32_TF32 (0) or
+                             TG_F32_3XTF32 (1) */
+    int32_t reserved;     /* must be 0 */
 } tg_options;
+
+/*
+ * How FP32 operands are contracted on the tensor cores.
+ *   TG_F32_TF32    one pass at TF32 precision (10 fraction bits per operand).
+ *   TG_F32_3XTF32  each operand x is split into TF32 parts x = hi + lo + r
+ *                  (hi = x rounded to TF32, lo = the rest rounded to TF32,
+ *                  |r| <= about 2^-22 |x|) and C = A_hi B_hi + A_lo B_hi +
+ *                  A_hi B_lo is accumulated in FP32: near-FP32 accuracy at three
+ *                  times the TF32 work.  The "TF32x3" alternative to IEEE mode
+ *                  that "Matrix Multiplication" (teenygrad docs, section
+ *                  "T::dot") lists among the input precisions.  The parts are
+ *                  written to workspace as A' = [A_hi | A_lo | A_hi] ([M, 3K])
+ *                  and B'^T = [B_hi | B_hi | B_lo]^T ([N, 3K]) and multiplied by
+ *                  the TF32 kernel over K' = 3K.  Operands with an infinite or
+ *                  NaN element, or of magnitude within 2^-11 of the largest
+ *                  FP32 value, may give NaN or Inf where a one-pass product is
+ *                  finite or +-Inf.  Other values of f32_mode, or a non-zero
+ *                  reserved field, return TG_ERR_INVALID_VALUE; TG_F32_3XTF32
+ *                  with other operand types, TG_ERR_UNSUPPORTED.
+ */
+typedef enum tg_f32_mode { TG_F32_TF32 = 0, TG_F32_3XTF32 = 1 } tg_f32_mode;
 
 /* What a call would launch (see tg_plan_gemm). */
 typedef struct tg_plan {
@@ -120,7 +144,9 @@ typedef struct tg_plan {
     int32_t ctas;          /* persistent grid size */
     int32_t pack_a;        /* 1 if A is first copied to an aligned workspace */
     int32_t pack_b;        /* 1 if B is first copied to an aligned workspace,
-                              2 if B is first transposed into it (TF32 operands) */
+                              2 if B is first transposed into it (TF32 operands),
+                              3 if B^T is split into TF32 parts (TG_F32_3XTF32;
+                              pack_a is then 3 as well) */
     int32_t c_vector;      /* 1 if C gets 16-byte vector stores */
     int32_t kernels;       /* kernel launches per call */
     int64_t tiles;         /* output tiles */

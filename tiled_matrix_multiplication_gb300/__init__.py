@@ -16,6 +16,7 @@ and streams passed as integers.  ``bmm`` runs a batch of products
 from __future__ import annotations
 
 from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_E4M3, TG_E5M2, TG_ERR_ARCH,
+                   TG_F32_3XTF32, TG_F32_TF32,
                    TG_ERR_CUDA,
                    TG_ERR_INVALID_VALUE, TG_ERR_NOT_IMPLEMENTED, TG_ERR_OUT_OF_MEMORY,
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
@@ -35,7 +36,7 @@ __all__ = [
     "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",
     "tg_plan_gemm_strided_batched", "NOALLOC_SCRATCH_BYTES", "tg_options", "tg_plan",
     "EXPORTS", "LIB_PATH",
-    "TG_F16", "TG_BF16", "TG_F32", "TG_E4M3", "TG_E5M2", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
+    "TG_F16", "TG_BF16", "TG_F32", "TG_E4M3", "TG_E5M2", "TG_F32_TF32", "TG_F32_3XTF32", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
     "TG_ERR_OUT_OF_MEMORY", "TG_ERR_CUDA", "TG_ERR_ARCH", "TG_ERR_TIMEOUT",
     "TG_ERR_NOT_IMPLEMENTED", "TG_PATH_AUTO", "TG_PATH_TC", "TG_PATH_TC_PAIR", "TG_PATH_SKINNY",
 ]

@@ -44,7 +44,8 @@ class tg_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("block_n", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("tail_splits", ctypes.c_int32), ("multicast", ctypes.c_int32)]
+                ("tail_splits", ctypes.c_int32), ("multicast", ctypes.c_int32),
+                ("f32_mode", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class tg_epilogue(ctypes.Structure):
@@ -128,12 +129,15 @@ def _code(dtype) -> int:
     return DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
 
 
+TG_F32_TF32, TG_F32_3XTF32 = 0, 1
+
+
 def make_options(path=0, splits=0, block_n=0, group_m=0, max_ctas=0, timeout_ms=0,
-                 tail_splits=0, multicast=0):
+                 tail_splits=0, multicast=0, f32_mode=0):
     o = tg_options()
     o.path, o.splits, o.block_n, o.group_m = path, splits, block_n, group_m
     o.max_ctas, o.timeout_ms, o.tail_splits = max_ctas, timeout_ms, tail_splits
-    o.multicast = multicast
+    o.multicast, o.f32_mode, o.reserved = multicast, f32_mode, 0
     return o
 
 

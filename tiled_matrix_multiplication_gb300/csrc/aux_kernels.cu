@@ -57,6 +57,68 @@ __global__ void pack_transpose_kernel(const T *__restrict__ src, int64_t ld_src,
     }
 }
 
+// x = hi + lo + r with hi and lo TF32 values (10 fraction bits; the
+// cvt.rna.tf32.f32 instruction: round to nearest, ties away from zero) and
+// |r| <= 2^-11 |lo| <= about 2^-22 |x|; x - hi is exact in FP32.  A non-finite
+// hi keeps lo = 0.
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    uint32_t h, l;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+    hi = __uint_as_float(h);
+    if (!isfinite(hi)) {
+        lo = 0.f;
+        return;
+    }
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(x - hi));
+    lo = __uint_as_float(l);
+}
+
+// A' = [hi(A) | lo(A) | hi(A)], [M, 3K] with pitch ld_dst.
+__global__ void split3_rows_kernel(const float *__restrict__ a, int64_t lda, float *__restrict__ dst,
+                                   int64_t ld_dst, int64_t M, int64_t K) {
+    const int64_t total = M * K;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / K;
+        const int64_t k = i - m * K;
+        float hi, lo;
+        split_tf32(a[m * lda + k], hi, lo);
+        float *row = dst + m * ld_dst;
+        row[k] = hi;
+        row[K + k] = lo;
+        row[2 * K + k] = hi;
+    }
+}
+
+// B'^T = [hi(B)^T | hi(B)^T | lo(B)^T], [N, 3K] with pitch ld_dst, through
+// 32 x 32 shared-memory tiles so reads of B and writes of B'^T are coalesced.
+__global__ void split3_transpose_kernel(const float *__restrict__ b, int64_t ldb,
+                                        float *__restrict__ dst, int64_t ld_dst, int64_t K,
+                                        int64_t N) {
+    __shared__ float hi_t[32][33], lo_t[32][33];
+    const int64_t tiles_n = (N + 31) / 32;
+    const int64_t tiles_k = (K + 31) / 32;
+    for (int64_t t = blockIdx.x; t < tiles_k * tiles_n; t += gridDim.x) {
+        const int64_t k0 = (t / tiles_n) * 32;
+        const int64_t n0 = (t % tiles_n) * 32;
+        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+            const int64_t k = k0 + i, n = n0 + threadIdx.x;
+            if (k < K && n < N) split_tf32(b[k * ldb + n], hi_t[i][threadIdx.x], lo_t[i][threadIdx.x]);
+        }
+        __syncthreads();
+        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+            const int64_t n = n0 + i, k = k0 + threadIdx.x;
+            if (k < K && n < N) {
+                float *row = dst + n * ld_dst;
+                row[k] = hi_t[threadIdx.x][i];
+                row[K + k] = hi_t[threadIdx.x][i];
+                row[2 * K + k] = lo_t[threadIdx.x][i];
+            }
+        }
+        __syncthreads();
+    }
+}
+
 __device__ __forceinline__ void store_out(void *c, int64_t off, int out_kind, float v) {
     if (out_kind == OUT_F32)
         static_cast<float *>(c)[off] = v;
@@ -148,6 +210,24 @@ cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, in
             rows, cols);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld_dst, int64_t M,
+                               int64_t K, cudaStream_t stream) {
+    if (M <= 0 || K <= 0) return cudaSuccess;
+    const int threads = 256;
+    split3_rows_kernel<<<grid_for(M * K, threads), threads, 0, stream>>>(
+        static_cast<const float *>(a), lda, static_cast<float *>(dst), ld_dst, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
+                                    int64_t K, int64_t N, cudaStream_t stream) {
+    if (K <= 0 || N <= 0) return cudaSuccess;
+    const int64_t tiles = ((K + 31) / 32) * ((N + 31) / 32);
+    split3_transpose_kernel<<<grid_for(tiles * 256, 256), dim3(32, 8), 0, stream>>>(
+        static_cast<const float *>(b), ldb, static_cast<float *>(dst), ld_dst, K, N);
     return cudaGetLastError();
 }
 

@@ -93,6 +93,7 @@ struct Plan {
     bool skinny_two = false;                   // small-M kernel: two CTAs per SM
     uint64_t timeout_ns = 0;
     int64_t stride_c = 0;                      // C batch stride (set before make_plan)
+    int64_t k_eff = 0;                         // K of the kernel (3K for 3xTF32)
 };
 
 constexpr int64_t kMaxGridY = 65535;           // gridDim.y: one row per product (small M)
@@ -112,6 +113,10 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
         return TG_ERR_UNSUPPORTED;
     if (opt) {
         if (opt->multicast < 0 || opt->multicast > 2) return TG_ERR_INVALID_VALUE;
+        if (opt->f32_mode < TG_F32_TF32 || opt->f32_mode > TG_F32_3XTF32 || opt->reserved != 0)
+            return TG_ERR_INVALID_VALUE;
+        if (opt->f32_mode == TG_F32_3XTF32 && (din != TG_F32 || 3 * K > kMaxDim))
+            return TG_ERR_UNSUPPORTED;
         if (opt->multicast == 2 &&
             (opt->path == TG_PATH_TC || opt->path == TG_PATH_SKINNY || opt->splits > 1 ||
              opt->tail_splits || (opt->block_n && !tg::tc_supported_mc(opt->block_n, 2))))
@@ -190,7 +195,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     num_sms = std::max(num_sms, 1);
     p.block_k = 128 / ei;
     p.group_m = (opt && opt->group_m) ? opt->group_m : kDefaultGroupM;
-    pl->k_tiles = std::max<int64_t>(cdiv(K, p.block_k), 1);
+    // 3xTF32: the kernel contracts the split operands over K' = 3K
+    const bool x3 = din == TG_F32 && opt && opt->f32_mode == TG_F32_3XTF32;
+    pl->k_eff = x3 ? 3 * K : K;
+    pl->k_tiles = std::max<int64_t>(cdiv(pl->k_eff, p.block_k), 1);
     const int64_t cap = (opt && opt->max_ctas) ? opt->max_ctas : num_sms;
 
     // Choose the kernel variant (single CTA with a 128-row tile, or CTA pair
@@ -344,9 +352,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
     p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
     if (din == TG_F32) p.pack_b = 2;   // kind::tf32 reads B K-major: B^T into the workspace
+    if (x3) p.pack_a = p.pack_b = 3;   // hi / lo TF32 parts of A and of B^T
     p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0 && (batch == 1 || (pl->stride_c * eo) % 16 == 0);
-    pl->lda_p = p.pack_a ? round_up(K, align_elems) : lda;
-    pl->ldb_p = p.pack_b == 2 ? round_up(K, align_elems)
+    pl->lda_p = p.pack_a ? round_up(pl->k_eff, align_elems) : lda;
+    pl->ldb_p = p.pack_b >= 2 ? round_up(pl->k_eff, align_elems)
                               : (p.pack_b ? round_up(N, align_elems) : ldb);
     int64_t ws = 0;
     if (p.pack_a) {
@@ -355,7 +364,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     }
     if (p.pack_b) {
         pl->off_b = ws;
-        ws = round_up(ws + (p.pack_b == 2 ? N : K) * pl->ldb_p * ei, 256);
+        ws = round_up(ws + (p.pack_b >= 2 ? N : K) * pl->ldb_p * ei, 256);
     }
     const bool global_partials = splits > 1 && p.path != TG_PATH_SKINNY;
     if (global_partials) {
@@ -523,16 +532,21 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     const void *B = b;
     if (p.pack_a) {
         A = ws + pl.off_a;
-        st = cuda_status(tg::launch_pack_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, ei, s));
+        st = cuda_status(p.pack_a == 3
+                             ? tg::launch_split3_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, s)
+                             : tg::launch_pack_rows(a, lda, ws + pl.off_a, pl.lda_p, M, K, ei, s));
         if (st != TG_OK) return fail(st);
     }
     if (p.pack_b) {
         B = ws + pl.off_b;
-        st = cuda_status(p.pack_b == 2
-                             ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
-                             : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
+        st = cuda_status(
+            p.pack_b == 3 ? tg::launch_split3_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, s)
+            : p.pack_b == 2
+                ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
+                : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
         if (st != TG_OK) return fail(st);
     }
+    const int64_t Ke = pl.k_eff;   // K of the kernel's operands
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
     if (p.path == TG_PATH_SKINNY) {
@@ -568,13 +582,13 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     const bool pair = p.path == TG_PATH_TC_PAIR;
     const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
     const int b_chunk = tg::tc_b_swizzle_bytes(in_kind_of(dtype_in), p.block_n, pair) / ei;
-    const tg_status sb = p.pack_b == 2
-                             ? encode_2d(&tmB, dtype_in, B, N, K, pl.ldb_p, p.block_k, bn_cta)
+    const tg_status sb = p.pack_b >= 2
+                             ? encode_2d(&tmB, dtype_in, B, N, Ke, pl.ldb_p, p.block_k, bn_cta)
                              : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, b_chunk, p.block_k,
                                          nb_b, bt.sb);
     // with A multicast each CTA loads half of its 128 rows of A
     const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
-    if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_rows, nb_a, bt.sa) != TG_OK ||
+    if (encode_2d(&tmA, dtype_in, A, M, Ke, pl.lda_p, p.block_k, a_rows, nb_a, bt.sa) != TG_OK ||
         sb != TG_OK)
         return fail(map_error());
 
@@ -582,7 +596,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     std::memset(&tp, 0, sizeof(tp));
     tp.M = static_cast<int32_t>(M);
     tp.N = static_cast<int32_t>(N);
-    tp.K = static_cast<int32_t>(K);
+    tp.K = static_cast<int32_t>(Ke);
     tp.tiles_m = static_cast<int32_t>(pl.tiles_m);
     tp.tiles_n = static_cast<int32_t>(pl.tiles_n);
     tp.k_tiles = static_cast<int32_t>(pl.k_tiles);

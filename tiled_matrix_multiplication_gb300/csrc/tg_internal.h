@@ -133,6 +133,13 @@ cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, in
                                   int64_t rows, int64_t cols, int esize, cudaStream_t stream);
 // C = the sum of the `splits` partial planes, through the epilogue `epi`
 // (splits == 0: the empty sum, i.e. the epilogue of zero).
+// 3xTF32 operand splitting (x = hi + lo with both parts TF32 values):
+// dst[m, 0:K) = hi(A), [K, 2K) = lo(A), [2K, 3K) = hi(A)      (A' rows)
+// dst[n, 0:K) = hi(B)^T, [K, 2K) = hi(B)^T, [2K, 3K) = lo(B)^T  (B'^T rows)
+cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld_dst, int64_t M,
+                               int64_t K, cudaStream_t stream);
+cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
+                                    int64_t K, int64_t N, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N,
                                  void *c, int64_t ldc, int out_kind, int c_vector,
                                  cudaStream_t stream, const EpiParams *epi = nullptr);
