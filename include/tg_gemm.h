@@ -225,10 +225,10 @@ typedef struct tg_epilogue {
  *
  *     C[m,n] = act(alpha * scale[n] * sum_k A[m,k] B[k,n] + bias[n]) + beta * R[m,n]
  *
- * The work done "while the data is already in registers" that "Matrix
- * Multiplication" (teenygrad docs, closing section) hands on to the next
- * chapter, "Fusing an Epilogue"; the same book's fused kernel applies a
- * per-channel scale and shift (batch norm) and a SiLU to a GEMM this way.
+ * "Matrix Multiplication" (teenygrad docs) closes by handing on to its next
+ * chapter, "Fusing an Epilogue": extra work on the output tile while it is
+ * still on chip.  The same book's fused kernel applies a per-channel scale and
+ * shift (batch norm) and a SiLU to a GEMM this way.
  *
  *   M .. dtype_out, stream, opt   as for tg_gemm_ex
  *   epilogue   NULL: exactly tg_gemm_ex.  Otherwise: activation out of range
