@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 5
+#define TG_ABI_VERSION 6
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -248,6 +248,37 @@ tg_status tg_gemm_fused(int64_t M, int64_t N, int64_t K,
                         tg_dtype dtype_in, tg_dtype dtype_out,
                         const tg_epilogue *epilogue,
                         void *stream, const tg_options *opt);
+
+/*
+ * tg_gemm_host -- C = A * B with A, B and C in HOST memory: the library stages
+ * them through device memory of its own and overlaps the transfers with the
+ * multiply.  B is copied first, then A in row panels (at least 1024 rows, at
+ * most 16 panels) on one copy stream; the panel products run on `stream` as
+ * each panel of A arrives, and each panel of C is copied back on a second copy
+ * stream while later panels are still being copied in or multiplied.
+ *
+ *   M .. dtype_out, opt   as for tg_gemm_ex, with a, b, c HOST pointers
+ *                         (page-locked memory, e.g. cudaHostAlloc, lets the
+ *                         copies run asynchronously and overlap; pageable
+ *                         memory works but the copies serialise)
+ *   stream                the multiply runs on it; the call returns at once and
+ *                         C is complete when the work enqueued on `stream` so
+ *                         far has finished (synchronise it before reading C)
+ *
+ * The staging buffers (M*K + K*N elements of dtype_in, M*N of dtype_out, row
+ * pitches rounded up to 16 bytes) come from the library's memory pool and go
+ * back to it in stream order.  The panels are separate products, so the
+ * result is the one tg_gemm_ex gives for each row panel.  Argument errors as
+ * for tg_gemm (the overlap rules apply to the host addresses).  One call per
+ * device runs its enqueueing at a time (a lock); the copies of successive
+ * calls may overlap on the GPU.
+ */
+tg_status tg_gemm_host(int64_t M, int64_t N, int64_t K,
+                       const void *a, int64_t lda,
+                       const void *b, int64_t ldb,
+                       void *c, int64_t ldc,
+                       tg_dtype dtype_in, tg_dtype dtype_out,
+                       void *stream, const tg_options *opt);
 
 /*
  * tg_gemm_strided_batched -- `batch` independent products

@@ -30,7 +30,8 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 # Every extern "C" symbol the header declares.
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
            "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
-           "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused")
+           "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused",
+           "tg_gemm_host")
 
 TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_ACT_GELU_TANH = 0, 1, 2, 3
 ACT_CODES = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "silu": TG_ACT_SILU,
@@ -120,6 +121,8 @@ def load(path: str | None = None):
         lib.tg_gemm_fused.argtypes = gemm_args[:-1] + [ctypes.POINTER(tg_epilogue), vp,
                                                         ctypes.POINTER(tg_options)]
         lib.tg_gemm_fused.restype = ctypes.c_int
+        lib.tg_gemm_host.argtypes = gemm_args + [ctypes.POINTER(tg_options)]
+        lib.tg_gemm_host.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -232,3 +235,12 @@ def tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, epilogue
     opt = ctypes.byref(options) if options is not None else None
     return int(load().tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
                                     _code(dtype_out), ep, stream, opt))
+
+
+def tg_gemm_host(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream,
+                 options=None) -> int:
+    """C = A B with HOST pointers a, b, c (page-locked for overlap); the copies
+    and the multiply are pipelined on the device.  Returns the tg_status."""
+    opt = ctypes.byref(options) if options is not None else None
+    return int(load().tg_gemm_host(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
+                                   _code(dtype_out), stream, opt))
