@@ -102,10 +102,12 @@ struct TcCfg {
     static constexpr int CTA_M = 128;             // accumulator rows held by one CTA
     static constexpr int TILE_M = PAIR ? 256 : 128;
     static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
-    // B operand layout in shared memory.  16-bit operands are consumed
-    // N-major, straight from row-major B.  kind::tf32 is given a K-major B
-    // (the host transposes B into the workspace first): an N-major B tile
-    // produced all-zero results with kind::tf32 on this hardware.
+    // B operand layout in shared memory.  16-bit and 8-bit operands are
+    // consumed N-major, straight from row-major B.  kind::tf32 is given a
+    // K-major B (the host transposes B into the workspace first): N-major B
+    // tiles gave wrong products with kind::tf32 on this hardware (all zeros
+    // with one descriptor variant; with the N-major descriptors that are exact
+    // for FP16 and FP8, errors of 10-20 % of sum |a b|).
     static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
     static constexpr int A_STAGE = CTA_M * 128;   // bytes
     static constexpr int B_BOX = BK * B_SW;       // one CHUNK_N-wide N-major TMA box
@@ -481,21 +483,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = wk.tm * Cfg::TILE_M + trow;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_STRIDE;
-            // tail-split unit: this range's FP32 partial row of the tile
-            float *prow = nullptr;
+            // tail-split unit: this range's FP32 partial tile, laid out as
+            // [BN/4 column quads][TILE_M rows][4] so that one store or load of
+            // a warp (32 consecutive rows, one column quad) covers 512
+            // contiguous bytes
+            float *ptile = nullptr;
             if (wk.tail >= 0)
-                prow = p.tail_partial +
-                       ((static_cast<int64_t>(wk.tail) * p.tail_splits + wk.split) * Cfg::TILE_M +
-                        trow) * BN;
+                ptile = p.tail_partial +
+                        (static_cast<int64_t>(wk.tail) * p.tail_splits + wk.split) * Cfg::TILE_M * BN;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;
-                if (prow != nullptr) {
+                if (ptile != nullptr) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<uint4 *>(prow + c0 + j) =
+                        *reinterpret_cast<uint4 *>(
+                            ptile + ((static_cast<int64_t>(c0 + j) >> 2) * Cfg::TILE_M + trow) * 4) =
                             make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
                 } else if (row < p.M && col < p.N) {
                     store_chunk(p, wk.split, row, col, r, wk.z);
@@ -524,8 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epilogue_bar_sync();
                 if (tail_last && row < p.M) {
                     const float *base = p.tail_partial +
-                                        (static_cast<int64_t>(wk.tail) * p.tail_splits * Cfg::TILE_M +
-                                         trow) * BN;
+                                        static_cast<int64_t>(wk.tail) * p.tail_splits * Cfg::TILE_M * BN;
                     const int64_t split_stride = static_cast<int64_t>(Cfg::TILE_M) * BN;
 #pragma unroll 1
                     for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -535,10 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
                         for (int sidx = 0; sidx < p.tail_splits; ++sidx) {
-                            const float *src = base + sidx * split_stride + c0;
+                            const float *src = base + sidx * split_stride;
 #pragma unroll
                             for (int j = 0; j < 32; j += 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + j));
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                    src + ((static_cast<int64_t>(c0 + j) >> 2) * Cfg::TILE_M + trow) * 4));
                                 acc[j] += v.x;
                                 acc[j + 1] += v.y;
                                 acc[j + 2] += v.z;

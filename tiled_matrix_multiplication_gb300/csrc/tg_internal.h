@@ -55,7 +55,7 @@ struct TcParams {
     // Tail split (splits == 1 only): the last `tail_tiles` tiles in raster
     // order are each split into `tail_splits` K ranges of `tail_kps` K tiles,
     // addressed by unit indices >= tail_start.  Each range writes an FP32
-    // partial tile to `tail_partial` ([tail_tiles][tail_splits][TILE_M][BN]);
+    // partial tile to `tail_partial` ([tail_tiles][tail_splits][BN/4][TILE_M][4]);
     // the range that finishes a tile last (counted per tile and CTA of a pair
     // in `tail_count`, zero before the launch) sums them in range order into C.
     int32_t tail_start, tail_tiles, tail_splits, tail_kps;
