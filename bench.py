@@ -81,7 +81,19 @@ WORKLOADS = {
                             "strided batch of 64 GEMMs 1024^3, BF16 N(0,0.02)"),
     "batched32x64x8192_f16": (64, 8192, 8192, "f16", "f16", "uniform",
                               "strided batch of 32 small-M GEMMs 64x8192x8192, FP16"),
+    # the fused epilogue and the 3xTF32 mode
+    "square4096_f16_bias_silu": (4096, 4096, 4096, "f16", "f16", "uniform",
+                                 "square GEMM 4096^3 FP16 with a fused epilogue: "
+                                 "silu(C + bias[n]), bias FP32 U[-1,1)"),
+    "square4096_f32_3xtf32": (4096, 4096, 4096, "f32", "f32", "uniform",
+                              "square GEMM 4096^3, FP32 operands as three TF32 products "
+                              "(near-FP32 accuracy), FP32 out"),
 }
+# planner options and fused epilogues that are part of a workload's definition
+WORKLOAD_OPTS = {"square4096_f32_3xtf32": {"f32_mode": 1}}
+WORKLOAD_EPILOGUE = {"square4096_f16_bias_silu": {"activation": "silu", "bias": True}}
+# tensor FLOPs the method performs per algorithmic 2MNK (3xTF32: three TF32 products)
+TENSOR_WORK = {"square4096_f32_3xtf32": 3.0}
 # products per call of the batched workloads (1 for every other workload)
 BATCH = {"batched16x2048_f16": 16, "batched64x1024_bf16": 64, "batched32x64x8192_f16": 32}
 DEFAULT_WORKLOAD = "square4096_f16"
@@ -336,9 +348,16 @@ def run_ours(args, world, rank, local):
     sh = stream.cuda_stream
     code_in, code_out = tg.dtype_code(din), tg.dtype_code(dout)
 
-    opts = dict(kv.split("=") for kv in args.opt)
-    opts = {k: int(v) for k, v in opts.items()}
+    opts = dict(WORKLOAD_OPTS.get(args.workload, {}))
+    opts.update({k: int(v) for k, v in (kv.split("=") for kv in args.opt)})
     topt = tg.make_options(**opts) if opts else None
+    epi = None
+    epi_spec = WORKLOAD_EPILOGUE.get(args.workload)
+    if epi_spec is not None:
+        bias_bits = inputs.matrix_bits(1, N, "f32", "uniform", 72)
+        bias_d = torch.from_numpy(bias_bits.view(np.float32)[0].copy()).cuda()
+        epi = tg.make_epilogue(bias=bias_d.data_ptr() if epi_spec.get("bias") else 0,
+                               activation=epi_spec["activation"])
     if nb > 1:
         plan = tg.plan_batched(nb, M, N, K, din, dout, num_sms=props.multi_processor_count,
                                **opts)
@@ -346,6 +365,9 @@ def run_ours(args, world, rank, local):
         plan = tg.plan(M, N, K, din, dout, num_sms=props.multi_processor_count, **opts)
 
     def call(a, b, c):
+        if epi is not None:
+            return tg.tg_gemm_fused(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                                    code_in, code_out, epi, sh, topt)
         if nb > 1:
             return tg.tg_gemm_strided_batched(nb, M, N, K, a.data_ptr(), K, M * K, b.data_ptr(),
                                               N, K * N, c.data_ptr(), N, M * N, code_in,
@@ -400,7 +422,18 @@ def run_ours(args, world, rank, local):
     a_pin = a_host.pin_memory()
     b_pin = b_host.pin_memory()
     c_pin = torch.empty((nb, M, N), dtype=tdt[dout]).pin_memory()
+    a_e, b_e, c_e = sets[0]
+
     def e2e_step():
+        if epi is not None:
+            # (tg_gemm_host has no epilogue: copy in, fused multiply, copy back)
+            a_e.copy_(a_pin, non_blocking=True)
+            b_e.copy_(b_pin, non_blocking=True)
+            st = call(a_e, b_e, c_e)
+            if st != tg.TG_OK:
+                raise tg.TgError(st, "tg_gemm_fused")
+            c_pin.copy_(c_e, non_blocking=True)
+            return
         # tg_gemm_host: host operands in, host result out, copies pipelined
         # with the multiply inside the library
         st = tg.TG_OK
@@ -445,12 +478,13 @@ def run_ours(args, world, rank, local):
         peak = float(pk["hbm_gbs"])
     else:
         bound, unit = "tensor", "TFLOP/s"
-        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        achieved = TENSOR_WORK.get(args.workload, 1.0) * flops / (kernel_ms * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"]) * PEAK_RATIO[din]
     roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
             "peak_source": f"{pk_kind} ({'hbm_gbs' if skinny else 'bf16_tflops'} burst"
                            f"{'' if skinny or PEAK_RATIO[din] == 1.0 else f', x{PEAK_RATIO[din]} nominal ratio to BF16'})",
+            "tensor_flops_per_useful_flop": TENSOR_WORK.get(args.workload, 1.0),
             "kernel": ("gemm_skinny_kernel" if plan["path"] == tg.TG_PATH_SKINNY else "gemm_tc_kernel")
                       + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
             "launch_ms": round(kernel_ms, 5)}
