@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 6
+#define TG_ABI_VERSION 7
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -343,6 +343,18 @@ const char *tg_status_string(tg_status status);
  * TG_ERR_CUDA if the synchronisation itself failed.
  */
 tg_status tg_last_device_error(void *stream);
+
+/*
+ * tg_selftest_timeout -- failure-detection check: enqueues on `stream` a
+ * one-thread kernel that waits on a shared-memory barrier nothing ever
+ * arrives on, with the same bounded wait (global-time limit) the GEMM kernels
+ * use, and records TG_ERR_TIMEOUT in the device status word when the limit
+ * (timeout_ms, 1 .. 10000) runs out; the kernel then exits normally and the
+ * context stays usable.  tg_last_device_error(stream) afterwards returns
+ * TG_ERR_TIMEOUT (and clears it).  No GEMM counterpart in the pages: this
+ * exercises the library's own bounded-wait failure path.
+ */
+tg_status tg_selftest_timeout(int32_t timeout_ms, void *stream);
 
 /* TG_ABI_VERSION of the loaded library. */
 int32_t tg_abi_version(void);

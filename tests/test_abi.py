@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert tg.tg_abi_version() == 6
+    assert tg.tg_abi_version() == 7
     assert tg.tg_status_string(tg.TG_OK) == "TG_OK"
     assert tg.tg_status_string(tg.TG_ERR_TIMEOUT) == "TG_ERR_TIMEOUT"
     assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
@@ -237,3 +237,9 @@ def test_python_gemm_checks_shapes():
         tg.gemm(a, b)
     with pytest.raises(ValueError):   # CPU tensors are refused: no CPU path exists
         tg.gemm(a, torch.zeros(4, 2, dtype=torch.float16))
+
+
+def test_selftest_timeout_argument_range(lib):
+    # rejected on the host, before any device call
+    assert tg.tg_selftest_timeout(0, 0) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_selftest_timeout(10001, 0) == tg.TG_ERR_INVALID_VALUE

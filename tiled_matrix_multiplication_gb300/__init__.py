@@ -24,13 +24,14 @@ from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_E4M3, TG_E5M2, TG
                    load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
                    ACT_CODES, TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU,
                    make_epilogue, tg_epilogue, tg_gemm_fused, tg_gemm_host,
+                   tg_selftest_timeout,
                    tg_gemm_splitk_noalloc, tg_gemm_strided_batched, tg_last_device_error,
                    tg_options, tg_plan, tg_plan_gemm, tg_plan_gemm_strided_batched,
                    tg_status_string)
 
 __all__ = [
     "gemm", "gemm_fused", "bmm", "plan", "plan_batched", "check_device_error",
-    "tg_gemm_fused", "tg_gemm_host", "tg_epilogue", "make_epilogue", "ACT_CODES", "TG_ACT_NONE", "TG_ACT_RELU",
+    "tg_gemm_fused", "tg_gemm_host", "tg_selftest_timeout", "tg_epilogue", "make_epilogue", "ACT_CODES", "TG_ACT_NONE", "TG_ACT_RELU",
     "TG_ACT_SILU", "TG_ACT_GELU_TANH", "dtype_code", "TgError", "load", "make_options",
     "tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string", "tg_last_device_error",
     "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",

@@ -31,7 +31,7 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
            "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
            "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused",
-           "tg_gemm_host")
+           "tg_gemm_host", "tg_selftest_timeout")
 
 TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_ACT_GELU_TANH = 0, 1, 2, 3
 ACT_CODES = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "silu": TG_ACT_SILU,
@@ -123,6 +123,8 @@ def load(path: str | None = None):
         lib.tg_gemm_fused.restype = ctypes.c_int
         lib.tg_gemm_host.argtypes = gemm_args + [ctypes.POINTER(tg_options)]
         lib.tg_gemm_host.restype = ctypes.c_int
+        lib.tg_selftest_timeout.argtypes = [i32, vp]
+        lib.tg_selftest_timeout.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -244,3 +246,9 @@ def tg_gemm_host(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream,
     opt = ctypes.byref(options) if options is not None else None
     return int(load().tg_gemm_host(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
                                    _code(dtype_out), stream, opt))
+
+
+def tg_selftest_timeout(timeout_ms, stream) -> int:
+    """Enqueue the failure-detection check (a bounded wait that always runs
+    out); tg_last_device_error then reports TG_ERR_TIMEOUT."""
+    return int(load().tg_selftest_timeout(timeout_ms, stream))

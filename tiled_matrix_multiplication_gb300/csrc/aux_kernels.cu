@@ -16,6 +16,8 @@
 
 #include "tg_epilogue.cuh"
 #include "tg_internal.h"
+#include "tg_kernel_common.cuh"
+#include "tg_ptx.cuh"
 
 namespace tg {
 namespace {
@@ -161,6 +163,22 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int spli
     }
 }
 
+// Failure-detection check: the wait of the GEMM kernels (mbar_wait, bounded
+// by global time) on a barrier whose phase never completes, then the same
+// failure record.  One thread; no memory other than the status word.
+__global__ void selftest_timeout_kernel(int *status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int never_abort;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        never_abort = 0;
+        mbar_init(b, 1);
+        fence_mbar_init();
+        if (!mbar_wait(b, 0, timeout_ns, &never_abort))
+            record_failure(status, 6, (ROLE_SELFTEST << 16) | 1);
+    }
+}
+
 int grid_for(int64_t work, int threads) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -210,6 +228,11 @@ cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, in
             rows, cols);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream) {
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
     return cudaGetLastError();
 }
 

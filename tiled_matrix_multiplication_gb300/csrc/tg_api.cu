@@ -1009,6 +1009,15 @@ tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
     return TG_OK;
 }
 
+tg_status tg_selftest_timeout(int32_t timeout_ms, void *stream) {
+    if (timeout_ms < 1 || timeout_ms > 10000) return TG_ERR_INVALID_VALUE;
+    DeviceState *dev = nullptr;
+    const tg_status st = device_state(&dev);
+    if (st != TG_OK) return st;
+    return cuda_status(tg::launch_selftest_timeout(
+        dev->status, static_cast<uint64_t>(timeout_ms) * 1000000ull, static_cast<cudaStream_t>(stream)));
+}
+
 tg_status tg_last_device_error(void *stream) {
     DeviceState *dev = nullptr;
     const tg_status st = device_state(&dev);

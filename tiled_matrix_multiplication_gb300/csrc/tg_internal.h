@@ -18,7 +18,8 @@ enum OutKind : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
 
 // Device status word layout: [0] first tg_status code recorded, [1] where it
 // was recorded (role << 16 | detail).
-enum FailRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
+enum FailRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4,
+                      ROLE_SELFTEST = 5 };
 
 enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
 
@@ -131,6 +132,9 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
                              int64_t rows, int64_t cols, int esize, cudaStream_t stream);
 cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                                   int64_t rows, int64_t cols, int esize, cudaStream_t stream);
+// One CTA waits, bounded by timeout_ns, on an mbarrier that nothing arrives
+// on, and records TG_ERR_TIMEOUT in `status` the way the GEMM kernels do.
+cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream);
 // C = the sum of the `splits` partial planes, through the epilogue `epi`
 // (splits == 0: the empty sum, i.e. the epilogue of zero).
 // 3xTF32 operand splitting (x = hi + lo with both parts TF32 values):
