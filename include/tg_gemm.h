@@ -31,8 +31,7 @@
  *                           FP8 input path of "Triton tiled matmul"
  *                           (llm-systems-cookbook), section "Exercises", item 2.
  *                           Row pitches (lda, ldb) and bases of A and B that are
- *                           not multiples of 16 bytes are packed first; the
- *                           small-M streaming kernel is not used for FP8.
+ *                           not multiples of 16 bytes are packed first.
  * Any other pair returns TG_ERR_UNSUPPORTED.
  *
  * Ownership.  a, b and c are DEVICE pointers owned by the caller and must stay

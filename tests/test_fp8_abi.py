@@ -1,6 +1,6 @@
 """Host-only rules of the FP8 operand types (no GPU): accepted type pairs,
 the 128-element K block, packing of pitches that are not 16-byte multiples,
-and the small-M kernel being unavailable for FP8."""
+and the small-M streaming kernel's K blocks for FP8."""
 from __future__ import annotations
 
 import pytest
@@ -46,10 +46,13 @@ def test_pitch_packing_rule():
     assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 1
 
 
-def test_small_m_stays_on_tensor_core_kernels():
+def test_small_m_uses_the_streaming_kernel():
     st, p = plan(16, 8192, 8192, "e4m3", "f16")
-    assert st == tg.TG_OK and p["path"] in (tg.TG_PATH_TC, tg.TG_PATH_TC_PAIR)
-    st, _ = plan(16, 8192, 8192, "e4m3", "f16", path=tg.TG_PATH_SKINNY)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_SKINNY and p["block_k"] == 128
+    st, p = plan(16, 8192, 8192, "e4m3", "f16", path=tg.TG_PATH_SKINNY, splits=8)
+    assert st == tg.TG_OK and p["splits"] == 8
+    # 8 K ranges of 128-element tiles need K > 7 * 128
+    st, _ = plan(16, 8192, 896, "e4m3", "f16", path=tg.TG_PATH_SKINNY, splits=8)
     assert st == tg.TG_ERR_UNSUPPORTED
 
 

@@ -1,8 +1,9 @@
 """GPU parity of the FP8 path (E4M3 / E5M2 operands through kind::f8f6f4,
 FP32 accumulate, FP16 / BF16 / FP32 output) against the oracle: bit-exact on
 small-integer operands, within the tolerance on uniform ones, on every
-tensor-core variant, with ragged sizes, padded and packed operands, the
-4096^3 problem (sampled rows), strided batches and the fused epilogue."""
+tensor-core variant and the small-M streaming kernel, with ragged sizes,
+padded and packed operands, the 4096^3 problem (sampled rows), strided
+batches and the fused epilogue."""
 from __future__ import annotations
 
 import numpy as np
@@ -62,12 +63,27 @@ def test_tail_split():
     compare(a, b, c, M, N, K, "e4m3", "f16", exact=True)
 
 
-@pytest.mark.parametrize("M", [1, 64, 128])
-def test_small_m_uses_tensor_core_kernel(M):
-    p = tg.plan(M, 4096, 4096, "e4m3", "f16", num_sms=152)
-    assert p["path"] != tg.TG_PATH_SKINNY
-    a, b, c = run_gemm(M, 4096, 4096, "e4m3", "f16")
-    compare(a, b, c, M, 4096, 4096, "e4m3", "f16")
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M", [1, 16, 64, 128])
+def test_small_m_kernel_exact(fmt, M):
+    # the transposed streaming kernel with FP8 operands (kind::f8f6f4 with an
+    # N-major B^T as the MMA's A operand), K split over a 4-CTA cluster
+    p = tg.plan(M, 8192, 8192, fmt, "f16", num_sms=152)
+    assert p["path"] == tg.TG_PATH_SKINNY and p["block_k"] == 128
+    a, b, c = run_gemm(M, 8192, 8192, fmt, "f16", dist="int")
+    compare(a, b, c, M, 8192, 8192, fmt, "f16", exact=True)
+
+
+@pytest.mark.parametrize("M,N,K,opts", [
+    (37, 1000, 700, {}),
+    (64, 512, 2048, dict(path=tg.TG_PATH_SKINNY, splits=8)),
+    (100, 1536, 640, dict(path=tg.TG_PATH_SKINNY, block_n=256, splits=2)),
+    (16, 2048, 1024, dict(path=tg.TG_PATH_SKINNY, block_n=512, splits=1)),
+])
+def test_small_m_kernel_uniform(M, N, K, opts):
+    a, b, c = run_gemm(M, N, K, "e4m3", "bf16", ldc=N + 8, **opts)
+    compare(a, b, c, M, N, K, "e4m3", "bf16")
+    assert padding_untouched(c, N, "bf16")
 
 
 def test_k_zero_and_tiny():
@@ -86,21 +102,11 @@ def test_square_4096(dist):
     compare(a, b, c, n, n, n, "e4m3", "f16", exact=(dist == "int"), rows=rows)
 
 
-def test_forced_small_m_kernel_is_unsupported():
-    import torch
-    from tests.gemm_util import to_device
-    from tiled_matrix_multiplication_gb300 import inputs
-    a = to_device(inputs.matrix_bits(16, 256, "e4m3", "int", 1), "e4m3")
-    b = to_device(inputs.matrix_bits(256, 256, "e4m3", "int", 2), "e4m3")
-    with pytest.raises(tg.TgError) as ei:
-        tg.gemm(a, b, out_dtype=torch.float16, path=tg.TG_PATH_SKINNY)
-    assert ei.value.status == tg.TG_ERR_UNSUPPORTED
-
-
 def test_batched_fp8():
     from tests.test_batched_gpu import check_all
     check_all(3, 300, 520, 256, "e4m3", "bf16")
     check_all(4, 256, 256, 512, "e5m2", "f16", exact=True, dist="int")
+    check_all(40, 16, 1024, 512, "e4m3", "f32")          # small-M kernel, two CTAs per SM
 
 
 def test_fused_epilogue_fp8():

@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtg_gemm.so")
 
 SOURCES = ["tg_api.cu", "gemm_tc.cu", "gemm_tc_f16.cu", "gemm_tc_tf32.cu", "gemm_tc_fp8.cu",
-           "gemm_skinny.cu", "aux_kernels.cu", "noalloc.cu"]
+           "gemm_skinny.cu", "gemm_skinny_fp8.cu", "aux_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-O2", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -141,15 +141,15 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             opt->timeout_ms < 0)
             return TG_ERR_INVALID_VALUE;
         if (opt->path == TG_PATH_SKINNY) {
-            // C^T = B^T A^T with all rows in one tile: 16-bit operands, M <= 128,
-            // K split over a cluster of 1, 2, 4 or 8 CTAs (none of them empty),
-            // 128, 256 or 512 columns per CTA
-            if (din == TG_F32 || is_fp8(din) || M > 128) return TG_ERR_UNSUPPORTED;
+            // C^T = B^T A^T with all rows in one tile: 16-bit or 8-bit operands,
+            // M <= 128, K split over a cluster of 1, 2, 4 or 8 CTAs (none of
+            // them empty), 128, 256 or 512 columns per CTA
+            if (din == TG_F32 || M > 128) return TG_ERR_UNSUPPORTED;
             if (opt->block_n && !tg::skinny_supported(tg::skinny_rows(M), opt->block_n))
                 return TG_ERR_UNSUPPORTED;
             const int64_t s = opt->splits;
             if (s != 0 && s != 1 && s != 2 && s != 4 && s != 8) return TG_ERR_UNSUPPORTED;
-            const int64_t kt = std::max<int64_t>(cdiv(K, 64), 1);
+            const int64_t kt = std::max<int64_t>(cdiv(K, 128 / esize_of(static_cast<tg_dtype>(din))), 1);
             if (s > 1 && (s - 1) * cdiv(kt, s) >= kt) return TG_ERR_UNSUPPORTED;
         }
         if (opt->block_n && opt->path != TG_PATH_SKINNY) {
@@ -291,7 +291,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // Small M with 16-bit operands: the transposed streaming kernel (one tile
     // holds all rows; work is spread over 128-column tiles and K splits).
     const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
-    const bool skinny_ok = din != TG_F32 && !is_fp8(din) && M <= 128 &&
+    const bool skinny_ok = din != TG_F32 && M <= 128 &&
                            (forced_skinny || !(opt && opt->block_n)) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&
                            batch <= kMaxGridY;
@@ -301,7 +301,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         // largest cluster that keeps every CTA resident at once (and every K
         // range non-empty): the kernel streams B, so more CTAs means more bytes
         // in flight.
-        const int64_t ktiles = std::max<int64_t>(cdiv(K, 64), 1);
+        const int64_t ktiles = std::max<int64_t>(cdiv(K, 128 / ei), 1);   // 128-byte K rows
         const int mp = tg::skinny_rows(M);
         // 128 columns per CTA by default: on GB300 wider tiles (256, 512: longer
         // contiguous runs of B, fewer re-reads of A) measured no faster at
@@ -336,7 +336,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         p.path = TG_PATH_SKINNY;
         p.block_m = mp;
         p.block_n = nt;
-        p.block_k = 64;
+        p.block_k = 128 / ei;
         p.splits = static_cast<int32_t>(best_s);
         p.tiles = tiles;
         pl->k_tiles = ktiles;

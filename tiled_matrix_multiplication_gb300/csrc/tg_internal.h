@@ -98,6 +98,10 @@ bool skinny_supported(int mp, int nt);
 int skinny_stages(int mp, int nt, bool two);
 cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &tmA,
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream);
+// gemm_skinny_fp8.cu: the E4M3 / E5M2 instantiations behind launch_gemm_skinny
+cudaError_t launch_gemm_skinny_fp8(int in_kind, int mp, int nt, const CUtensorMap &tmA,
+                                   const CUtensorMap &tmB, const SkParams &p,
+                                   cudaStream_t stream);
 
 // gemm_tc.cu
 // `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `mc` = 2: clusters
