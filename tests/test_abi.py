@@ -243,3 +243,18 @@ def test_selftest_timeout_argument_range(lib):
     # rejected on the host, before any device call
     assert tg.tg_selftest_timeout(0, 0) == tg.TG_ERR_INVALID_VALUE
     assert tg.tg_selftest_timeout(10001, 0) == tg.TG_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("opts", [dict(path=tg.TG_PATH_TC_PAIR, max_ctas=1),
+                                  dict(multicast=2, max_ctas=3),
+                                  dict(path=tg.TG_PATH_TC_PAIR, block_n=256, multicast=2,
+                                       max_ctas=2)])
+def test_options_that_exclude_every_variant(lib, opts):
+    # no kernel variant fits: refused on the host, nothing planned or launched
+    st, _ = plan(2048, 2048, 2048, **opts)
+    assert st == tg.TG_ERR_UNSUPPORTED
+    o = tg.make_options(**opts)
+    st, _ = tg.tg_plan_gemm_strided_batched(4, 1024, 1024, 1024, A, 1024, 1024 * 1024, B, 1024,
+                                             1024 * 1024, C, 1024, 1024 * 1024, "f16", "f16",
+                                             148, o)
+    assert st == tg.TG_ERR_UNSUPPORTED

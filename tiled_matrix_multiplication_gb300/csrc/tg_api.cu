@@ -107,6 +107,7 @@ struct Plan {
     uint64_t timeout_ns = 0;
     int64_t stride_c = 0;                      // C batch stride (set before make_plan)
     int64_t k_eff = 0;                         // K of the kernel (3K for 3xTF32)
+    bool valid = true;                         // false: no kernel variant fits the options
 };
 
 constexpr int64_t kMaxGridY = 65535;           // gridDim.y: one row per product (small M)
@@ -342,6 +343,12 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         pl->k_tiles = ktiles;
         pl->k_per_split = cdiv(ktiles, best_s);
     }
+    if (best_cost < 0 && p.path != TG_PATH_SKINNY) {
+        // the options exclude every variant (e.g. a CTA budget below one
+        // cluster of the forced variant): nothing to launch
+        pl->valid = false;
+        return;
+    }
     const bool pair = p.path == TG_PATH_TC_PAIR;
     p.stages = p.path == TG_PATH_SKINNY ? tg::skinny_stages(p.block_m, p.block_n, pl->skinny_two)
                                          : tg::tc_stages(in_kind_of(din), p.block_n, pair);
@@ -520,6 +527,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     pl.stride_c = bt.sc;
     make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, opt, &pl,
               dev->pair_slots, dev->quad_slots, bt.count);
+    if (!pl.valid) return TG_ERR_UNSUPPORTED;
     const tg_plan &p = pl.pub;
     const int ei = esize_of(dtype_in);
     const bool batched = bt.count > 1;
@@ -803,6 +811,7 @@ tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t l
     if (v != TG_OK) return v;
     Plan pl;
     make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, opt, &pl);
+    if (!pl.valid) return TG_ERR_UNSUPPORTED;
     if (M == 0 || N == 0 || K == 0) {   // nothing, or a memset of C: no kernel of the library
         pl.pub.kernels = 0;
         pl.pub.workspace_bytes = 0;
@@ -954,6 +963,7 @@ tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int6
     pl.stride_c = stride_c;
     make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, num_sms, opt, &pl, 0, 0,
               one ? batch : 1);
+    if (!pl.valid) return TG_ERR_UNSUPPORTED;
     if (batch > 1 && !one) {   // one call per product
         pl.pub.per_batch = 1;
         pl.pub.kernels *= static_cast<int32_t>(std::min<int64_t>(batch, 1 << 24));
