@@ -169,3 +169,28 @@ def test_larger_batch_sampled():
     for z in range(batch):
         rows = np.unique(np.concatenate([rng.choice(n, 12, replace=False), [0, n - 1]]))
         compare(a_mats[z], b_mats[z], outs[z], n, n, n, "f16", "f16", rows=rows)
+
+
+def _sampled_batch_check(batch, M, N, K, din, dout, dist, rows_per, seed):
+    """The bench's contiguous [batch, rows, cols] layout at full size: every
+    product's C is checked on a seeded sample of rows (all columns)."""
+    a_mats, b_mats, outs = run_batched(batch, M, N, K, din, dout, dist=dist)
+    rng = np.random.default_rng(seed)
+    for z in range(batch):
+        rows = np.unique(np.concatenate([rng.choice(M, min(rows_per, M), replace=False),
+                                         [0, M - 1]]))
+        compare(a_mats[z], b_mats[z], outs[z], M, N, K, din, dout, rows=rows)
+
+
+def test_bench_batch_16x2048_f16():
+    _sampled_batch_check(16, 2048, 2048, 2048, "f16", "f16", "uniform", 6, 11)
+
+
+def test_bench_batch_64x1024_bf16():
+    _sampled_batch_check(64, 1024, 1024, 1024, "bf16", "bf16", "normal", 4, 12)
+
+
+def test_bench_batch_32_small_m():
+    # 32 products of 64 x 8192 x 8192 (the small-M kernel, two CTAs per SM):
+    # every row of every product
+    _sampled_batch_check(32, 64, 8192, 8192, "f16", "f16", "uniform", 64, 13)

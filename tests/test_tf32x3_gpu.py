@@ -103,3 +103,19 @@ def test_fused_epilogue():
     err = np.abs(out.cpu().numpy().astype(np.float64) - D_ref)
     assert np.all(err <= oracle.rel_tol_3xtf32(K) * S + oracle.ulp(D_ref, "f32") +
                   2.0 ** -20 * (np.abs(C_ref) + 1.0))
+
+
+def test_bench_shape_4096_sampled():
+    n = 4096
+    a, b, c = run_gemm(n, n, n, "f32", "f32", **X3)
+    rows = np.unique(np.concatenate([np.random.default_rng(14).choice(n, 16, replace=False),
+                                     [0, n - 1]]))
+    check_x3(a, b, c, n, n, n, rows=rows)
+
+
+def test_multicast_pairs():
+    # TF32 on clusters of two CTA pairs sharing A (one pass and three)
+    a, b, c = run_gemm(1000, 1999, 777, "f32", "f32", path=tg.TG_PATH_TC_PAIR, multicast=2)
+    compare(a, b, c, 1000, 1999, 777, "f32", "f32")
+    a, b, c = run_gemm(1000, 1999, 777, "f32", "f32", path=tg.TG_PATH_TC_PAIR, multicast=2, **X3)
+    check_x3(a, b, c, 1000, 1999, 777)

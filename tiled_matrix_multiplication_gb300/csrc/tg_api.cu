@@ -237,7 +237,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         if (opt && opt->block_n && opt->block_n != cd.bn) continue;
         if (cd.pair && cap < 2 * cd.mc) continue;
         if (opt && opt->multicast && opt->multicast != cd.mc) continue;
-        if (cd.mc == 2 && ((opt && (opt->splits > 1 || opt->tail_splits)) || din == TG_F32))
+        if (cd.mc == 2 && opt && (opt->splits > 1 || opt->tail_splits))
             continue;
         const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
         // resident clusters: 4-CTA clusters can leave SMs of a GPC unused
