@@ -11,6 +11,8 @@
 // splitk_reduce: C[m,n] = round(epilogue(sum_{s=0}^{S-1} P[s,m,n])) in increasing s --
 //   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
 //   both steps"), finished across work units instead of inside one.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,28 +36,44 @@ __global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *_
     }
 }
 
-// dst[c * ld_dst + r] = src[r * ld_src + c] for a rows x cols block, through
-// 32 x 32 shared-memory tiles so both the reads and the writes are coalesced.
+// dst[c * ld_dst + r] = src[r * ld_src + c] for a rows x cols block.  One
+// block per 32-row x 128-column tile (four 32 x 32 shared-memory sub-tiles,
+// padded against bank conflicts): each thread issues its 16 loads before any
+// store, so a warp keeps 16 row segments of 128 bytes in flight, and both the
+// reads of src and the writes of dst are whole 128-byte rows.
+constexpr int kTrRows = 32, kTrCols = 128;
+
 template <typename T>
-__global__ void pack_transpose_kernel(const T *__restrict__ src, int64_t ld_src,
-                                      T *__restrict__ dst, int64_t ld_dst, int64_t rows,
-                                      int64_t cols) {
-    __shared__ T tile[32][33];
-    const int64_t tiles_c = (cols + 31) / 32;
-    const int64_t tiles_r = (rows + 31) / 32;
-    for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
-        const int64_t r0 = (t / tiles_c) * 32;
-        const int64_t c0 = (t % tiles_c) * 32;
-        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-            const int64_t r = r0 + i, c = c0 + threadIdx.x;
-            if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * ld_src + c];
+__global__ void __launch_bounds__(256) pack_transpose_kernel(const T *__restrict__ src,
+                                                             int64_t ld_src, T *__restrict__ dst,
+                                                             int64_t ld_dst, int64_t rows,
+                                                             int64_t cols) {
+    __shared__ T tile[kTrCols / 32][32][33];
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTrRows; r0 < rows;
+         r0 += static_cast<int64_t>(gridDim.y) * kTrRows) {
+    T v[kTrCols / 32][4];
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = r0 + ty + 8 * i, c = c0 + 32 * sb + tx;
+            v[sb][i] = (r < rows && c < cols) ? src[r * ld_src + c] : T(0);
         }
-        __syncthreads();
-        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-            const int64_t c = c0 + i, r = r0 + threadIdx.x;
-            if (r < rows && c < cols) dst[c * ld_dst + r] = tile[threadIdx.x][i];
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tile[sb][ty + 8 * i][tx] = v[sb][i];
+    __syncthreads();
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t c = c0 + 32 * sb + ty + 8 * i, r = r0 + tx;
+            if (r < rows && c < cols) dst[c * ld_dst + r] = tile[sb][tx][ty + 8 * i];
         }
-        __syncthreads();
+    __syncthreads();   // the tile is refilled by the next row tile
     }
 }
 
@@ -92,32 +110,46 @@ __global__ void split3_rows_kernel(const float *__restrict__ a, int64_t lda, flo
     }
 }
 
-// B'^T = [hi(B)^T | hi(B)^T | lo(B)^T], [N, 3K] with pitch ld_dst, through
-// 32 x 32 shared-memory tiles so reads of B and writes of B'^T are coalesced.
-__global__ void split3_transpose_kernel(const float *__restrict__ b, int64_t ldb,
-                                        float *__restrict__ dst, int64_t ld_dst, int64_t K,
-                                        int64_t N) {
-    __shared__ float hi_t[32][33], lo_t[32][33];
-    const int64_t tiles_n = (N + 31) / 32;
-    const int64_t tiles_k = (K + 31) / 32;
-    for (int64_t t = blockIdx.x; t < tiles_k * tiles_n; t += gridDim.x) {
-        const int64_t k0 = (t / tiles_n) * 32;
-        const int64_t n0 = (t % tiles_n) * 32;
-        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-            const int64_t k = k0 + i, n = n0 + threadIdx.x;
-            if (k < K && n < N) split_tf32(b[k * ldb + n], hi_t[i][threadIdx.x], lo_t[i][threadIdx.x]);
+// B'^T = [hi(B)^T | hi(B)^T | lo(B)^T], [N, 3K] with pitch ld_dst: the
+// transpose above (32 K rows x 128 N columns per block, 16 loads in flight
+// per thread) with each element split on the way.
+__global__ void __launch_bounds__(256) split3_transpose_kernel(const float *__restrict__ b,
+                                                               int64_t ldb,
+                                                               float *__restrict__ dst,
+                                                               int64_t ld_dst, int64_t K,
+                                                               int64_t N) {
+    __shared__ float hi_t[kTrCols / 32][32][33], lo_t[kTrCols / 32][32][33];
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTrRows; k0 < K;
+         k0 += static_cast<int64_t>(gridDim.y) * kTrRows) {
+    float v[kTrCols / 32][4];
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t k = k0 + ty + 8 * i, n = n0 + 32 * sb + tx;
+            v[sb][i] = (k < K && n < N) ? b[k * ldb + n] : 0.f;
         }
-        __syncthreads();
-        for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-            const int64_t n = n0 + i, k = k0 + threadIdx.x;
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            split_tf32(v[sb][i], hi_t[sb][ty + 8 * i][tx], lo_t[sb][ty + 8 * i][tx]);
+    __syncthreads();
+#pragma unroll
+    for (int sb = 0; sb < kTrCols / 32; ++sb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t n = n0 + 32 * sb + ty + 8 * i, k = k0 + tx;
             if (k < K && n < N) {
                 float *row = dst + n * ld_dst;
-                row[k] = hi_t[threadIdx.x][i];
-                row[K + k] = hi_t[threadIdx.x][i];
-                row[2 * K + k] = lo_t[threadIdx.x][i];
+                row[k] = hi_t[sb][tx][ty + 8 * i];
+                row[K + k] = hi_t[sb][tx][ty + 8 * i];
+                row[2 * K + k] = lo_t[sb][tx][ty + 8 * i];
             }
         }
-        __syncthreads();
+    __syncthreads();   // the tiles are refilled by the next row tile
     }
 }
 
@@ -215,15 +247,16 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
 cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                                   int64_t rows, int64_t cols, int esize, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-    const dim3 block(32, 8);
-    const int blocks = grid_for(tiles * 256, 256);
+    const int64_t gx = (cols + kTrCols - 1) / kTrCols;
+    const int64_t gy = std::min<int64_t>((rows + kTrRows - 1) / kTrRows, 65535);   // + row loop
+    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
     if (esize == 2)
-        pack_transpose_kernel<uint16_t><<<blocks, block, 0, stream>>>(
+        pack_transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(
             static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst,
             rows, cols);
     else if (esize == 4)
-        pack_transpose_kernel<uint32_t><<<blocks, block, 0, stream>>>(
+        pack_transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(
             static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst,
             rows, cols);
     else
@@ -248,9 +281,12 @@ cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld
 cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
                                     int64_t K, int64_t N, cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
-    const int64_t tiles = ((K + 31) / 32) * ((N + 31) / 32);
-    split3_transpose_kernel<<<grid_for(tiles * 256, 256), dim3(32, 8), 0, stream>>>(
-        static_cast<const float *>(b), ldb, static_cast<float *>(dst), ld_dst, K, N);
+    const int64_t gx = (N + kTrCols - 1) / kTrCols;
+    const int64_t gy = std::min<int64_t>((K + kTrRows - 1) / kTrRows, 65535);   // + row loop
+    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    split3_transpose_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
+                              dim3(32, 8), 0, stream>>>(static_cast<const float *>(b), ldb,
+                                                       static_cast<float *>(dst), ld_dst, K, N);
     return cudaGetLastError();
 }
 
