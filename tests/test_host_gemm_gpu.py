@@ -92,3 +92,46 @@ def test_repeated_calls_on_one_stream():
 def test_argument_errors_before_any_copy():
     assert tg.tg_gemm_host(4, 4, 4, 0, 4, 0, 4, 0, 4, "f16", "f16", 0, None) \
         == tg.TG_ERR_INVALID_VALUE
+
+
+def test_alternating_streams():
+    # consecutive calls on two streams overlap their copies; each result is
+    # still complete once its own stream is synchronised
+    import torch
+    M, N, K = 2048, 1024, 512
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    calls = []
+    for i in range(4):
+        a_bits = inputs.matrix_bits(M, K, "bf16", "int", 70 + i)
+        b_bits = inputs.matrix_bits(K, N, "bf16", "int", 80 + i)
+        a, b = pinned(a_bits), pinned(b_bits)
+        c = pinned(np.zeros((M, N), dtype=np.uint16))
+        s = streams[i % 2]
+        assert tg.tg_gemm_host(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                               "bf16", "bf16", s.cuda_stream, None) == tg.TG_OK
+        calls.append((a_bits, b_bits, a, b, c, s))
+    for a_bits, b_bits, _, _, c, s in calls:
+        s.synchronize()
+        compare(a_bits, b_bits, c.numpy(), M, N, K, "bf16", "bf16", exact=True)
+
+
+def test_result_feeds_the_next_call_on_one_stream():
+    # the second call reads, as its A, the host buffer the first call writes:
+    # stream order makes the first call's copy-back land before the read
+    import torch
+    n = 1024
+    s = torch.cuda.current_stream()
+    a_bits = inputs.matrix_bits(n, n, "f32", "int", 90)
+    b_bits = inputs.matrix_bits(n, n, "f32", "int", 91)
+    a, b = pinned(a_bits), pinned(b_bits)
+    c1 = pinned(np.zeros((n, n), dtype=np.uint32))
+    c2 = pinned(np.zeros((n, n), dtype=np.uint32))
+    assert tg.tg_gemm_host(n, n, n, a.data_ptr(), n, b.data_ptr(), n, c1.data_ptr(), n, "f32",
+                           "f32", s.cuda_stream, None) == tg.TG_OK
+    assert tg.tg_gemm_host(n, n, n, c1.data_ptr(), n, b.data_ptr(), n, c2.data_ptr(), n, "f32",
+                           "f32", s.cuda_stream, None) == tg.TG_OK
+    s.synchronize()
+    compare(a_bits, b_bits, c1.numpy(), n, n, n, "f32", "f32", exact=True)
+    # C1 holds integers up to 4096 in magnitude: exact in TF32 only below 2^11,
+    # so the second product is checked within the TF32 tolerance
+    compare(c1.numpy(), b_bits, c2.numpy(), n, n, n, "f32", "f32")
