@@ -140,12 +140,12 @@ def test_plan_tf32(lib):
     assert p["workspace_bytes"] >= 1000 * 780 * 4 + 1999 * 780 * 4
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 128])
+@pytest.mark.parametrize("M", [1, 16, 64])
 def test_plan_skinny_splits_k(lib, M):
     st, p = plan(M, 8192, 8192, sms=148)
     assert st == tg.TG_OK
     assert p["path"] == tg.TG_PATH_SKINNY and p["block_n"] in (128, 256, 512)
-    assert p["block_m"] == {1: 16, 16: 16, 64: 64, 128: 128}[M]
+    assert p["block_m"] == {1: 16, 16: 16, 64: 64}[M]
     assert p["tiles"] == 8192 // p["block_n"] and p["splits"] in (2, 4, 8)
     # one CTA per unit, all resident at once (two per SM when there are more
     # units than SMs), with the largest cluster that allows that
@@ -192,8 +192,19 @@ def test_plan_multicast_rules(lib):
     assert st == tg.TG_OK and p["multicast"] == 2 and p["ctas"] % 4 == 0
     st, p = plan(4096, 4096, 4096, multicast=1, sms=148)
     assert st == tg.TG_OK and p["multicast"] == 1
-    for bad in (dict(multicast=2, path=tg.TG_PATH_TC), dict(multicast=2, splits=2),
-                dict(multicast=2, block_n=128), dict(multicast=2, tail_splits=2)):
+    # single CTAs share A in clusters of two (128- or 256-wide tiles); pairs in
+    # clusters of two pairs (192, 224, 256); either may split K
+    st, p = plan(4096, 4096, 4096, multicast=2, path=tg.TG_PATH_TC, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC and p["ctas"] % 2 == 0
+    st, p = plan(4096, 4096, 4096, multicast=2, path=tg.TG_PATH_TC, block_n=128, sms=148)
+    assert st == tg.TG_OK and p["block_n"] == 128 and p["multicast"] == 2
+    st, p = plan(128, 8192, 8192, multicast=2, path=tg.TG_PATH_TC, splits=4, sms=148)
+    assert st == tg.TG_OK and p["splits"] == 4 and p["kernels"] == 2
+    st, p = plan(4096, 4096, 4096, multicast=2, splits=2, sms=148)
+    assert st == tg.TG_OK and p["splits"] == 2
+    for bad in (dict(multicast=2, path=tg.TG_PATH_TC, block_n=192),
+                dict(multicast=2, path=tg.TG_PATH_TC_PAIR, block_n=128),
+                dict(multicast=2, tail_splits=2), dict(multicast=2, path=tg.TG_PATH_SKINNY)):
         st, _ = plan(4096, 4096, 4096, **bad)
         assert st == tg.TG_ERR_UNSUPPORTED, bad
     st, _ = plan(4096, 4096, 4096, multicast=3)
@@ -246,7 +257,7 @@ def test_selftest_timeout_argument_range(lib):
 
 
 @pytest.mark.parametrize("opts", [dict(path=tg.TG_PATH_TC_PAIR, max_ctas=1),
-                                  dict(multicast=2, max_ctas=3),
+                                  dict(multicast=2, max_ctas=1),
                                   dict(path=tg.TG_PATH_TC_PAIR, block_n=256, multicast=2,
                                        max_ctas=2)])
 def test_options_that_exclude_every_variant(lib, opts):
@@ -258,3 +269,17 @@ def test_options_that_exclude_every_variant(lib, opts):
                                              1024 * 1024, C, 1024, 1024 * 1024, "f16", "f16",
                                              148, o)
     assert st == tg.TG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M,din", [(65, "f16"), (128, "f16"), (128, "bf16"), (33, "e4m3"),
+                                   (128, "e4m3")])
+def test_plan_mid_m_uses_single_cta_tiles(lib, M, din):
+    # 65..128 rows (33..128 for FP8): 128-wide single-CTA tiles with a K split
+    st, p = plan(M, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC
+    assert p["block_m"] == 128 and p["block_n"] == 128 and p["multicast"] == 1
+    assert p["splits"] >= 2
+    # the small-M kernel can still be forced up to 128 rows
+    st, p = plan(M, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148,
+                 path=tg.TG_PATH_SKINNY)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_SKINNY

@@ -194,3 +194,7 @@ def test_bench_batch_32_small_m():
     # 32 products of 64 x 8192 x 8192 (the small-M kernel, two CTAs per SM):
     # every row of every product
     _sampled_batch_check(32, 64, 8192, 8192, "f16", "f16", "uniform", 64, 13)
+
+
+def test_single_cta_multicast_batched():
+    check_all(3, 300, 520, 256, "f16", "f16", path=tg.TG_PATH_TC, multicast=2, block_n=128)

@@ -101,9 +101,10 @@ def test_paths_and_activations(path, act):
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("M", [1, 40, 128])
 def test_small_m_kernel(M, act):
-    p = tg.plan(M, 1000, 700, "bf16", num_sms=152)
+    p = tg.plan(M, 1000, 700, "bf16", num_sms=152, path=tg.TG_PATH_SKINNY)
     assert p["path"] == tg.TG_PATH_SKINNY
-    run_fused(M, 1000, 700, "bf16", "bf16", act=act, alpha=1.25, beta=1.0)
+    run_fused(M, 1000, 700, "bf16", "bf16", act=act, alpha=1.25, beta=1.0,
+              path=tg.TG_PATH_SKINNY)
 
 
 @pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
@@ -160,3 +161,10 @@ def test_torch_helper():
     ok, rep = oracle.epilogue.check_epilogue(out.cpu().numpy().astype(np.float64), C_ref, S,
                                              "bf16", "f32", bias=bias.cpu().numpy(), act="relu")
     assert ok, rep
+
+
+def test_single_cta_multicast_epilogue():
+    run_fused(300, 1100, 512, "f16", "f16", act="gelu_tanh", alpha=0.5, beta=1.0,
+              path=tg.TG_PATH_TC, multicast=2, block_n=256)
+    run_fused(128, 2048, 2048, "bf16", "bf16", act="silu", beta=0.5,
+              path=tg.TG_PATH_TC, multicast=2, block_n=128, splits=4)

@@ -68,10 +68,13 @@ def test_tail_split():
 def test_small_m_kernel_exact(fmt, M):
     # the transposed streaming kernel with FP8 operands (kind::f8f6f4 with an
     # N-major B^T as the MMA's A operand), K split over a 4-CTA cluster
-    p = tg.plan(M, 8192, 8192, fmt, "f16", num_sms=152)
+    p = tg.plan(M, 8192, 8192, fmt, "f16", num_sms=152, path=tg.TG_PATH_SKINNY)
     assert p["path"] == tg.TG_PATH_SKINNY and p["block_k"] == 128
-    a, b, c = run_gemm(M, 8192, 8192, fmt, "f16", dist="int")
+    a, b, c = run_gemm(M, 8192, 8192, fmt, "f16", dist="int", path=tg.TG_PATH_SKINNY)
     compare(a, b, c, M, 8192, 8192, fmt, "f16", exact=True)
+    if M > 32:   # what the planner picks for these rows: single-CTA tiles, K split
+        a, b, c = run_gemm(M, 8192, 8192, fmt, "f16", dist="int")
+        compare(a, b, c, M, 8192, 8192, fmt, "f16", exact=True)
 
 
 @pytest.mark.parametrize("M,N,K,opts", [

@@ -217,3 +217,21 @@ def test_multicast_pairs_uniform(din, dout):
                        ldc=N + 8)
     compare(a, b, c, M, N, K, din, dout)
     assert padding_untouched(c, N, dout)
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("M,N,K,splits", [(300, 1100, 512, 0), (128, 8192, 2048, 4),
+                                          (513, 640, 300, 2), (130, 2000, 777, 0)])
+def test_single_cta_multicast_exact(block_n, M, N, K, splits):
+    """Clusters of two single CTAs on adjacent tiles sharing A by multicast,
+    with and without a K split; odd tile counts leave a half-empty unit."""
+    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=1, block_n=block_n, multicast=2,
+                       splits=splits)
+    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
+
+
+@pytest.mark.parametrize("din,dout", [("bf16", "f32"), ("e4m3", "bf16"), ("f32", "f32")])
+def test_single_cta_multicast_types(din, dout):
+    a, b, c = run_gemm(300, 1100, 640, din, dout, path=1, block_n=128, multicast=2, ldc=1104)
+    compare(a, b, c, 300, 1100, 640, din, dout)
+    assert padding_untouched(c, 1100, dout)

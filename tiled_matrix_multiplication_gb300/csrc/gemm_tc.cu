@@ -60,14 +60,17 @@ int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair) {
     return ((cols * es) % 128 != 0 && (cols * es) % 64 == 0) ? 64 : 128;
 }
 
-bool tc_supported_mc(int block_n, int mc) {
-    return mc == 1 || (mc == 2 && (block_n == 192 || block_n == 224 || block_n == 256));
+bool tc_supported_mc(int block_n, int mc, bool pair) {
+    if (mc == 1) return true;
+    if (mc != 2) return false;
+    return pair ? (block_n == 192 || block_n == 224 || block_n == 256)
+                : (block_n == 128 || block_n == 256);
 }
 
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream) {
-    if (mc == 2 && !pair) return cudaErrorInvalidValue;
+    if (!tc_supported_mc(block_n, mc, pair)) return cudaErrorInvalidValue;
     switch (in_kind) {
     case IN_F16:
     case IN_BF16:

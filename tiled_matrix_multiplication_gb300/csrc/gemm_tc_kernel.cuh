@@ -128,7 +128,7 @@ struct TcCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-    static_assert(MC == 1 || (MC == 2 && PAIR), "A multicast pairs CTA pairs");
+    static_assert(MC == 1 || MC == 2, "A is shared by at most two tiles");
 };
 
 struct Work {
@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = PAIR ? cluster_cta_rank() : 0u;       // rank in the cluster
+    constexpr bool CLUSTERED = PAIR || MC > 1;
+    const uint32_t crank = CLUSTERED ? cluster_cta_rank() : 0u;  // rank in the cluster
     const uint32_t rank = crank % CG;                             // position in the pair
     const int q = static_cast<int>(crank / CG);                   // pair within the cluster
     const uint32_t pair_leader = static_cast<uint32_t>(q * CG);   // cluster rank of my leader
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync_all();   // peer barriers initialised before any remote signal
+    if constexpr (CLUSTERED) cluster_sync_all();   // peer barriers initialised before any remote signal
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Prologue done: let the next kernel's prologue start, then wait for the
@@ -357,10 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
                         const uint32_t dst = sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2);
                         const int ya = row0 + q * (Cfg::CTA_M / 2);
-                        if (p.a_batched)
-                            tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
-                        else
-                            tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
+                        if constexpr (PAIR) {
+                            if (p.a_batched)
+                                tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
+                            else
+                                tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
+                        } else {
+                            if (p.a_batched)
+                                tma_load_3d_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
+                            else
+                                tma_load_2d_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
+                        }
                     } else {
                         load(sA + stage * Cfg::A_STAGE, &tmA, p.a_batched, kt * Cfg::BK, row0);
                     }
@@ -437,6 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if constexpr (PAIR)   // every CTA whose stage this pair read from
                         umma_commit_pair(empty_bar(stage), MC == 2 ? 0xF : 0x3);
+                    else if constexpr (MC == 2)   // both CTAs filled this stage's A
+                        umma_commit_mc(empty_bar(stage), 0x3);
                     else
                         umma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -564,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync_all();   // the peer is done with this CTA's smem/TMEM
+    // the peers are done with this CTA's smem, barriers and TMEM
+    if constexpr (CLUSTERED) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
@@ -593,7 +604,7 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if constexpr (PAIR) {
+    if constexpr (PAIR || MC > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = Cfg::CLUSTER;
         attr[1].val.clusterDim.y = 1;
@@ -629,11 +640,17 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
 template <int IN_KIND, bool PAIR, int MC>
 cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const TcParams &p, int ctas, cudaStream_t stream) {
-    if constexpr (MC == 2) {
+    if constexpr (MC == 2 && PAIR) {
         switch (block_n) {
         case 192: return launch_impl<IN_KIND, 192, true, 2>(tmA, tmB, p, ctas, stream);
         case 224: return launch_impl<IN_KIND, 224, true, 2>(tmA, tmB, p, ctas, stream);
         case 256: return launch_impl<IN_KIND, 256, true, 2>(tmA, tmB, p, ctas, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    } else if constexpr (MC == 2) {
+        switch (block_n) {
+        case 128: return launch_impl<IN_KIND, 128, false, 2>(tmA, tmB, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, false, 2>(tmA, tmB, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
     } else if constexpr (PAIR) {
@@ -672,9 +689,11 @@ template <int IN_KIND>
 cudaError_t launch_variant(int block_n, bool pair, int mc, const CUtensorMap &tmA,
                            const CUtensorMap &tmB, const TcParams &p, int ctas,
                            cudaStream_t stream) {
-    return mc == 2 ? launch_kind<IN_KIND, true, 2>(block_n, tmA, tmB, p, ctas, stream)
-           : pair  ? launch_kind<IN_KIND, true, 1>(block_n, tmA, tmB, p, ctas, stream)
-                   : launch_kind<IN_KIND, false, 1>(block_n, tmA, tmB, p, ctas, stream);
+    if (mc == 2)
+        return pair ? launch_kind<IN_KIND, true, 2>(block_n, tmA, tmB, p, ctas, stream)
+                    : launch_kind<IN_KIND, false, 2>(block_n, tmA, tmB, p, ctas, stream);
+    return pair ? launch_kind<IN_KIND, true, 1>(block_n, tmA, tmB, p, ctas, stream)
+                : launch_kind<IN_KIND, false, 1>(block_n, tmA, tmB, p, ctas, stream);
 }
 
 }  // namespace

@@ -131,10 +131,14 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             return TG_ERR_INVALID_VALUE;
         if (opt->f32_mode == TG_F32_3XTF32 && (din != TG_F32 || 3 * K > kMaxDim))
             return TG_ERR_UNSUPPORTED;
-        if (opt->multicast == 2 &&
-            (opt->path == TG_PATH_TC || opt->path == TG_PATH_SKINNY || opt->splits > 1 ||
-             opt->tail_splits || (opt->block_n && !tg::tc_supported_mc(opt->block_n, 2))))
-            return TG_ERR_UNSUPPORTED;
+        if (opt->multicast == 2) {
+            const bool pair_ok = opt->path != TG_PATH_TC &&
+                                 (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, true));
+            const bool single_ok = opt->path != TG_PATH_TC_PAIR &&
+                                   (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, false));
+            if (opt->path == TG_PATH_SKINNY || opt->tail_splits || (!pair_ok && !single_ok))
+                return TG_ERR_UNSUPPORTED;
+        }
         if (opt->tail_splits < 0 || opt->tail_splits == 1 || opt->tail_splits > 8)
             return TG_ERR_INVALID_VALUE;
         if (opt->path < TG_PATH_AUTO || opt->path > TG_PATH_SKINNY) return TG_ERR_INVALID_VALUE;
@@ -223,30 +227,39 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // an FP32 partial tile that a second kernel sums (about 24 K tiles' worth
     // for 128 rows, less for fewer rows).  Ties go to the earlier candidate.
     // Relative efficiencies (percent of the best variant) measured on GB300 at
-    // 8192^3 and on the prefill shapes.
-    // mc = 2: clusters of two pairs sharing A by multicast (two tiles per unit).
+    // 8192^3 and on the prefill shapes; single-CTA clusters sharing A measured
+    // about 5 % slower than unshared single CTAs at 128 to 2048 rows.
+    // mc = 2: clusters of two pairs (or two single CTAs) sharing A by multicast
+    // (two tiles per unit).
     struct Cand { bool pair; int mc; int bn; int eff; };
     static const Cand kCands[] = {
         {true, 2, 256, 105}, {true, 1, 256, 100}, {true, 2, 224, 90}, {true, 2, 192, 86},
-        {true, 1, 224, 92}, {true, 1, 192, 84}, {false, 1, 256, 90},
-        {false, 1, 192, 82}, {false, 1, 224, 80}, {true, 1, 128, 62}, {false, 1, 128, 62}};
+        {true, 1, 224, 92}, {true, 1, 192, 84}, {false, 1, 256, 90}, {false, 2, 256, 85},
+        {false, 1, 192, 82}, {false, 1, 224, 80}, {false, 1, 128, 62}, {true, 1, 128, 62},
+        {false, 2, 128, 58}};
+    // At most 128 rows the product streams B (memory-bound): single-CTA tiles
+    // 128 wide, with the K split below, measured fastest (pair tiles would be
+    // half empty; wider tiles give fewer concurrent streams).
+    const bool few_rows = M <= kBlockM && !(opt && (opt->block_n || opt->multicast ||
+                                                     opt->path == TG_PATH_TC_PAIR));
     double best_cost = -1.0;
     for (const Cand &cd : kCands) {
+        if (few_rows && (cd.pair || cd.mc != 1 || cd.bn != 128)) continue;
         if (opt && opt->path == TG_PATH_TC && cd.pair) continue;
         if (opt && opt->path == TG_PATH_TC_PAIR && !cd.pair) continue;
         if (opt && opt->block_n && opt->block_n != cd.bn) continue;
-        if (cd.pair && cap < 2 * cd.mc) continue;
+        const int64_t cl = (cd.pair ? 2 : 1) * cd.mc;   // CTAs per cluster
+        if (cap < cl) continue;
         if (opt && opt->multicast && opt->multicast != cd.mc) continue;
-        if (cd.mc == 2 && opt && (opt->splits > 1 || opt->tail_splits))
-            continue;
+        if (cd.mc == 2 && opt && opt->tail_splits) continue;
         const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
         // resident clusters: 4-CTA clusters can leave SMs of a GPC unused
         int64_t resident = cap;
-        if (cd.pair) {
+        if (cl > 1) {
             // without a device: 4-CTA clusters measured at 36 on 152 SMs
-            const int64_t est = cd.mc == 2 ? (quad_slots ? quad_slots : num_sms * 19 / 80)
-                                           : (pair_slots ? pair_slots : num_sms / 2);
-            resident = std::min<int64_t>(cap / (2 * cd.mc), est);
+            const int64_t est = cl == 4 ? (quad_slots ? quad_slots : num_sms * 19 / 80)
+                                        : (pair_slots ? pair_slots : num_sms / 2);
+            resident = std::min<int64_t>(cap / cl, est);
         }
         const int64_t slots = std::max<int64_t>(1, resident);
         // work units: tiles, or pairs of horizontally adjacent tiles
@@ -254,7 +267,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         int64_t s_lo = 1, s_hi = 1;
         if (opt && opt->splits && batch == 1) {
             s_lo = s_hi = opt->splits;
-        } else if (tiles < slots / 2 && cd.mc == 1 && batch == 1) {
+        } else if (tiles < slots / 2 && batch == 1) {
             s_hi = std::min<int64_t>(pl->k_tiles, 16);   // too few tiles: consider split K
         }
         for (int64_t s = s_lo; s <= s_hi; ++s) {
@@ -292,7 +305,12 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // Small M with 16-bit operands: the transposed streaming kernel (one tile
     // holds all rows; work is spread over 128-column tiles and K splits).
     const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
-    const bool skinny_ok = din != TG_F32 && M <= 128 &&
+    // The transposed streaming kernel wins for up to 64 rows of 16-bit operands
+    // and up to 32 of FP8 ones; beyond that (to 128 rows, where it can still
+    // be forced) the tile kernel with a K split measured faster on GB300
+    // (M = 128, N = K = 8192: FP16 35.0 vs 39.0 us, E4M3 23.7 vs 29.6 us).
+    const int64_t skinny_rows_max = forced_skinny ? 128 : (is_fp8(din) ? 32 : 64);
+    const bool skinny_ok = din != TG_F32 && M <= skinny_rows_max &&
                            (forced_skinny || !(opt && opt->block_n)) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&
                            batch <= kMaxGridY;
@@ -359,10 +377,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     if (p.path == TG_PATH_SKINNY) {
         p.ctas = static_cast<int32_t>(units);   // not persistent: one CTA per unit
         p.multicast = 1;
-    } else if (pair) {
-        const int64_t cl = 2 * std::max(p.multicast, 1);
+    } else if (pair || p.multicast == 2) {
+        const int64_t cl = (pair ? 2 : 1) * std::max(p.multicast, 1);
         int64_t resident = cap / cl;
-        if (p.multicast == 2) resident = std::min<int64_t>(resident, quad_slots ? quad_slots : num_sms * 19 / 80);
+        if (cl == 4) resident = std::min<int64_t>(resident, quad_slots ? quad_slots : num_sms * 19 / 80);
         else resident = std::min<int64_t>(resident, pair_slots ? pair_slots : num_sms / 2);
         const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, resident));
         p.ctas = static_cast<int32_t>(cl * clusters);

@@ -105,10 +105,12 @@ cudaError_t launch_gemm_skinny_fp8(int in_kind, int mp, int nt, const CUtensorMa
 
 // gemm_tc.cu
 // `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `mc` = 2: clusters
-// of two pairs sharing A by multicast (pair only); `ctas` counts CTAs.
+// of two pairs (or two single CTAs) sharing A by multicast; `ctas` counts CTAs.
 int tc_stages(int in_kind, int block_n, bool pair);
 bool tc_supported_block_n(int block_n, bool pair);
-bool tc_supported_mc(int block_n, int mc);
+// A-multicast clusters (mc = 2): pairs with 192-, 224- or 256-wide tiles,
+// single CTAs with 128- or 256-wide tiles.
+bool tc_supported_mc(int block_n, int mc, bool pair);
 // Swizzle (row bytes of a TMA box) of the N-major B tile of a variant.
 int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair);
 // Clusters of `cluster_size` (2 or 4) CTAs of the pair kernel resident at
