@@ -51,6 +51,8 @@ METRIC = "GEMM TFLOP/s (FP16/BF16 at 4096³) and % of GB300 dense tensor peak, 1
 
 WORKLOADS = {
     # name: (M, N, K, dtype_in, dtype_out, dist, description)
+    "small127_f16": (127, 255, 65, "f16", "f32", "uniform",
+                     "ragged 127x255x65, FP16 in U[-1,1), FP32 out (the correctness case)"),
     "square4096_f16": (4096, 4096, 4096, "f16", "f16", "uniform",
                        "square GEMM 4096^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
     "square8192_f16": (8192, 8192, 8192, "f16", "f16", "uniform",
