@@ -31,7 +31,9 @@
  *                           FP8 input path of "Triton tiled matmul"
  *                           (llm-systems-cookbook), section "Exercises", item 2.
  *                           Row pitches (lda, ldb) and bases of A and B that are
- *                           not multiples of 16 bytes are packed first.
+ *                           not multiples of 16 bytes are packed first.  Per-tensor
+ *                           scale factors of FP8 data go in as the product
+ *                           scale_a * scale_b in tg_gemm_fused's alpha.
  * Any other pair returns TG_ERR_UNSUPPORTED.
  *
  * Ownership.  a, b and c are DEVICE pointers owned by the caller and must stay

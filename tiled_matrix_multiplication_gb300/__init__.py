@@ -69,8 +69,8 @@ def gemm(a, b, out_dtype=None, out=None, stream=None, **options):
     column stride (any row stride).  ``out_dtype`` defaults to the input dtype;
     ``out`` may be a preallocated [M, N] tensor with unit column stride.
     ``options`` are tg_options fields (path, splits, block_n, group_m, max_ctas,
-    timeout_ms).  Raises ``ValueError`` on a shape mismatch and ``TgError`` on
-    any status other than TG_OK.
+    timeout_ms, tail_splits, multicast, f32_mode).  Raises ``ValueError`` on a
+    shape mismatch and ``TgError`` on any status other than TG_OK.
     """
     import torch
     if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
