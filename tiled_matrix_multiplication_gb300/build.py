@@ -23,8 +23,9 @@ BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtg_gemm.so")
 
-SOURCES = ["tg_api.cu", "gemm_tc.cu", "gemm_tc_f16.cu", "gemm_tc_tf32.cu", "gemm_tc_fp8.cu",
-           "gemm_skinny.cu", "gemm_skinny_fp8.cu", "aux_kernels.cu", "noalloc.cu"]
+SOURCES = ["tg_api.cu", "tg_plan.cu", "tg_host.cu", "gemm_tc.cu", "gemm_tc_f16.cu",
+           "gemm_tc_tf32.cu", "gemm_tc_fp8.cu", "gemm_skinny.cu", "gemm_skinny_fp8.cu",
+           "aux_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-O2", f"-I{INCLUDE}", f"-I{CSRC}"]
