@@ -198,3 +198,8 @@ def test_bench_batch_32_small_m():
 
 def test_single_cta_multicast_batched():
     check_all(3, 300, 520, 256, "f16", "f16", path=tg.TG_PATH_TC, multicast=2, block_n=128)
+
+
+def test_small_m_shared_a_batched():
+    check_all(5, 48, 1100, 640, "f16", "f16", path=tg.TG_PATH_SKINNY, multicast=2, splits=2)
+    check_all(3, 64, 1024, 512, "bf16", "bf16", path=tg.TG_PATH_SKINNY, multicast=2, sa=0)

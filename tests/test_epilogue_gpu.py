@@ -168,3 +168,8 @@ def test_single_cta_multicast_epilogue():
               path=tg.TG_PATH_TC, multicast=2, block_n=256)
     run_fused(128, 2048, 2048, "bf16", "bf16", act="silu", beta=0.5,
               path=tg.TG_PATH_TC, multicast=2, block_n=128, splits=4)
+
+
+def test_small_m_shared_a_epilogue():
+    run_fused(64, 1100, 1024, "f16", "f16", act="silu", alpha=0.5, beta=1.0,
+              path=tg.TG_PATH_SKINNY, multicast=2, splits=4)

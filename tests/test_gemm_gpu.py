@@ -235,3 +235,28 @@ def test_single_cta_multicast_types(din, dout):
     a, b, c = run_gemm(300, 1100, 640, din, dout, path=1, block_n=128, multicast=2, ldc=1104)
     compare(a, b, c, 300, 1100, 640, din, dout)
     assert padding_untouched(c, 1100, dout)
+
+
+@pytest.mark.parametrize("M", [16, 37, 64, 128])
+@pytest.mark.parametrize("N,K,splits", [(1100, 1000, 4), (1000, 700, 2), (384, 513, 1)])
+def test_skinny_shared_a_exact(M, N, K, splits):
+    """The small-M kernel with A^T shared by two adjacent column tiles
+    (multicast); odd tile counts leave the last CTA of a pair past N."""
+    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=3, multicast=2, splits=splits)
+    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
+
+
+@pytest.mark.parametrize("din,dout", [("bf16", "f32"), ("e4m3", "f16"), ("e5m2", "bf16")])
+def test_skinny_shared_a_types(din, dout):
+    a, b, c = run_gemm(64, 2100, 1536, din, dout, path=3, multicast=2, ldc=2104)
+    compare(a, b, c, 64, 2100, 1536, din, dout)
+    assert padding_untouched(c, 2100, dout)
+
+
+def test_skinny_shared_a_full_size():
+    # 64 x 8192 x 8192 with two CTAs per SM in clusters of 8 (4 K ranges x 2 tiles)
+    import tiled_matrix_multiplication_gb300 as tg
+    p = tg.plan(64, 8192, 8192, "f16", num_sms=152, path=3, multicast=2)
+    assert p["path"] == tg.TG_PATH_SKINNY and p["multicast"] == 2 and p["ctas"] == 256
+    a, b, c = run_gemm(64, 8192, 8192, "f16", "f16", dist="int", path=3, multicast=2)
+    compare(a, b, c, 64, 8192, 8192, "f16", "f16", exact=True)

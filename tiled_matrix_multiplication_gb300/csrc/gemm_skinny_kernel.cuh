@@ -122,16 +122,25 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int splits = static_cast<int>(cluster_num_ctas());   // == p.splits
-    const int split = static_cast<int>(cluster_cta_rank());
-    const int tn = static_cast<int>(blockIdx.x) / splits;
+    // Cluster = `share` adjacent column tiles x `splits` K ranges; cluster rank
+    // jn * splits + split.  With share = 2 the two CTAs of a K range (one per
+    // column tile) each load half of the A^T rows and multicast them to both.
+    const int share = p.a_share > 1 ? 2 : 1;
+    const int csize = static_cast<int>(cluster_num_ctas());     // splits * share
+    const int splits = csize / share;                            // == p.splits
+    const int crank = static_cast<int>(cluster_cta_rank());
+    const int split = crank % splits;
+    const int jn = crank / splits;
+    const int tn = (static_cast<int>(blockIdx.x) / csize) * share + jn;
+    const uint16_t share_mask =
+        static_cast<uint16_t>((1u << split) | (1u << (splits + split)));   // share == 2
     const int kt0 = split * p.k_tiles_per_split;
     const int kt1 = min(kt0 + p.k_tiles_per_split, p.k_tiles);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), share);   // one MMA commit per CTA reading the stage's A^T
         }
         mbar_init(tfull_bar, 1);
         *abort_flag = 0;
@@ -148,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (share > 1) cluster_sync_all();   // the partner's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Prologue done: let the next kernel's prologue start, then wait for the
@@ -170,10 +180,18 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                 mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
                 const uint32_t fb = full_bar(stage);
                 const int z = static_cast<int>(blockIdx.y);   // batch
-                if (p.a_batched)
+                if (share > 1) {
+                    // rows [jn*MP/2, (jn+1)*MP/2) of A^T, to this CTA and its partner
+                    const uint32_t dst = sAt + stage * Cfg::AT_STAGE + jn * (Cfg::AT_STAGE / 2);
+                    if (p.a_batched)
+                        tma_load_3d_mc(dst, &tmA, fb, kt * Cfg::BK, jn * (MP / 2), z, share_mask);
+                    else
+                        tma_load_2d_mc(dst, &tmA, fb, kt * Cfg::BK, jn * (MP / 2), share_mask);
+                } else if (p.a_batched) {
                     tma_load_3d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0, z);
-                else
+                } else {
                     tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
+                }
 #pragma unroll
                 for (int j = 0; j < NT / Cfg::CHUNK_N; ++j) {
                     const uint32_t dst = sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX;
@@ -229,7 +247,10 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                                               (kt > kt0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                umma_commit(empty_bar(stage));
+                if (share > 1)
+                    umma_commit_mc(empty_bar(stage), share_mask);   // both CTAs filled the A^T
+                else
+                    umma_commit(empty_bar(stage));
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
@@ -304,10 +325,13 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
             const int n = tn * NT + nl;
             const uint32_t off = part_addr + static_cast<uint32_t>((m * NT + nl) * 4);
             float acc = 0.f;
-            for (int s = 0; s < splits; ++s) acc += ld_shared_cluster_f32(map_to_cta(off, s));
+            for (int s = 0; s < splits; ++s)
+                acc += ld_shared_cluster_f32(map_to_cta(off, jn * splits + s));
             if (n < p.N) sk_store(p, m, n, acc);
         }
         cluster_sync_all();                       // peers are done reading this CTA's smem
+    } else if (share > 1) {
+        cluster_sync_all();   // the partner's last commits to this CTA's barriers have landed
     }
     if (warp == 1) {
         tc_fence_after_sync();
@@ -324,13 +348,15 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits),
+    const int share = p.a_share > 1 ? 2 : 1;
+    const int tiles = (p.tiles_n + share - 1) / share * share;   // whole sharing groups
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * p.splits),
                        static_cast<unsigned>(p.batch > 0 ? p.batch : 1), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits * share);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

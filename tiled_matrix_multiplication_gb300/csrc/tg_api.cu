@@ -160,7 +160,9 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
     if (p.path == TG_PATH_SKINNY) {
-        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, p.block_m, nb_a, bt.sa) != TG_OK ||
+        // with A^T shared by two CTAs each loads half of its rows
+        const int a_box_rows = p.multicast == 2 ? p.block_m / 2 : p.block_m;
+        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_box_rows, nb_a, bt.sa) != TG_OK ||
             encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k, nb_b, bt.sb) != TG_OK)
             return fail(map_error());
         tg::SkParams sp;
@@ -178,6 +180,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
         sp.two_per_sm = pl.skinny_two ? 1 : 0;
+        sp.a_share = p.multicast == 2 ? 2 : 1;
         sp.batch = static_cast<int32_t>(bt.count);
         sp.a_batched = nb_a > 1;
         sp.b_batched = nb_b > 1;

@@ -27,7 +27,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
                                  (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, true));
             const bool single_ok = opt->path != TG_PATH_TC_PAIR &&
                                    (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, false));
-            if (opt->path == TG_PATH_SKINNY || opt->tail_splits || (!pair_ok && !single_ok))
+            // the small-M kernel shares A^T between two column tiles, in
+            // clusters of at most 8 CTAs (K split over at most 4)
+            const bool skinny_ok = opt->splits <= 4;
+            if (opt->tail_splits || (opt->path == TG_PATH_SKINNY && !skinny_ok) ||
+                (opt->path != TG_PATH_SKINNY && !pair_ok && !single_ok))
                 return TG_ERR_UNSUPPORTED;
         }
         if (opt->tail_splits < 0 || opt->tail_splits == 1 || opt->tail_splits > 8)
@@ -226,6 +230,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             const int64_t kps = cdiv(ktiles, sc);
             if ((sc - 1) * kps >= ktiles) continue;          // a K range would be empty
             if (opt && opt->splits && opt->splits != sc) continue;
+            if (opt && opt->multicast == 2 && sc > 4) continue;   // clusters of <= 8 CTAs
             if (tiles * sc <= cap) {
                 best_s = sc;
                 two = false;
@@ -243,6 +248,11 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             two = nt == 128 && tiles * best_s > cap;
         }
         pl->skinny_two = two;
+        // A^T shared by the CTAs of two adjacent column tiles (multicast = 2,
+        // clusters of 2 x splits <= 8) halves the re-reads of A, but measured
+        // no faster on GB300 at 16 to 128 rows (N = K = 8192), so only on
+        // request.
+        p.multicast = (opt && opt->multicast) ? opt->multicast : 1;
         p.path = TG_PATH_SKINNY;
         p.block_m = mp;
         p.block_n = nt;
@@ -266,8 +276,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     const int64_t splits = p.splits;
     const int64_t units = p.tiles * splits;   // (tiles = work units: tile pairs when mc = 2)
     if (p.path == TG_PATH_SKINNY) {
-        p.ctas = static_cast<int32_t>(units);   // not persistent: one CTA per unit
-        p.multicast = 1;
+        // not persistent: one CTA per unit, whole sharing groups of column tiles
+        p.ctas = static_cast<int32_t>(round_up(p.tiles, std::max(p.multicast, 1)) * splits);
     } else if (pair || p.multicast == 2) {
         const int64_t cl = (pair ? 2 : 1) * std::max(p.multicast, 1);
         int64_t resident = cap / cl;
