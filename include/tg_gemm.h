@@ -100,15 +100,20 @@ typedef enum tg_path {
  * TG_ERR_UNSUPPORTED. */
 typedef struct tg_options {
     int32_t path;         /* tg_path */
-    int32_t splits;       /* number of K splits (>= 1) */
-    int32_t block_n;      /* output tile width: 64, 128 or 256 */
+    int32_t splits;       /* number of K splits (>= 1); the small-M kernel splits K
+                             over a cluster of 1, 2, 4 or 8 CTAs */
+    int32_t block_n;      /* output tile width: 128, 192, 224 or 256 for the tile
+                             kernels, 128, 256 or 512 for the small-M kernel */
     int32_t group_m;      /* grouped raster height in tiles (default 8) */
     int32_t max_ctas;     /* cap on the persistent grid (default: one per SM) */
     int32_t timeout_ms;   /* bound on every device-side wait (default 2000) */
     int32_t tail_splits;  /* split each tile of a short last wave over this many K
                              ranges (2..8; partials summed in the kernel); 0 = no */
-    int32_t multicast;    /* CTA pairs only: 2 = clusters of two pairs that share A
-                             tiles by TMA multicast, 1 = no sharing, 0 = planner */
+    int32_t multicast;    /* 2 = two neighbouring tiles share their A tile by TMA
+                             multicast: clusters of two CTA pairs (192-, 224- or
+                             256-wide tiles), of two single CTAs (128 or 256), or
+                             in the small-M kernel two column tiles (K split over
+                             at most 4); 1 = no sharing; 0 = planner */
     int32_t f32_mode;     /* FP32 operands only (tg_f32_mode): TG_F32_TF32 (0) or
                              TG_F32_3XTF32 (1) */
     int32_t reserved;     /* must be 0 */
@@ -142,7 +147,7 @@ typedef struct tg_plan {
     int32_t stages;        /* shared-memory ring depth */
     int32_t splits;        /* K splits (1 = none) */
     int32_t group_m;
-    int32_t ctas;          /* persistent grid size */
+    int32_t ctas;          /* grid size (persistent for the tile kernels) */
     int32_t pack_a;        /* 1 if A is first copied to an aligned workspace */
     int32_t pack_b;        /* 1 if B is first copied to an aligned workspace,
                               2 if B is first transposed into it (TF32 operands),
@@ -150,11 +155,12 @@ typedef struct tg_plan {
                               pack_a is then 3 as well) */
     int32_t c_vector;      /* 1 if C gets 16-byte vector stores */
     int32_t kernels;       /* kernel launches per call */
-    int64_t tiles;         /* output tiles */
+    int64_t tiles;         /* work units: output tiles, or groups of `multicast`
+                              neighbouring tiles; over all products of a batch */
     int64_t workspace_bytes;
     int32_t tail_tiles;    /* last tiles split over K to balance the last wave */
     int32_t tail_splits;   /* K ranges per tail tile (partials summed in-kernel) */
-    int32_t multicast;     /* tiles per cluster sharing A (1 or 2) */
+    int32_t multicast;     /* tiles sharing one A tile (1 or 2) */
     int32_t per_batch;     /* strided batches only: 1 if each product of the batch
                               is run as its own call (kernels counts them all), 0
                               if one launch covers every product */
