@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 7
+#define TG_ABI_VERSION 8
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -327,6 +327,43 @@ tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
                                   void *c, int64_t ldc, int64_t stride_c,
                                   tg_dtype dtype_in, tg_dtype dtype_out,
                                   void *stream, const tg_options *opt);
+
+/*
+ * tg_gemm_strided_batched_fused -- tg_gemm_strided_batched with the epilogue
+ * of tg_gemm_fused applied to every product:
+ *
+ *     C_z[m,n] = act(alpha * scale[n] * (A_z B_z)[m,n] + bias[n]) + beta * R_z[m,n]
+ *     R_z = residual + z*stride_r
+ *
+ * The batched product and the fused epilogue together: the batch axis of the
+ * tiled multiply ("Triton tiled matmul", llm-systems-cookbook, "Exercises")
+ * with the output-tile work that "Matrix Multiplication" (teenygrad docs)
+ * hands on to its chapter "Fusing an Epilogue".
+ *
+ *   batch .. stride_c, dtype_in, dtype_out, stream, opt
+ *              as for tg_gemm_strided_batched
+ *   epilogue   NULL: exactly tg_gemm_strided_batched (stride_r must be 0).
+ *              alpha, beta, activation and the per-column scale / bias are
+ *              shared by every product; rules as for tg_gemm_fused.
+ *   stride_r   elements between consecutive products' residual blocks (>= 0;
+ *              0 reads one residual block for every product; must be 0
+ *              without a residual).  The residuals of all products may be C
+ *              itself (residual == c, ldr == ldc, stride_r == stride_c: each
+ *              product's C is its own residual) but must not otherwise
+ *              overlap the whole of C -> else TG_ERR_INVALID_VALUE.
+ *
+ * One launch covers every product under the conditions of
+ * tg_gemm_strided_batched; otherwise each product is one tg_gemm_fused call
+ * on `stream`, in order of z.  K == 0 writes each product's epilogue of the
+ * empty sum.
+ */
+tg_status tg_gemm_strided_batched_fused(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                        const void *a, int64_t lda, int64_t stride_a,
+                                        const void *b, int64_t ldb, int64_t stride_b,
+                                        void *c, int64_t ldc, int64_t stride_c,
+                                        tg_dtype dtype_in, tg_dtype dtype_out,
+                                        const tg_epilogue *epilogue, int64_t stride_r,
+                                        void *stream, const tg_options *opt);
 
 /*
  * tg_plan_gemm_strided_batched -- host only, like tg_plan_gemm: validates as

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert tg.tg_abi_version() == 7
+    assert tg.tg_abi_version() == 8
     assert tg.tg_status_string(tg.TG_OK) == "TG_OK"
     assert tg.tg_status_string(tg.TG_ERR_TIMEOUT) == "TG_ERR_TIMEOUT"
     assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"

@@ -60,3 +60,53 @@ def test_struct_layout_matches_header():
     import ctypes
     assert ctypes.sizeof(tg.tg_epilogue) == 48
     assert tg.tg_epilogue.ldr.offset == 32 and tg.tg_epilogue.activation.offset == 40
+
+
+# ---- tg_gemm_strided_batched_fused: the same rules over a batch of products ----
+
+BATCH = 3
+SC = M * N            # stacked C blocks
+
+
+def bcall(ep, sr=0, c=C, sc=SC, batch=BATCH):
+    return tg.tg_gemm_strided_batched_fused(batch, M, N, K, A, K, M * K, B, N, K * N, c, N, sc,
+                                            "f16", "f16", ep, sr, 0)
+
+
+@pytest.mark.parametrize("kw,sr", [
+    (dict(residual=C + (BATCH - 1) * SC * 2, ldr=N), SC),   # inside the last product's C
+    (dict(residual=C - SC * 2, ldr=N), SC // 2),             # runs into the first C block
+    (dict(residual=C, ldr=N), SC // 2),                       # same base, other batch stride
+    (dict(residual=C, ldr=N), 0),                             # one shared residual that is C
+    (dict(residual=0x300000000, ldr=N), -1),                  # negative stride
+    (dict(), SC),                                             # stride without a residual
+    (dict(bias=C + (BATCH - 1) * SC * 2 + 64), 0),            # bias inside the last C block
+])
+def test_batched_rejected(kw, sr):
+    assert bcall(tg.make_epilogue(**kw), sr) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_batched_stride_without_epilogue():
+    assert bcall(None, sr=SC) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_batched_accepted_without_device():
+    # batch == 0 and M == 0 are decided on the host; in place and a shared
+    # residual block pass validation
+    ep = tg.make_epilogue(residual=C, ldr=N, beta=1.0)
+    assert bcall(ep, sr=SC, batch=0) == tg.TG_OK
+    assert tg.tg_gemm_strided_batched_fused(BATCH, 0, N, K, A, K, M * K, B, N, K * N, C, N, SC,
+                                            "f16", "f16", ep, SC, 0) == tg.TG_OK
+    shared = tg.make_epilogue(residual=0x300000000, ldr=N, beta=0.5)
+    assert tg.tg_gemm_strided_batched_fused(BATCH, 0, N, K, A, K, M * K, B, N, K * N, C, N, SC,
+                                            "f16", "f16", shared, 0, 0) == tg.TG_OK
+
+
+def test_batched_product_rules_still_apply():
+    ep = tg.make_epilogue()
+    # C blocks of the products overlap
+    assert bcall(ep, sc=N) == tg.TG_ERR_INVALID_VALUE
+    # K split across kernels is not available with a batch
+    opt = tg.make_options(splits=2, path=tg.TG_PATH_TC)
+    assert tg.tg_gemm_strided_batched_fused(BATCH, M, N, K, A, K, M * K, B, N, K * N, C, N, SC,
+                                            "f16", "f16", ep, 0, 0, opt) == tg.TG_ERR_UNSUPPORTED

@@ -24,14 +24,14 @@ from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_E4M3, TG_E5M2, TG
                    load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
                    ACT_CODES, TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU,
                    make_epilogue, tg_epilogue, tg_gemm_fused, tg_gemm_host,
-                   tg_selftest_timeout,
+                   tg_selftest_timeout, tg_gemm_strided_batched_fused,
                    tg_gemm_splitk_noalloc, tg_gemm_strided_batched, tg_last_device_error,
                    tg_options, tg_plan, tg_plan_gemm, tg_plan_gemm_strided_batched,
                    tg_status_string)
 
 __all__ = [
-    "gemm", "gemm_fused", "bmm", "plan", "plan_batched", "check_device_error",
-    "tg_gemm_fused", "tg_gemm_host", "tg_selftest_timeout", "tg_epilogue", "make_epilogue", "ACT_CODES", "TG_ACT_NONE", "TG_ACT_RELU",
+    "gemm", "gemm_fused", "bmm", "bmm_fused", "plan", "plan_batched", "check_device_error",
+    "tg_gemm_fused", "tg_gemm_strided_batched_fused", "tg_gemm_host", "tg_selftest_timeout", "tg_epilogue", "make_epilogue", "ACT_CODES", "TG_ACT_NONE", "TG_ACT_RELU",
     "TG_ACT_SILU", "TG_ACT_GELU_TANH", "dtype_code", "TgError", "load", "make_options",
     "tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string", "tg_last_device_error",
     "tg_abi_version", "tg_gemm_splitk_noalloc", "tg_gemm_strided_batched",
@@ -158,15 +158,8 @@ def _batch_stride(t, dims: int) -> int:
     return 0 if t.dim() == dims - 1 else (t.stride(0) if t.shape[0] > 1 else 0)
 
 
-def bmm(a, b, out_dtype=None, out=None, stream=None, **options):
-    """C[z] = A[z] @ B[z] through ``tg_gemm_strided_batched``.
-
-    ``a`` is [B, M, K] or a shared [M, K]; ``b`` is [B, K, N] or a shared
-    [K, N] (at least one of them 3-D), same dtype, unit column stride.  The
-    result is a new [B, M, N] tensor of ``out_dtype`` (default: the input
-    dtype), or ``out`` with unit column stride.  Raises ``ValueError`` on a
-    shape mismatch and ``TgError`` on any status other than TG_OK.
-    """
+def _bmm_args(a, b, out_dtype, out):
+    """Shapes, pitches and batch strides of C[z] = A[z] @ B[z] (see ``bmm``)."""
     import torch
     if a.dim() not in (2, 3) or b.dim() not in (2, 3) or (a.dim() == 2 and b.dim() == 2):
         raise ValueError("bmm expects [B, M, K] or [M, K] times [B, K, N] or [K, N]")
@@ -193,14 +186,68 @@ def bmm(a, b, out_dtype=None, out=None, stream=None, **options):
     ldb = b.stride(-2) if K > 1 else max(N, 1)
     ldc = out.stride(-2) if M > 1 else max(N, 1)
     sc = out.stride(0) if batch > 1 else (M - 1) * ldc + N
+    return (batch, M, N, K, lda, _batch_stride(a, 3), ldb, _batch_stride(b, 3), ldc, sc,
+            out_dtype, out)
+
+
+def bmm(a, b, out_dtype=None, out=None, stream=None, **options):
+    """C[z] = A[z] @ B[z] through ``tg_gemm_strided_batched``.
+
+    ``a`` is [B, M, K] or a shared [M, K]; ``b`` is [B, K, N] or a shared
+    [K, N] (at least one of them 3-D), same dtype, unit column stride.  The
+    result is a new [B, M, N] tensor of ``out_dtype`` (default: the input
+    dtype), or ``out`` with unit column stride.  Raises ``ValueError`` on a
+    shape mismatch and ``TgError`` on any status other than TG_OK.
+    """
+    import torch
+    batch, M, N, K, lda, sa, ldb, sb, ldc, sc, out_dtype, out = _bmm_args(a, b, out_dtype, out)
     opt = make_options(**options) if options else None
     with torch.cuda.device(a.device):
-        st = tg_gemm_strided_batched(batch, M, N, K, a.data_ptr(), lda, _batch_stride(a, 3),
-                                     b.data_ptr(), ldb, _batch_stride(b, 3), out.data_ptr(), ldc,
-                                     sc, dtype_code(a.dtype), dtype_code(out_dtype),
-                                     _stream_handle(stream), opt)
+        st = tg_gemm_strided_batched(batch, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(), ldb, sb,
+                                     out.data_ptr(), ldc, sc, dtype_code(a.dtype),
+                                     dtype_code(out_dtype), _stream_handle(stream), opt)
     if st != TG_OK:
         raise TgError(st, f"tg_gemm_strided_batched(batch={batch}, M={M}, N={N}, K={K})")
+    return out
+
+
+def bmm_fused(a, b, out_dtype=None, out=None, stream=None, alpha=1.0, scale=None, bias=None,
+              activation="none", beta=0.0, residual=None, **options):
+    """C[z] = act(alpha * scale * (A[z] @ B[z]) + bias) + beta * residual[z],
+    through ``tg_gemm_strided_batched_fused``.
+
+    Operands as for ``bmm``; ``scale`` / ``bias`` as for ``gemm_fused`` (shared
+    by every product); ``residual`` a [B, M, N] tensor (one block per product,
+    possibly ``out`` itself) or a shared [M, N] one, of ``out_dtype`` with unit
+    column stride.
+    """
+    import torch
+    batch, M, N, K, lda, sa, ldb, sb, ldc, sc, out_dtype, out = _bmm_args(a, b, out_dtype, out)
+    for name, v in (("scale", scale), ("bias", bias)):
+        if v is not None and (v.dtype != torch.float32 or v.shape != (N,) or not v.is_cuda
+                              or (v.stride(0) != 1 and N > 1)):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA vector of length N")
+    ldr, sr = 0, 0
+    if residual is not None:
+        if (residual.shape not in ((batch, M, N), (M, N)) or residual.dtype != out_dtype
+                or not residual.is_cuda or (residual.stride(-1) != 1 and N > 1)):
+            raise ValueError("residual must be [B, M, N] or [M, N] of out_dtype with unit "
+                             "column stride")
+        ldr = residual.stride(-2) if M > 1 else max(N, 1)
+        sr = _batch_stride(residual, 3)
+    ep = make_epilogue(alpha=alpha, beta=beta,
+                       scale=scale.data_ptr() if scale is not None else 0,
+                       bias=bias.data_ptr() if bias is not None else 0,
+                       residual=residual.data_ptr() if residual is not None else 0, ldr=ldr,
+                       activation=activation)
+    opt = make_options(**options) if options else None
+    with torch.cuda.device(a.device):
+        st = tg_gemm_strided_batched_fused(batch, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(),
+                                           ldb, sb, out.data_ptr(), ldc, sc, dtype_code(a.dtype),
+                                           dtype_code(out_dtype), ep, sr,
+                                           _stream_handle(stream), opt)
+    if st != TG_OK:
+        raise TgError(st, f"tg_gemm_strided_batched_fused(batch={batch}, M={M}, N={N}, K={K})")
     return out
 
 

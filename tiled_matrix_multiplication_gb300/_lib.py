@@ -31,7 +31,7 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
            "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
            "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused",
-           "tg_gemm_host", "tg_selftest_timeout")
+           "tg_gemm_host", "tg_selftest_timeout", "tg_gemm_strided_batched_fused")
 
 TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_ACT_GELU_TANH = 0, 1, 2, 3
 ACT_CODES = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "silu": TG_ACT_SILU,
@@ -121,6 +121,9 @@ def load(path: str | None = None):
         lib.tg_gemm_fused.argtypes = gemm_args[:-1] + [ctypes.POINTER(tg_epilogue), vp,
                                                         ctypes.POINTER(tg_options)]
         lib.tg_gemm_fused.restype = ctypes.c_int
+        lib.tg_gemm_strided_batched_fused.argtypes = batched + [ctypes.POINTER(tg_epilogue), i64,
+                                                                vp, ctypes.POINTER(tg_options)]
+        lib.tg_gemm_strided_batched_fused.restype = ctypes.c_int
         lib.tg_gemm_host.argtypes = gemm_args + [ctypes.POINTER(tg_options)]
         lib.tg_gemm_host.restype = ctypes.c_int
         lib.tg_selftest_timeout.argtypes = [i32, vp]
@@ -237,6 +240,18 @@ def tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, epilogue
     opt = ctypes.byref(options) if options is not None else None
     return int(load().tg_gemm_fused(M, N, K, a, lda, b, ldb, c, ldc, _code(dtype_in),
                                     _code(dtype_out), ep, stream, opt))
+
+
+def tg_gemm_strided_batched_fused(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc,
+                                  stride_c, dtype_in, dtype_out, epilogue, stride_r, stream,
+                                  options=None) -> int:
+    """The batched product with the fused epilogue on every product; residual
+    blocks ``stride_r`` elements apart (0 = one shared).  Returns the tg_status."""
+    ep = ctypes.byref(epilogue) if epilogue is not None else None
+    opt = ctypes.byref(options) if options is not None else None
+    return int(load().tg_gemm_strided_batched_fused(batch, M, N, K, a, lda, stride_a, b, ldb,
+                                                    stride_b, c, ldc, stride_c, _code(dtype_in),
+                                                    _code(dtype_out), ep, stride_r, stream, opt))
 
 
 def tg_gemm_host(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream,

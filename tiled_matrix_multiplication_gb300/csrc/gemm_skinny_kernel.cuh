@@ -88,7 +88,7 @@ struct SkCfg {
 __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float v) {
     const int64_t off = static_cast<int64_t>(blockIdx.y) * p.stride_c +   // batch
                         static_cast<int64_t>(m) * p.ldc + n;
-    if (p.epi.on) v = epi_one(p.epi, p.out_kind, m, n, v);
+    if (p.epi.on) v = epi_one(p.epi, p.out_kind, m, n, v, static_cast<int>(blockIdx.y));
     if (p.out_kind == OUT_F32)
         static_cast<float *>(p.c)[off] = v;
     else if (p.out_kind == OUT_F16)

@@ -205,7 +205,7 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
         }
         return;
     }
-    if (p.epi.on) epi_chunk32(p.epi, p.out_kind, row, col, ncols, r);
+    if (p.epi.on) epi_chunk32(p.epi, p.out_kind, row, col, ncols, r, z);
     const int64_t off = static_cast<int64_t>(z) * p.stride_c + static_cast<int64_t>(row) * p.ldc + col;
     if (p.out_kind == OUT_F32) {
         float *dst = static_cast<float *>(p.c) + off;

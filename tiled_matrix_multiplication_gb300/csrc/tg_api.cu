@@ -363,6 +363,48 @@ tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
     return TG_OK;
 }
 
+tg_status tg_gemm_strided_batched_fused(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                        const void *a, int64_t lda, int64_t stride_a,
+                                        const void *b, int64_t ldb, int64_t stride_b, void *c,
+                                        int64_t ldc, int64_t stride_c, tg_dtype dtype_in,
+                                        tg_dtype dtype_out, const tg_epilogue *epilogue,
+                                        int64_t stride_r, void *stream, const tg_options *opt) {
+    tg_status st = validate_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc,
+                                    stride_c, dtype_in, dtype_out, opt);
+    if (st != TG_OK) return st;
+    if (epilogue == nullptr && stride_r != 0) return TG_ERR_INVALID_VALUE;
+    tg::EpiParams e;
+    st = validate_epilogue(M, N, c, ldc, dtype_out, epilogue, &e, batch, stride_c, stride_r);
+    if (st != TG_OK) return st;
+    if (epilogue == nullptr)
+        return tg_gemm_strided_batched(batch, M, N, K, a, lda, stride_a, b, ldb, stride_b, c, ldc,
+                                       stride_c, dtype_in, dtype_out, stream, opt);
+    if (batch == 0 || M == 0 || N == 0) return TG_OK;
+    const int ei = esize_of(dtype_in), eo = esize_of(dtype_out);
+    if (K > 0 && batch > 1 && batch_in_one_launch(dtype_in, a, lda, stride_a, b, ldb, stride_b)) {
+        DeviceState *dev = nullptr;
+        st = device_state(&dev);
+        if (st != TG_OK) return st;
+        bool map_failed = false;
+        st = enqueue(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out,
+                     static_cast<cudaStream_t>(stream), opt, dev,
+                     Batch{batch, stride_a, stride_b, stride_c}, &map_failed, &e);
+        if (!map_failed) return st;
+    }
+    // one fused call per product, in order of z, each with its own residual
+    tg_epilogue one = *epilogue;
+    for (int64_t z = 0; z < batch; ++z) {
+        if (epilogue->residual)
+            one.residual = static_cast<const uint8_t *>(epilogue->residual) + z * stride_r * eo;
+        st = tg_gemm_fused(M, N, K, static_cast<const uint8_t *>(a) + z * stride_a * ei, lda,
+                           static_cast<const uint8_t *>(b) + z * stride_b * ei, ldb,
+                           static_cast<uint8_t *>(c) + z * stride_c * eo, ldc, dtype_in,
+                           dtype_out, &one, stream, opt);
+        if (st != TG_OK) return st;
+    }
+    return TG_OK;
+}
+
 tg_status tg_selftest_timeout(int32_t timeout_ms, void *stream) {
     if (timeout_ms < 1 || timeout_ms > 10000) return TG_ERR_INVALID_VALUE;
     DeviceState *dev = nullptr;

@@ -40,13 +40,13 @@ __device__ __forceinline__ float epi_load_res(const EpiParams &e, int out_kind, 
     return __bfloat162float(static_cast<const __nv_bfloat16 *>(e.res)[off]);
 }
 
-// One element (m, n); acc is the FP32 accumulator value.
+// One element (m, n) of batch product z; acc is the FP32 accumulator value.
 __device__ __forceinline__ float epi_one(const EpiParams &e, int out_kind, int64_t m, int64_t n,
-                                         float acc) {
+                                         float acc, int z = 0) {
     const float s = e.scale ? e.scale[n] : 1.f;
     const float b = e.bias ? e.bias[n] : 0.f;
     float v = epi_act(e.act, fmaf(acc * e.alpha, s, b));
-    if (e.res) v = fmaf(e.beta, epi_load_res(e, out_kind, m * e.ldr + n), v);
+    if (e.res) v = fmaf(e.beta, epi_load_res(e, out_kind, z * e.stride_r + m * e.ldr + n), v);
     return v;
 }
 
@@ -54,7 +54,7 @@ __device__ __forceinline__ float epi_one(const EpiParams &e, int out_kind, int64
 // FP32 bit patterns r[].  The residual is read before C is written, by the
 // thread that writes it, so R may be C itself.
 __device__ __forceinline__ void epi_chunk32(const EpiParams &e, int out_kind, int row, int col,
-                                            int ncols, uint32_t (&r)[32]) {
+                                            int ncols, uint32_t (&r)[32], int z = 0) {
     float sc[32], bi[32], res[32];
     const bool full = ncols == 32;
     if (full && e.sb_vector) {
@@ -75,7 +75,7 @@ __device__ __forceinline__ void epi_chunk32(const EpiParams &e, int out_kind, in
         }
     }
     if (e.res) {
-        const int64_t off = static_cast<int64_t>(row) * e.ldr + col;
+        const int64_t off = z * e.stride_r + static_cast<int64_t>(row) * e.ldr + col;
         if (full && e.res_vector && out_kind != OUT_F32) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 static_cast<const uint16_t *>(e.res) + off);

@@ -123,7 +123,8 @@ tg_status validate_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const
 bool batch_in_one_launch(tg_dtype din, const void *a, int64_t lda, int64_t sa, const void *b,
                          int64_t ldb, int64_t sb);
 tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg_dtype dout,
-                            const tg_epilogue *ep, tg::EpiParams *e);
+                            const tg_epilogue *ep, tg::EpiParams *e, int64_t batch = 1,
+                            int64_t sc = 0, int64_t sr = 0);
 
 // tg_api.cu
 tg_status device_state(DeviceState **out);

@@ -33,6 +33,7 @@ struct EpiParams {
     const float *bias;          // [N] or null (0)
     const void *res;            // [M][ldr] in the output type, or null
     int64_t ldr;                // elements
+    int64_t stride_r;           // elements between the residuals of batch products
     int32_t res_vector;         // res base and pitch allow 16-byte loads
     int32_t sb_vector;          // scale and bias allow 16-byte loads
 };

@@ -395,13 +395,17 @@ bool batch_in_one_launch(tg_dtype din, const void *a, int64_t lda, int64_t sa, c
 }
 
 // Argument rules of the fused epilogue (on top of those of the product);
-// fills *e for the kernels.
+// fills *e for the kernels.  With `batch` > 1 the products' C blocks start
+// `sc` elements apart and their residuals `sr` apart (0: one residual block
+// read by every product); scale and bias are shared.
 tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg_dtype dout,
-                            const tg_epilogue *ep, tg::EpiParams *e) {
+                            const tg_epilogue *ep, tg::EpiParams *e, int64_t batch, int64_t sc,
+                            int64_t sr) {
     std::memset(e, 0, sizeof(*e));
     if (ep == nullptr) return TG_OK;
     if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_GELU_TANH || ep->reserved != 0)
         return TG_ERR_INVALID_VALUE;
+    if (sr < 0 || (sr != 0 && ep->residual == nullptr)) return TG_ERR_INVALID_VALUE;
     const int eo = esize_of(dout);
     e->on = 1;
     e->act = ep->activation;
@@ -411,9 +415,13 @@ tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg
     e->bias = ep->bias;
     e->res = ep->residual;
     e->ldr = ep->residual ? ep->ldr : 0;
-    if (M == 0 || N == 0) return TG_OK;
-    uintptr_t c0, c1;
-    span(c, M, N, ldc, eo, &c0, &c1);
+    e->stride_r = batch > 1 ? sr : 0;
+    if (M == 0 || N == 0 || batch == 0) return TG_OK;
+    const int64_t last = batch > 1 ? batch - 1 : 0;   // index of the last product
+    if (sr > 0 && last > (int64_t(1) << 46) / sr) return TG_ERR_UNSUPPORTED;
+    // bytes spanned by every product's C block
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(c);
+    const uintptr_t c1 = c0 + static_cast<uintptr_t>((last * sc + (M - 1) * ldc + N) * eo);
     for (const float *v : {ep->scale, ep->bias}) {
         if (v == nullptr) continue;
         if (reinterpret_cast<uintptr_t>(v) % 4) return TG_ERR_INVALID_VALUE;
@@ -423,11 +431,14 @@ tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg
     if (ep->residual) {
         if (ep->ldr < N || ep->ldr > (int64_t(1) << 36)) return TG_ERR_INVALID_VALUE;
         if (reinterpret_cast<uintptr_t>(ep->residual) % eo) return TG_ERR_INVALID_VALUE;
-        const bool in_place = ep->residual == c && ep->ldr == ldc;
-        uintptr_t r0, r1;
-        span(ep->residual, M, N, ep->ldr, eo, &r0, &r1);
+        // in place: every product reads its own C block as the residual
+        const bool in_place = ep->residual == c && ep->ldr == ldc && (last == 0 || sr == sc);
+        const uintptr_t r0 = reinterpret_cast<uintptr_t>(ep->residual);
+        const uintptr_t r1 =
+            r0 + static_cast<uintptr_t>((last * sr + (M - 1) * ep->ldr + N) * eo);
         if (!in_place && overlaps(c0, c1, r0, r1)) return TG_ERR_INVALID_VALUE;
-        e->res_vector = aligned16(ep->residual) && (ep->ldr * eo) % 16 == 0;
+        e->res_vector = aligned16(ep->residual) && (ep->ldr * eo) % 16 == 0 &&
+                        (last == 0 || (sr * eo) % 16 == 0);
     }
     e->sb_vector = (!ep->scale || aligned16(ep->scale)) && (!ep->bias || aligned16(ep->bias));
     return TG_OK;
