@@ -273,13 +273,17 @@ def test_options_that_exclude_every_variant(lib, opts):
 
 @pytest.mark.parametrize("M,din", [(65, "f16"), (128, "f16"), (128, "bf16"), (33, "e4m3"),
                                    (128, "e4m3")])
-def test_plan_mid_m_uses_single_cta_tiles(lib, M, din):
-    # 65..128 rows (33..128 for FP8): 128-wide single-CTA tiles with a K split
+def test_plan_small_m_up_to_128_rows(lib, M, din):
+    # up to 128 rows, 16-bit and FP8 alike: the transposed streaming kernel,
+    # 128 columns per CTA, a cluster K split summed on chip
     st, p = plan(M, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148)
-    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC
-    assert p["block_m"] == 128 and p["block_n"] == 128 and p["multicast"] == 1
-    assert p["splits"] >= 2
-    # the small-M kernel can still be forced up to 128 rows
-    st, p = plan(M, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148,
-                 path=tg.TG_PATH_SKINNY)
     assert st == tg.TG_OK and p["path"] == tg.TG_PATH_SKINNY
+    assert p["block_n"] == 128 and p["splits"] >= 2 and p["workspace_bytes"] == 0
+    assert p["block_m"] == (64 if M <= 64 else 128)
+    # the tile kernel can still be forced
+    st, p = plan(M, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148,
+                 path=tg.TG_PATH_TC)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC
+    # 129 rows: no longer the small-M kernel
+    st, p = plan(129, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148)
+    assert st == tg.TG_OK and p["path"] != tg.TG_PATH_SKINNY

@@ -23,17 +23,20 @@
 //
 // Work split: one CTA per (NT-column tile, K range).  The S CTAs that share a
 // column tile form a thread-block cluster (S = 1, 2, 4 or 8, cluster rank =
-// K range).  After its main loop each CTA parks its FP32 partial tile in its
-// own shared memory; after a cluster barrier, CTA r sums columns
-// [r*NT/S, (r+1)*NT/S) of the tile over all S partials, read in rank order
-// from the peers' shared memory (distributed shared memory), rounds once and
-// writes C.  No partials go to global memory and no second kernel runs; the
-// sum order is fixed, so results do not depend on timing.
+// K range).  After its main loop, and a cluster barrier, each CTA pushes the
+// FP32 partial of every column straight from tensor memory to the CTA that
+// owns the column -- CTA r owns columns [r*NT/S, (r+1)*NT/S) -- with
+// asynchronous remote stores (st.async) into the owner's idle ring; the owner
+// waits on one mbarrier for all the bytes, sums the S partials in K-range
+// order, rounds once and writes C.  No partials go to global memory and no
+// second kernel runs; the sum order is fixed, so results do not depend on
+// timing.  (Pulling the partials with remote loads instead cost one cluster
+// round trip per few outputs: 5 to 10 us per call at 64 to 128 rows.)
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = TMEM -> shared epilogue; all six warps then do the cluster
-// reduction.  Every mbarrier wait is bounded (status word + abort flag, as in
-// gemm_tc.cu).
+// warps 2..5 = TMEM epilogue (direct stores, or the pushes); all six warps
+// then sum the received partials.  Every mbarrier wait is bounded (status
+// word + abort flag, as in gemm_tc.cu).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -69,16 +72,21 @@ struct SkCfg {
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
     static constexpr int BUDGET = TWO ? 112 * 1024 : kSmemBudget;
     static constexpr int STAGES = BUDGET / STAGE_BYTES > 12 ? 12 : BUDGET / STAGE_BYTES;
-    static constexpr int PARTIAL_BYTES = NT * MP * 4;   // FP32 partial tile, [m][n]
+    // received K-split partials: [K range][row group of 4][column][4 rows] FP32,
+    // then the finished tile [row][column] in the output type
+    static constexpr int G4 = MP / 4;
+    static constexpr int RECV_BYTES = NT * MP * 4;
+    static constexpr int OUT_STAGE_MAX = MP * (NT / 2) * 4;   // K split >= 2, FP32 out
     static constexpr int ACC_COLS = MP < 32 ? 32 : MP;  // TMEM columns per accumulator
     static constexpr int TMEM_COLS = SUB * ACC_COLS;
-    static constexpr int NUM_BARS = 2 * STAGES + 1;
+    static constexpr int NUM_BARS = 2 * STAGES + 2;   // ring, TMEM full, partials received
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     // A operand (B^T) N-major, B operand (A^T) K-major; M = 128, N = MP.
     static constexpr uint32_t IDESC =
         make_idesc(FMT, 1u, 0u, kSubN, MP);
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte swizzle alignment");
-    static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "partial tile reuses the ring");
+    static_assert(RECV_BYTES + OUT_STAGE_MAX <= STAGES * STAGE_BYTES,
+                  "received partials and the output tile reuse the ring");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 128, "MMA N");
     static_assert(NT % kSubN == 0 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "accumulators fit one power-of-two TMEM allocation");
@@ -117,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     const uint32_t tfull_bar = bars + 8u * (2 * S);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *partial = reinterpret_cast<float *>(gbase);  // after the main loop: [MP][NT]
+    // after the main loop the ring receives the K-split partials
+    const uint32_t recv_base = base;
+    const uint32_t recv_bar = bars + 8u * (2 * S + 1);
+    bool epi_ok = true;
     __shared__ int never_abort;
 
     const int warp = threadIdx.x >> 5;
@@ -143,9 +154,14 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
             mbar_init(empty_bar(s), share);   // one MMA commit per CTA reading the stage's A^T
         }
         mbar_init(tfull_bar, 1);
+        mbar_init(recv_bar, 1);
         *abort_flag = 0;
         never_abort = 0;
         fence_mbar_init();
+        // one phase: the partials of this CTA's columns, rows rounded up to 4
+        // (peers push them after the cluster barrier that follows the main loop)
+        if (splits > 1)
+            mbar_arrive_expect_tx(recv_bar, NT * 16 * ((min(p.M, MP) + 3) / 4));
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
@@ -268,43 +284,38 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------- epilogue: TMEM -> smem
-        // Thread (quad, lane) owns column n = quad*32 + lane of the tile.
+        // ------------------------------------------- epilogue: wait for TMEM
+        // Thread (quad, lane) owns column n = quad*32 + lane of each 128-column
+        // accumulator.  Without a K split it writes C here; with one it pushes
+        // its column to the owning CTA after the cluster barrier below.
         const int quad = warp & 3;
         const bool got = mbar_wait(tfull_bar, 0, p.timeout_ns, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
+        epi_ok = __all_sync(0xffffffffu, got);
+        if (!epi_ok) {
             if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
             *abort_flag = 1;
-        } else {
+        } else if (splits == 1) {
             tc_fence_after_sync();
 #pragma unroll 1
             for (int j = 0; j < Cfg::SUB; ++j) {
-                const int nl = j * kSubN + quad * 32 + lane;   // column within the tile
-                const int n = tn * NT + nl;
+                const int n = tn * NT + j * kSubN + quad * 32 + lane;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                        j * Cfg::ACC_COLS;
                 if constexpr (MP == 16) {
                     uint32_t r[16];
                     tmem_load_16cols_sync(taddr, r);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        if (splits > 1)
-                            partial[q * NT + nl] = __uint_as_float(r[q]);
-                        else if (q < p.M && n < p.N)
-                            sk_store(p, q, n, __uint_as_float(r[q]));
-                    }
+                    for (int q = 0; q < 16; ++q)
+                        if (q < p.M && n < p.N) sk_store(p, q, n, __uint_as_float(r[q]));
                 } else {
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 32) {
                         uint32_t r[32];
                         tmem_load_32cols_sync(taddr + c0, r);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            if (splits > 1)
-                                partial[(c0 + q) * NT + nl] = __uint_as_float(r[q]);
-                            else if (c0 + q < p.M && n < p.N)
+                        for (int q = 0; q < 32; ++q)
+                            if (c0 + q < p.M && n < p.N)
                                 sk_store(p, c0 + q, n, __uint_as_float(r[q]));
-                        }
                     }
                 }
             }
@@ -314,22 +325,157 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     tc_fence_before_sync();
     __syncthreads();
     if (splits > 1) {
-        // --------------------------- cluster reduction over distributed smem
-        cluster_sync_all();                       // every CTA's partial is in place
-        const int cols = NT / splits;             // columns reduced by this CTA
-        const int rows = min(p.M, MP);
-        const uint32_t part_addr = smem_addr(partial);
-        for (int i = threadIdx.x; i < rows * cols; i += kThreads) {
-            const int m = i / cols;
-            const int nl = split * cols + (i - m * cols);
-            const int n = tn * NT + nl;
-            const uint32_t off = part_addr + static_cast<uint32_t>((m * NT + nl) * 4);
-            float acc = 0.f;
-            for (int s = 0; s < splits; ++s)
-                acc += ld_shared_cluster_f32(map_to_cta(off, jn * splits + s));
-            if (n < p.N) sk_store(p, m, n, acc);
+        // ------------------------ K-split reduction through distributed smem
+        // CTA r of the K ranges owns columns [r*cols, (r+1)*cols) of the tile.
+        // Each CTA pushes every column's FP32 partial to its owner with
+        // asynchronous remote stores into the owner's (now idle) ring; the
+        // owner waits on one barrier for all the bytes, sums the S partials in
+        // K-range order and writes C.
+        cluster_sync_all();   // every ring of the cluster is idle from here on
+        const int cols = NT / splits;
+        const int push_groups = (min(p.M, MP) + 3) / 4;   // groups of 4 rows
+        if (warp >= 2 && warp < 6 && epi_ok) {
+            const int quad = warp & 3;
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int j = 0; j < Cfg::SUB; ++j) {
+                const int nl = j * kSubN + quad * 32 + lane;   // column within the tile
+                const int owner = nl / cols;
+                const int c = nl - owner * cols;
+                const uint32_t rank = static_cast<uint32_t>(jn * splits + owner);
+                // lanes hold consecutive columns: each push of a warp fills one
+                // contiguous run of 16-byte (4-row) cells at the owner
+                const uint32_t dst = map_to_cta(
+                    recv_base + static_cast<uint32_t>((split * Cfg::G4 * cols + c) * 16), rank);
+                const uint32_t gstep = static_cast<uint32_t>(cols * 16);   // next row group
+                const uint32_t rbar = map_to_cta(recv_bar, rank);
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       j * Cfg::ACC_COLS;
+                // only the groups of 4 rows that hold rows < M are sent
+                if constexpr (MP == 16) {
+                    uint32_t r[16];
+                    tmem_load_16cols_sync(taddr, r);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        if (g < push_groups)
+                            st_async_v4(dst + gstep * g, r[4 * g], r[4 * g + 1], r[4 * g + 2],
+                                        r[4 * g + 3], rbar);
+                } else {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 4 * push_groups; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_load_32cols_sync(taddr + c0, r);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            if (c0 / 4 + g < push_groups)
+                                st_async_v4(dst + gstep * (c0 / 4 + g), r[4 * g], r[4 * g + 1],
+                                            r[4 * g + 2], r[4 * g + 3], rbar);
+                    }
+                }
+            }
         }
-        cluster_sync_all();                       // peers are done reading this CTA's smem
+        const bool got = mbar_wait<true>(recv_bar, 0, p.timeout_ns, abort_flag);
+        if (!got && !*abort_flag) {
+            record_failure(p.status, 6, (ROLE_DRAIN << 16) | 4);
+            *abort_flag = 1;
+        }
+        // Every push to this CTA has landed and its own pushes are issued: tell
+        // the cluster, and wait for the others only before leaving (no CTA may
+        // leave while a peer can still push to it).  Nothing is published
+        // through this barrier -- the pushes are ordered by the receivers'
+        // mbarriers -- so the arrive is relaxed and need not wait for them.
+        tc_fence_before_sync();
+        cluster_arrive_relaxed();
+        // Sum the S partials of each (row group, column) cell in K-range order,
+        // apply the epilogue, round, and stage the cells [row group][column][4
+        // rows] behind the received partials ...
+        const int eo = p.out_kind == OUT_F32 ? 4 : 2;
+        uint8_t *out_tile = gbase + Cfg::RECV_BYTES;
+        const int n_base = tn * NT + split * cols;
+        const int z = static_cast<int>(blockIdx.y);
+        if (got) {
+            for (int i = threadIdx.x; i < push_groups * cols; i += kThreads) {
+                const int g = i / cols;
+                const int c = i - g * cols;
+                const int n = n_base + c;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int s = 0; s < splits; ++s) {
+                    const float4 v = *reinterpret_cast<const float4 *>(
+                        gbase + ((s * Cfg::G4 + g) * cols + c) * 16);
+                    acc[0] += v.x;
+                    acc[1] += v.y;
+                    acc[2] += v.z;
+                    acc[3] += v.w;
+                }
+                if (p.epi.on) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (4 * g + u < p.M && n < p.N)
+                            acc[u] = epi_one(p.epi, p.out_kind, 4 * g + u, n, acc[u], z);
+                }
+                // one store per cell: its 4 rows side by side (shared-memory
+                // stores are expensive here, one wide store beats four narrow)
+                uint8_t *cell = out_tile + (g * cols + c) * 4 * eo;
+                if (p.out_kind == OUT_F32) {
+                    *reinterpret_cast<float4 *>(cell) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                } else if (p.out_kind == OUT_F16) {
+                    const __half2 lo = __floats2half2_rn(acc[0], acc[1]);
+                    const __half2 hi = __floats2half2_rn(acc[2], acc[3]);
+                    *reinterpret_cast<uint2 *>(cell) =
+                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                   *reinterpret_cast<const uint32_t *>(&hi));
+                } else {
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
+                    *reinterpret_cast<uint2 *>(cell) =
+                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                   *reinterpret_cast<const uint32_t *>(&hi));
+                }
+            }
+        }
+        // ... then write it to C in 16-byte pieces (element by element where C
+        // is not 16-byte aligned or a piece runs past column N).
+        if (__syncthreads_and(got)) {
+            const int per = 16 / eo;                 // elements per piece
+            const int pieces = cols / per;           // per row (cols >= 16)
+            const int rows = min(p.M, MP);
+            uint8_t *cz = static_cast<uint8_t *>(p.c) + static_cast<int64_t>(z) * p.stride_c * eo;
+            for (int i = threadIdx.x; i < rows * pieces; i += kThreads) {
+                const int m = i / pieces;
+                const int c = (i - m * pieces) * per;
+                const int n = n_base + c;
+                // the piece's elements sit 4 elements apart in consecutive cells
+                const uint8_t *src = out_tile + (((m >> 2) * cols + c) * 4 + (m & 3)) * eo;
+                uint8_t *dst = cz + (static_cast<int64_t>(m) * p.ldc + n) * eo;
+                if (p.c_vector && n + per <= p.N) {
+                    uint32_t w[4];
+                    if (eo == 4) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = *reinterpret_cast<const uint32_t *>(src + e * 16);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = static_cast<uint32_t>(
+                                       *reinterpret_cast<const uint16_t *>(src + 16 * e)) |
+                                   (static_cast<uint32_t>(
+                                        *reinterpret_cast<const uint16_t *>(src + 16 * e + 8))
+                                    << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    for (int e = 0; e < per && n + e < p.N; ++e) {
+                        if (eo == 4)
+                            *reinterpret_cast<uint32_t *>(dst + e * 4) =
+                                *reinterpret_cast<const uint32_t *>(src + e * 16);
+                        else
+                            *reinterpret_cast<uint16_t *>(dst + e * 2) =
+                                *reinterpret_cast<const uint16_t *>(src + e * 8);
+                    }
+                }
+            }
+        }
+        cluster_wait();
     } else if (share > 1) {
         cluster_sync_all();   // the partner's last commits to this CTA's barriers have landed
     }

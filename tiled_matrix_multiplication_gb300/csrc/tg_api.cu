@@ -185,6 +185,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         sp.a_batched = nb_a > 1;
         sp.b_batched = nb_b > 1;
         sp.stride_c = bt.sc;
+        sp.c_vector = p.c_vector;
         if (epi) sp.epi = *epi;
         st = cuda_status(
             tg::launch_gemm_skinny(in_kind_of(dtype_in), p.block_m, p.block_n, tmA, tmB, sp, s));

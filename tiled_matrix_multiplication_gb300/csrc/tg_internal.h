@@ -85,6 +85,7 @@ struct SkParams {
     int32_t a_share;            // 2: CTAs on adjacent column tiles share A^T by multicast
     int32_t batch;              // gridDim.y; A / B rank-3 when a_batched / b_batched
     int32_t a_batched, b_batched;
+    int32_t c_vector;           // C base, row pitch and batch stride are 16-byte multiples
     int64_t stride_c;           // elements between the C of consecutive batches
     int64_t ldc;
     void *c;

@@ -200,11 +200,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // Small M with 16-bit operands: the transposed streaming kernel (one tile
     // holds all rows; work is spread over 128-column tiles and K splits).
     const bool forced_skinny = opt && opt->path == TG_PATH_SKINNY;
-    // The transposed streaming kernel wins for up to 64 rows of 16-bit operands
-    // and up to 32 of FP8 ones; beyond that (to 128 rows, where it can still
-    // be forced) the tile kernel with a K split measured faster on GB300
-    // (M = 128, N = K = 8192: FP16 35.0 vs 39.0 us, E4M3 23.7 vs 29.6 us).
-    const int64_t skinny_rows_max = forced_skinny ? 128 : (is_fp8(din) ? 32 : 64);
+    // The transposed streaming kernel wins up to 128 rows for 16-bit and FP8
+    // operands alike (GB300, N = K = 8192, M = 128: FP16 30.5 vs 35.0 us for
+    // the tile kernel with a K split, E4M3 20.8 vs 24.7 us).
+    const int64_t skinny_rows_max = 128;
     const bool skinny_ok = din != TG_F32 && M <= skinny_rows_max &&
                            (forced_skinny || !(opt && opt->block_n)) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&

@@ -136,6 +136,16 @@ __device__ __forceinline__ void cluster_sync_all() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync_all(), for work placed between them.  The
+// relaxed arrive publishes no memory: it only marks this thread's progress.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_num_ctas() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
@@ -147,6 +157,19 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// Stores four 32-bit words to shared memory of a CTA of this cluster (`addr`,
+// 16-byte aligned, from map_to_cta) and signals their 16 bytes on the
+// mbarrier `bar` of the same CTA (complete_tx): the receiver learns that the
+// data has landed by waiting on its barrier, with no round trip per store.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+        : "memory");
 }
 
 // Address of the same shared-memory offset in CTA `rank` of this cluster.
