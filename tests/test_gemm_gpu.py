@@ -156,6 +156,20 @@ def test_skinny_path_strided_uniform(M):
     assert padding_untouched(c, N, "bf16")
 
 
+@pytest.mark.parametrize("dout,ldc", [("f16", 1008), ("f32", 1004), ("bf16", 1001)])
+@pytest.mark.parametrize("M", [3, 64, 128])
+def test_skinny_split_store_pieces(M, dout, ldc):
+    """The K-split owner writes C in 16-byte pieces where C allows them: a
+    padded C whose last piece straddles column N (ldc 1008 / 1004: aligned rows,
+    the piece at N = 1001 partly outside), and an unaligned row pitch (1001:
+    element stores throughout).  Padding columns must keep their poison."""
+    N, K = 1001, 1500
+    din = "bf16" if dout == "bf16" else "f16"
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=3, splits=4, ldc=ldc)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+    assert padding_untouched(c, N, dout)
+
+
 @pytest.mark.parametrize("M", [1, 16, 64, 128])
 def test_skinny_two_ctas_per_sm_exact(M):
     """The half-ring variant (two CTAs per SM), forced by a small CTA budget."""

@@ -50,12 +50,18 @@
 namespace tg {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSmemBudget = 232448 - 1024 - 256;
+constexpr int kSmemBudget = 232448 - 1024 - 256;   // one CTA per SM (227 KB per CTA)
+constexpr int kTwoSmemPerCta = 233472 / 2 - 1024;  // two per SM (228 KB, 1 KB each reserved)
 constexpr int kSubN = 128;    // output columns per MMA (the MMA's M)
 
 // TWO: a half-size ring so that two CTAs share an SM (twice the CTAs, and
 // twice the independent TMA streams, for the same shared memory).
+// SPLIT (128 rows, two per SM): A^T tiles are as large as B^T tiles there and
+// only three (B^T, A^T) stage pairs would fit; separate rings -- 4 B^T stages
+// from HBM, 3 A^T stages (L2 hits) with a producer warp of their own -- keep
+// more of B in flight (measured 1 us faster per call at N = K = 8192).  The
+// ring then starts at the 1024-byte aligned base of the dynamic area (no
+// alignment pad; checked at run time).
 template <int IN_KIND, int MP, int NT, bool TWO>
 struct SkCfg {
     static constexpr int ESIZE = in_esize(IN_KIND);   // 2 (FP16, BF16) or 1 (FP8)
@@ -70,8 +76,17 @@ struct SkCfg {
     static constexpr int BT_STAGE = (NT / CHUNK_N) * BT_BOX;   // NT columns of B
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
-    static constexpr int BUDGET = TWO ? 112 * 1024 : kSmemBudget;
-    static constexpr int STAGES = BUDGET / STAGE_BYTES > 12 ? 12 : BUDGET / STAGE_BYTES;
+    static constexpr bool SPLIT = TWO && MP == 128;
+    static constexpr int THREADS = SPLIT ? 224 : 192;   // + the A^T producer warp
+    static constexpr int PAD = SPLIT ? 0 : 1024;        // room to align the ring
+    static constexpr int BUDGET =
+        TWO ? (SPLIT ? kTwoSmemPerCta - 512 : 112 * 1024) : kSmemBudget;
+    static constexpr int A_SPLIT = 3;                   // A^T stages when SPLIT
+    static constexpr int FIT = SPLIT ? (BUDGET - A_SPLIT * AT_STAGE) / BT_STAGE
+                                     : BUDGET / STAGE_BYTES;
+    static constexpr int STAGES = FIT > 12 ? 12 : FIT;  // B^T stages (pairs unless SPLIT)
+    static constexpr int A_STAGES = SPLIT ? A_SPLIT : STAGES;
+    static constexpr int RING_BYTES = STAGES * BT_STAGE + A_STAGES * AT_STAGE;
     // received K-split partials: [K range][row group of 4][column][4 rows] FP32,
     // then the finished tile [row][column] in the output type
     static constexpr int G4 = MP / 4;
@@ -79,14 +94,17 @@ struct SkCfg {
     static constexpr int OUT_STAGE_MAX = MP * (NT / 2) * 4;   // K split >= 2, FP32 out
     static constexpr int ACC_COLS = MP < 32 ? 32 : MP;  // TMEM columns per accumulator
     static constexpr int TMEM_COLS = SUB * ACC_COLS;
-    static constexpr int NUM_BARS = 2 * STAGES + 2;   // ring, TMEM full, partials received
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+    // ring(s), TMEM full, partials received
+    static constexpr int NUM_BARS = 2 * STAGES + (SPLIT ? 2 * A_STAGES : 0) + 2;
+    static constexpr int SMEM_BYTES = PAD + RING_BYTES + NUM_BARS * 8 + 16;
     // A operand (B^T) N-major, B operand (A^T) K-major; M = 128, N = MP.
     static constexpr uint32_t IDESC =
         make_idesc(FMT, 1u, 0u, kSubN, MP);
-    static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte swizzle alignment");
-    static_assert(RECV_BYTES + OUT_STAGE_MAX <= STAGES * STAGE_BYTES,
+    static_assert(BT_STAGE % 1024 == 0 && AT_STAGE % 1024 == 0,
+                  "stages keep 1024-byte swizzle alignment");
+    static_assert(RECV_BYTES + OUT_STAGE_MAX <= RING_BYTES,
                   "received partials and the output tile reuse the ring");
+    static_assert(!TWO || SMEM_BYTES <= kTwoSmemPerCta, "two CTAs per SM");
     static_assert(MP % 16 == 0 && MP >= 16 && MP <= 128, "MMA N");
     static_assert(NT % kSubN == 0 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "accumulators fit one power-of-two TMEM allocation");
@@ -106,30 +124,45 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int m, int n, float 
 }
 
 template <int IN_KIND, int MP, int NT, bool TWO>
-__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
+__global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 : 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const SkParams p) {
     using Cfg = SkCfg<IN_KIND, MP, NT, TWO>;
-    constexpr int S = Cfg::STAGES;
+    constexpr int S = Cfg::STAGES;      // B^T stages
+    constexpr int SA = Cfg::A_STAGES;   // A^T stages (== S unless SPLIT)
+    constexpr bool SPLIT = Cfg::SPLIT;
+    constexpr int kThreads = Cfg::THREADS;
 
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
+    if (SPLIT && base != raw) {
+        // no pad was reserved: the declared alignment must hold.  Every CTA of
+        // the launch sees the same layout, so all of them (whole clusters)
+        // return here and the call reports the failure.
+        if (threadIdx.x == 0) record_failure(p.status, 4, ROLE_LAYOUT << 16);
+        return;
+    }
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t sBt = base;                           // S x BT_STAGE
-    const uint32_t sAt = base + S * Cfg::BT_STAGE;       // S x AT_STAGE
-    const uint32_t bars = sAt + S * Cfg::AT_STAGE;
+    const uint32_t sAt = base + S * Cfg::BT_STAGE;       // SA x AT_STAGE
+    const uint32_t bars = sAt + SA * Cfg::AT_STAGE;
     uint8_t *gbars = gbase + (bars - base);
+    // full / empty: the (B^T, A^T) stage pairs, or the B^T ring when SPLIT
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
-    const uint32_t tfull_bar = bars + 8u * (2 * S);
+    // afull / aempty: the A^T ring when SPLIT
+    constexpr int kABars = SPLIT ? 2 * SA : 0;
+    auto afull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
+    auto aempty_bar = [&](int s) { return bars + 8u * (2 * S + SA + s); };
+    const uint32_t tfull_bar = bars + 8u * (2 * S + kABars);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int &never_abort = *reinterpret_cast<int *>(tmem_slot + 2);
     // after the main loop the ring receives the K-split partials
     const uint32_t recv_base = base;
-    const uint32_t recv_bar = bars + 8u * (2 * S + 1);
+    const uint32_t recv_bar = bars + 8u * (2 * S + kABars + 1);
     bool epi_ok = true;
-    __shared__ int never_abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -151,7 +184,14 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), share);   // one MMA commit per CTA reading the stage's A^T
+            // one MMA commit per CTA reading the stage's A^T
+            mbar_init(empty_bar(s), SPLIT ? 1 : share);
+        }
+        if constexpr (SPLIT) {
+            for (int s = 0; s < SA; ++s) {
+                mbar_init(afull_bar(s), 1);
+                mbar_init(aempty_bar(s), share);
+            }
         }
         mbar_init(tfull_bar, 1);
         mbar_init(recv_bar, 1);
@@ -181,21 +221,25 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
     if (threadIdx.x == 0) grid_launch_dependents();
     grid_dependency_wait();
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            for (int kt = kt0; kt < kt1; ++kt) {
-                if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
-                const uint32_t fb = full_bar(stage);
-                const int z = static_cast<int>(blockIdx.y);   // batch
+    // A TMA producer thread fills its ring: waits for a free slot, announces
+    // the slot's bytes, issues the loads; then waits for the loads it still
+    // has in flight (the CTA may leave only after they have landed).  One
+    // producer loads (B^T, A^T) stage pairs, or with SPLIT one per ring.
+    auto produce = [&](bool with_a, bool with_b, int slots, uint32_t full0, uint32_t empty0,
+                       uint32_t bytes, int tag) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        const int z = static_cast<int>(blockIdx.y);   // batch
+        for (int kt = kt0; kt < kt1; ++kt) {
+            if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = full0 + 8u * stage;
+            mbar_arrive_expect_tx(fb, bytes);
+            if (with_a) {
                 if (share > 1) {
                     // rows [jn*MP/2, (jn+1)*MP/2) of A^T, to this CTA and its partner
                     const uint32_t dst = sAt + stage * Cfg::AT_STAGE + jn * (Cfg::AT_STAGE / 2);
@@ -208,6 +252,8 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                 } else {
                     tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
                 }
+            }
+            if (with_b) {
 #pragma unroll
                 for (int j = 0; j < NT / Cfg::CHUNK_N; ++j) {
                     const uint32_t dst = sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX;
@@ -216,40 +262,52 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                     else
                         tma_load_2d(dst, &tmB, fb, tn * NT + j * Cfg::CHUNK_N, kt * Cfg::BK);
                 }
-                ++issued;
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok) {
-                record_failure(p.status, 6, (ROLE_PRODUCER << 16) | stage);
-                *abort_flag = 1;
-            }
-            const int64_t first = issued > S ? issued - S : 0;
-            for (int64_t i = first; i < issued; ++i) {
-                if (!mbar_wait(full_bar(static_cast<int>(i % S)),
-                               static_cast<uint32_t>((i / S) & 1), p.timeout_ns, &never_abort)) {
-                    record_failure(p.status, 6, (ROLE_DRAIN << 16) | 1);
-                    break;
-                }
+            ++issued;
+            if (++stage == slots) {
+                stage = 0;
+                phase ^= 1u;
             }
         }
+        if (!ok) {
+            record_failure(p.status, 6, (ROLE_PRODUCER << 16) | tag | stage);
+            *abort_flag = 1;
+        }
+        const int64_t first = issued > slots ? issued - slots : 0;
+        for (int64_t i = first; i < issued; ++i) {
+            if (!mbar_wait(full0 + 8u * static_cast<uint32_t>(i % slots),
+                           static_cast<uint32_t>((i / slots) & 1), p.timeout_ns, &never_abort)) {
+                record_failure(p.status, 6, (ROLE_DRAIN << 16) | tag | 1);
+                break;
+            }
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------- TMA producer: B^T (and A^T)
+        if (lane == 0)
+            produce(!SPLIT, true, S, full_bar(0), empty_bar(0),
+                    SPLIT ? Cfg::BT_STAGE : Cfg::STAGE_BYTES, 0);
+        __syncwarp();
+    } else if (SPLIT && warp == 6) {
+        // ----------------------------------- TMA producer: the A^T ring (L2)
+        if (lane == 0) produce(true, false, SA, afull_bar(0), aempty_bar(0), Cfg::AT_STAGE, 0x100);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, astage = 0;   // astage == stage unless SPLIT
+            uint32_t phase = 0, aphase = 0;
             bool ok = true;
             for (int kt = kt0; kt < kt1; ++kt) {
-                if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+                if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag) ||
+                    (SPLIT && !mbar_wait(afull_bar(astage), aphase, p.timeout_ns, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t bt0 = sBt + stage * Cfg::BT_STAGE;
-                const uint32_t at0 = sAt + stage * Cfg::AT_STAGE;
+                const uint32_t at0 = sAt + astage * Cfg::AT_STAGE;
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
                     const uint64_t bd = smem_desc_sw128(at0 + kk * 32, 16, 1024);
@@ -263,13 +321,20 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1)
                                               (kt > kt0 || kk > 0) ? 1u : 0u);
                     }
                 }
+                // the slot holding A^T is released to both CTAs that filled it
+                const uint32_t a_release = SPLIT ? aempty_bar(astage) : empty_bar(stage);
+                if (SPLIT) umma_commit(empty_bar(stage));
                 if (share > 1)
-                    umma_commit_mc(empty_bar(stage), share_mask);   // both CTAs filled the A^T
+                    umma_commit_mc(a_release, share_mask);
                 else
-                    umma_commit(empty_bar(stage));
+                    umma_commit(a_release);
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
+                }
+                if (++astage == SA) {
+                    astage = 0;
+                    aphase ^= 1u;
                 }
             }
             if (!ok) {
@@ -498,7 +563,7 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     const int tiles = (p.tiles_n + share - 1) / share * share;   // whole sharing groups
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * p.splits),
                        static_cast<unsigned>(p.batch > 0 ? p.batch : 1), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -19,7 +19,7 @@ enum OutKind : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
 // Device status word layout: [0] first tg_status code recorded, [1] where it
 // was recorded (role << 16 | detail).
 enum FailRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4,
-                      ROLE_SELFTEST = 5 };
+                      ROLE_SELFTEST = 5, ROLE_LAYOUT = 6 };
 
 enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
 
