@@ -53,6 +53,14 @@ WORKLOADS = {
     # name: (M, N, K, dtype_in, dtype_out, dist, description)
     "small127_f16": (127, 255, 65, "f16", "f32", "uniform",
                      "ragged 127x255x65, FP16 in U[-1,1), FP32 out (the correctness case)"),
+    "square256_f16": (256, 256, 256, "f16", "f16", "uniform",
+                      "square GEMM 256^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square512_f16": (512, 512, 512, "f16", "f16", "uniform",
+                      "square GEMM 512^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square1024_f16": (1024, 1024, 1024, "f16", "f16", "uniform",
+                       "square GEMM 1024^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "square2048_f16": (2048, 2048, 2048, "f16", "f16", "uniform",
+                       "square GEMM 2048^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
     "square4096_f16": (4096, 4096, 4096, "f16", "f16", "uniform",
                        "square GEMM 4096^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
     "square8192_f16": (8192, 8192, 8192, "f16", "f16", "uniform",
