@@ -384,7 +384,9 @@ const char *tg_status_string(tg_status status);
  * tg_last_device_error -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns TG_OK if no kernel recorded a
  * failure since the last call, TG_ERR_TIMEOUT if a bounded wait ran out, or
- * TG_ERR_CUDA if the synchronisation itself failed.
+ * TG_ERR_CUDA if the synchronisation itself failed or a kernel found its
+ * shared memory not aligned as it requires (it then returns without writing
+ * C).
  */
 tg_status tg_last_device_error(void *stream);
 
