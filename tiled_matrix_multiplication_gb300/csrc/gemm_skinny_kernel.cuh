@@ -28,15 +28,17 @@
 // owns the column -- CTA r owns columns [r*NT/S, (r+1)*NT/S) -- with
 // asynchronous remote stores (st.async) into the owner's idle ring; the owner
 // waits on one mbarrier for all the bytes, sums the S partials in K-range
-// order, rounds once and writes C.  No partials go to global memory and no
+// order, rounds once, stages the tile and writes C in 16-byte pieces.  No
+// partials go to global memory and no
 // second kernel runs; the sum order is fixed, so results do not depend on
 // timing.  (Pulling the partials with remote loads instead cost one cluster
 // round trip per few outputs: 5 to 10 us per call at 64 to 128 rows.)
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = TMEM epilogue (direct stores, or the pushes); all six warps
-// then sum the received partials.  Every mbarrier wait is bounded (status
-// word + abort flag, as in gemm_tc.cu).
+// warps 2..5 = TMEM epilogue (direct stores, or the pushes), and at 128 rows
+// (two CTAs per SM) warp 6 = a second TMA producer for a separate A^T ring;
+// all warps then sum the received partials.  Every mbarrier wait is bounded
+// (status word + abort flag, as in gemm_tc.cu).
 #pragma once
 
 #include <cuda_bf16.h>
