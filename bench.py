@@ -81,6 +81,9 @@ WORKLOADS = {
                         "square GEMM 8192^3, FP8 E4M3 in U[-1,1), FP32 accumulate, FP16 out"),
     "tf32_2048": (2048, 2048, 2048, "f32", "f32", "uniform",
                   "FP32 operands at TF32 2048^3, FP32 out"),
+    "tf32_ragged": (1000, 1999, 777, "f32", "f32", "uniform",
+                    "FP32 operands at TF32, ragged 1000x1999x777 (tails in M, N and K), "
+                    "FP32 out"),
     "skinny1_f16": (1, 8192, 8192, "f16", "f16", "uniform", "skinny M=1, N=K=8192 FP16"),
     "skinny16_f16": (16, 8192, 8192, "f16", "f16", "uniform", "skinny M=16, N=K=8192 FP16"),
     "skinny64_f16": (64, 8192, 8192, "f16", "f16", "uniform", "skinny M=64, N=K=8192 FP16"),

@@ -11,7 +11,16 @@
 // splitk_reduce: C[m,n] = round(epilogue(sum_{s=0}^{S-1} P[s,m,n])) in increasing s --
 //   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
 //   both steps"), finished across work units instead of inside one.
+//
+// All of them are launched with programmatic dependent launch, like the GEMM
+// kernels: a launch may be scheduled while the previous kernel of the stream
+// drains, waits for that kernel's writes before its first global-memory
+// access (griddepcontrol.wait), and at once lets the kernel after it be
+// scheduled.  A call made of a pack and a GEMM then pays one launch latency
+// instead of two (127 x 255 x 65 with both operands packed: 18.5 us a call
+// with plain launches).
 #include <algorithm>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -27,6 +36,8 @@ namespace {
 template <typename T>
 __global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
                                  int64_t ld_dst, int64_t rows, int64_t cols) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t total = rows * cols;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -49,6 +60,8 @@ __global__ void __launch_bounds__(256) pack_transpose_kernel(const T *__restrict
                                                              int64_t ld_dst, int64_t rows,
                                                              int64_t cols) {
     __shared__ T tile[kTrCols / 32][32][33];
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
     const int tx = threadIdx.x, ty = threadIdx.y;
     for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTrRows; r0 < rows;
@@ -96,6 +109,8 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 // A' = [hi(A) | lo(A) | hi(A)], [M, 3K] with pitch ld_dst.
 __global__ void split3_rows_kernel(const float *__restrict__ a, int64_t lda, float *__restrict__ dst,
                                    int64_t ld_dst, int64_t M, int64_t K) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t total = M * K;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -119,6 +134,8 @@ __global__ void __launch_bounds__(256) split3_transpose_kernel(const float *__re
                                                                int64_t ld_dst, int64_t K,
                                                                int64_t N) {
     __shared__ float hi_t[kTrCols / 32][32][33], lo_t[kTrCols / 32][32][33];
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
     const int tx = threadIdx.x, ty = threadIdx.y;
     for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTrRows; k0 < K;
@@ -166,6 +183,8 @@ __device__ __forceinline__ void store_out(void *c, int64_t off, int out_kind, fl
 __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, int64_t M,
                                      int64_t N, void *c, int64_t ldc, int out_kind,
                                      int vec_ok, const EpiParams epi) {
+    grid_dependency_wait();      // the partials of the GEMM kernel before it
+    grid_launch_dependents();
     const int64_t groups_per_row = (N + 3) / 4;
     const int64_t total = M * groups_per_row;
     const int64_t plane = M * N;
@@ -220,6 +239,24 @@ int grid_for(int64_t work, int threads) {
     return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
 }
 
+// Launches `kern` with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
@@ -228,20 +265,18 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
     const int threads = 256;
     const int blocks = grid_for(rows * cols, threads);
     if (esize == 1)
-        pack_rows_kernel<uint8_t><<<blocks, threads, 0, stream>>>(
-            static_cast<const uint8_t *>(src), ld_src, static_cast<uint8_t *>(dst), ld_dst, rows,
-            cols);
-    else if (esize == 2)
-        pack_rows_kernel<uint16_t><<<blocks, threads, 0, stream>>>(
-            static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst, rows,
-            cols);
-    else if (esize == 4)
-        pack_rows_kernel<uint32_t><<<blocks, threads, 0, stream>>>(
-            static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst, rows,
-            cols);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(pack_rows_kernel<uint8_t>, dim3(blocks), dim3(threads), stream,
+                          static_cast<const uint8_t *>(src), ld_src, static_cast<uint8_t *>(dst),
+                          ld_dst, rows, cols);
+    if (esize == 2)
+        return launch_pdl(pack_rows_kernel<uint16_t>, dim3(blocks), dim3(threads), stream,
+                          static_cast<const uint16_t *>(src), ld_src,
+                          static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    if (esize == 4)
+        return launch_pdl(pack_rows_kernel<uint32_t>, dim3(blocks), dim3(threads), stream,
+                          static_cast<const uint32_t *>(src), ld_src,
+                          static_cast<uint32_t *>(dst), ld_dst, rows, cols);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
@@ -252,16 +287,14 @@ cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, in
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
     if (esize == 2)
-        pack_transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint16_t *>(src), ld_src, static_cast<uint16_t *>(dst), ld_dst,
-            rows, cols);
-    else if (esize == 4)
-        pack_transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint32_t *>(src), ld_src, static_cast<uint32_t *>(dst), ld_dst,
-            rows, cols);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(pack_transpose_kernel<uint16_t>, grid, block, stream,
+                          static_cast<const uint16_t *>(src), ld_src,
+                          static_cast<uint16_t *>(dst), ld_dst, rows, cols);
+    if (esize == 4)
+        return launch_pdl(pack_transpose_kernel<uint32_t>, grid, block, stream,
+                          static_cast<const uint32_t *>(src), ld_src,
+                          static_cast<uint32_t *>(dst), ld_dst, rows, cols);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream) {
@@ -273,9 +306,9 @@ cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld
                                int64_t K, cudaStream_t stream) {
     if (M <= 0 || K <= 0) return cudaSuccess;
     const int threads = 256;
-    split3_rows_kernel<<<grid_for(M * K, threads), threads, 0, stream>>>(
-        static_cast<const float *>(a), lda, static_cast<float *>(dst), ld_dst, M, K);
-    return cudaGetLastError();
+    return launch_pdl(split3_rows_kernel, dim3(grid_for(M * K, threads)), dim3(threads), stream,
+                      static_cast<const float *>(a), lda, static_cast<float *>(dst), ld_dst, M,
+                      K);
 }
 
 cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
@@ -284,10 +317,10 @@ cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64
     const int64_t gx = (N + kTrCols - 1) / kTrCols;
     const int64_t gy = std::min<int64_t>((K + kTrRows - 1) / kTrRows, 65535);   // + row loop
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    split3_transpose_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
-                              dim3(32, 8), 0, stream>>>(static_cast<const float *>(b), ldb,
-                                                       static_cast<float *>(dst), ld_dst, K, N);
-    return cudaGetLastError();
+    return launch_pdl(split3_transpose_kernel,
+                      dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8),
+                      stream, static_cast<const float *>(b), ldb, static_cast<float *>(dst),
+                      ld_dst, K, N);
 }
 
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N, void *c,
@@ -300,9 +333,8 @@ cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, in
     const int vec_ok = (N % 4) == 0;
     EpiParams e{};
     if (epi) e = *epi;
-    splitk_reduce_kernel<<<grid_for(work, threads), threads, 0, stream>>>(partial, splits, M, N, c,
-                                                                          ldc, out_kind, vec_ok, e);
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel, dim3(grid_for(work, threads)), dim3(threads), stream,
+                      partial, splits, M, N, c, ldc, out_kind, vec_ok, e);
 }
 
 }  // namespace tg

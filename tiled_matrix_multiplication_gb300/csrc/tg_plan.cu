@@ -228,6 +228,10 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         for (int64_t sc : {2, 4, 8}) {
             const int64_t kps = cdiv(ktiles, sc);
             if ((sc - 1) * kps >= ktiles) continue;          // a K range would be empty
+            // K ranges of fewer than 4 k-tiles (512 bytes of K) stream too little
+            // to pay for the reduction (127 x 255 x 65: 10.3 us unsplit, 13.7 us
+            // with two ranges of one k-tile each)
+            if (kps < 4) continue;
             if (opt && opt->splits && opt->splits != sc) continue;
             if (opt && opt->multicast == 2 && sc > 4) continue;   // clusters of <= 8 CTAs
             if (tiles * sc <= cap) {
