@@ -47,3 +47,32 @@ def test_traffic_lookup_follows_the_code_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("w_same") == 123
     assert bench.profiled_traffic("w_old") is None
     assert bench.profiled_traffic("missing") is None
+
+
+def test_every_bench_workload_plans_on_the_host():
+    """Each workload bench.py can time gets a valid plan from the host-only
+    planner (152 SMs): the small-M kernel at most 128 rows, the tile kernel
+    otherwise, one launch per batch where the batch allows it, and no
+    operand packing except where a row pitch is not a 16-byte multiple."""
+    import tiled_matrix_multiplication_gb300 as tg
+    from tiled_matrix_multiplication_gb300 import build as tgbuild
+    tgbuild.build()
+    tg.load()
+    for name, (M, N, K, din, dout, _dist, _desc) in bench.WORKLOADS.items():
+        opts = dict(bench.WORKLOAD_OPTS.get(name, {}))
+        batch = bench.BATCH.get(name, 1)
+        if batch > 1:
+            p = tg.plan_batched(batch, M, N, K, din, dout, num_sms=152, **opts)
+            assert p["per_batch"] == 0, name
+        else:
+            p = tg.plan(M, N, K, din, dout, num_sms=152, **opts)
+        want_skinny = M <= 128
+        assert (p["path"] == tg.TG_PATH_SKINNY) == want_skinny, (name, p)
+        aligned = (K * bench.ESIZE[din]) % 16 == 0 and (N * bench.ESIZE[din]) % 16 == 0
+        if aligned and din != "f32":
+            assert p["pack_a"] == 0 and p["pack_b"] == 0, (name, p)
+        assert p["ctas"] >= 1 and p["tiles"] >= 1, (name, p)
+    # the default workload is the A-multicast pair kernel the profiles describe
+    M, N, K, din, dout = bench.WORKLOADS[bench.DEFAULT_WORKLOAD][:5]
+    p = tg.plan(M, N, K, din, dout, num_sms=152)
+    assert (p["path"], p["block_n"], p["multicast"]) == (tg.TG_PATH_TC_PAIR, 256, 2)
