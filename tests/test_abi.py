@@ -287,3 +287,28 @@ def test_plan_small_m_up_to_128_rows(lib, M, din):
     # 129 rows: no longer the small-M kernel
     st, p = plan(129, 8192, 8192, din, "f16" if din == "e4m3" else din, sms=148)
     assert st == tg.TG_OK and p["path"] != tg.TG_PATH_SKINNY
+
+
+def test_noalloc_argument_errors_on_the_host(lib):
+    """tg_gemm_splitk_noalloc rejects bad arguments before it touches a device
+    (the device array's set-up comes after these checks), and an empty output
+    is a no-op.  Only calls that stop before any device work are made here."""
+    call = tg.tg_gemm_splitk_noalloc
+    ok = dict(M=256, N=512, K=1024, lda=1024, ldb=512, ldc=512)
+
+    def st(splits=2, din="f16", dout="f16", a=A, b=B, c=C, **kw):
+        d = dict(ok, **kw)
+        return call(d["M"], d["N"], d["K"], a, d["lda"], b, d["ldb"], c, d["ldc"], din, dout,
+                    splits, 0)
+
+    assert st(splits=0) == tg.TG_ERR_INVALID_VALUE
+    assert st(splits=129) == tg.TG_ERR_INVALID_VALUE
+    assert st(din="f32", dout="f32") == tg.TG_ERR_UNSUPPORTED        # TF32 needs B^T
+    assert st(din="e4m3", dout="f16") == tg.TG_ERR_UNSUPPORTED
+    assert st(din="f16", dout="bf16") == tg.TG_ERR_UNSUPPORTED       # not a type pair
+    assert st(M=-1) == tg.TG_ERR_INVALID_VALUE
+    assert st(lda=1000) == tg.TG_ERR_INVALID_VALUE                   # lda < K
+    assert st(ldc=500) == tg.TG_ERR_INVALID_VALUE                    # ldc < N
+    assert st(a=0) == tg.TG_ERR_INVALID_VALUE
+    assert st(c=A + 64) == tg.TG_ERR_INVALID_VALUE                   # C overlaps A
+    assert st(M=0) == tg.TG_OK and st(N=0) == tg.TG_OK               # nothing to do
