@@ -312,3 +312,22 @@ def test_noalloc_argument_errors_on_the_host(lib):
     assert st(a=0) == tg.TG_ERR_INVALID_VALUE
     assert st(c=A + 64) == tg.TG_ERR_INVALID_VALUE                   # C overlaps A
     assert st(M=0) == tg.TG_OK and st(N=0) == tg.TG_OK               # nothing to do
+
+
+def test_host_operand_call_argument_errors_on_the_host(lib):
+    """tg_gemm_host applies tg_gemm's argument rules to its host pointers
+    before it stages anything, and an empty output is a no-op.  Only calls
+    that stop before any device work are made here."""
+    call = tg.tg_gemm_host
+
+    def st(M=300, N=200, K=100, lda=100, ldb=200, ldc=200, din="f16", dout="f16", a=A, b=B,
+           c=C, options=None):
+        return call(M, N, K, a, lda, b, ldb, c, ldc, din, dout, 0, options)
+
+    assert st(K=-1) == tg.TG_ERR_INVALID_VALUE
+    assert st(ldb=199) == tg.TG_ERR_INVALID_VALUE
+    assert st(din="bf16", dout="f16") == tg.TG_ERR_UNSUPPORTED
+    assert st(b=0) == tg.TG_ERR_INVALID_VALUE
+    assert st(c=B + 16) == tg.TG_ERR_INVALID_VALUE                   # C overlaps B
+    assert st(options=tg.make_options(multicast=3)) == tg.TG_ERR_INVALID_VALUE
+    assert st(M=0) == tg.TG_OK and st(N=0) == tg.TG_OK
