@@ -167,7 +167,9 @@ typedef struct tg_plan {
 } tg_plan;
 
 /*
- * tg_gemm -- C = A * B (see the top of this file for layout, types and errors).
+ * tg_gemm -- C = A * B, the product of "Matrix multiplication: reuse the
+ * inputs" (triton-cuda-lab lesson 6), section "The three dimensions have
+ * different jobs" (see the top of this file for layout, types and errors).
  *   M, N, K   sizes (>= 0)
  *   a, lda    device pointer to A and its leading dimension (elements, >= K)
  *   b, ldb    device pointer to B and its leading dimension (elements, >= N)
@@ -183,7 +185,15 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K,
                   tg_dtype dtype_in, tg_dtype dtype_out,
                   void *stream);
 
-/* tg_gemm with planner overrides (`opt` may be NULL). */
+/*
+ * tg_gemm_ex -- tg_gemm (the same operation, arguments, layout, ownership and
+ * errors) with planner overrides; `opt` may be NULL.  The overrides pick among
+ * the compiled variants of the tiled multiply -- tile width, CTA pair or single
+ * CTA, K split, grouped-raster height -- which the pages fix per kernel as
+ * constants ("Matrix Multiplication", teenygrad docs, section "Tiles"; "Triton
+ * tiled matmul", llm-systems-cookbook, section "The kernel"); values the
+ * compiled kernels cannot honour return TG_ERR_UNSUPPORTED.
+ */
 tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K,
                      const void *a, int64_t lda,
                      const void *b, int64_t ldb,
@@ -196,7 +206,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K,
  * as tg_gemm_ex does (pointers are inspected for alignment and overlap only,
  * never dereferenced) and fills *plan with what tg_gemm_ex would launch on a
  * device with `num_sms` SMs.  Returns the status tg_gemm_ex would return for
- * an argument error, else TG_OK.
+ * an argument error, else TG_OK.  No counterpart in the pages: it reports the
+ * library's own choice of kernel variant.  `plan` is owned by the caller.
  */
 tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K,
                        const void *a, int64_t lda,
@@ -257,7 +268,9 @@ tg_status tg_gemm_fused(int64_t M, int64_t N, int64_t K,
                         void *stream, const tg_options *opt);
 
 /*
- * tg_gemm_host -- C = A * B with A, B and C in HOST memory: the library stages
+ * tg_gemm_host -- C = A * B with A, B and C in HOST memory (the operation of
+ * tg_gemm, "Matrix multiplication: reuse the inputs", triton-cuda-lab lesson 6,
+ * section "The three dimensions have different jobs"): the library stages
  * them through device memory of its own and overlaps the transfers with the
  * multiply.  B is copied first, then A in row panels (at least 1024 rows, at
  * most 16 panels) on one copy stream; the panel products run on `stream` as
@@ -368,7 +381,8 @@ tg_status tg_gemm_strided_batched_fused(int64_t batch, int64_t M, int64_t N, int
 /*
  * tg_plan_gemm_strided_batched -- host only, like tg_plan_gemm: validates as
  * tg_gemm_strided_batched does and fills *plan with what it would launch on a
- * device with `num_sms` SMs (tiles counts the tiles of all products).
+ * device with `num_sms` SMs (tiles counts the tiles of all products).  No
+ * counterpart in the pages.
  */
 tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
                                        const void *a, int64_t lda, int64_t stride_a,
@@ -377,7 +391,8 @@ tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int6
                                        tg_dtype dtype_in, tg_dtype dtype_out,
                                        int32_t num_sms, const tg_options *opt, tg_plan *plan);
 
-/* Static, human-readable name of a status code. */
+/* Static, human-readable name of a status code (library plumbing, no
+ * counterpart in the pages; the string is owned by the library). */
 const char *tg_status_string(tg_status status);
 
 /*
@@ -386,7 +401,7 @@ const char *tg_status_string(tg_status status);
  * failure since the last call, TG_ERR_TIMEOUT if a bounded wait ran out, or
  * TG_ERR_CUDA if the synchronisation itself failed or a kernel found its
  * shared memory not aligned as it requires (it then returns without writing
- * C).
+ * C).  No counterpart in the pages, which report no device-side failures.
  */
 tg_status tg_last_device_error(void *stream);
 
@@ -402,7 +417,7 @@ tg_status tg_last_device_error(void *stream);
  */
 tg_status tg_selftest_timeout(int32_t timeout_ms, void *stream);
 
-/* TG_ABI_VERSION of the loaded library. */
+/* TG_ABI_VERSION of the loaded library (no counterpart in the pages). */
 int32_t tg_abi_version(void);
 
 /* Size of the library-owned device array used by tg_gemm_splitk_noalloc. */

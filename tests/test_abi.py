@@ -331,3 +331,17 @@ def test_host_operand_call_argument_errors_on_the_host(lib):
     assert st(c=B + 16) == tg.TG_ERR_INVALID_VALUE                   # C overlaps B
     assert st(options=tg.make_options(multicast=3)) == tg.TG_ERR_INVALID_VALUE
     assert st(M=0) == tg.TG_OK and st(N=0) == tg.TG_OK
+
+
+def test_every_declaration_cites_its_passage_or_says_it_has_none():
+    """Each entry point's comment in the header names the page passage that
+    defines what it computes, or states that the pages have no counterpart."""
+    text = open(HEADER).read()
+    pages = ("teenygrad", "llm-systems-cookbook", "triton-cuda-lab", "Fast matrix multiplication")
+    for name in declared_functions():
+        decl = re.search(r"\n(?:tg_status|const char\s*\*|int32_t)\s+" + name + r"\s*\(", text)
+        assert decl, name
+        comment = text[:decl.start()].rsplit("/*", 1)[1]
+        assert "*/" in comment and text[:decl.start()].rstrip().endswith("*/"), name
+        assert any(p in comment for p in pages) or \
+            ("counterpart" in comment and "pages" in comment), name
