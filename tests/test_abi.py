@@ -339,7 +339,7 @@ def test_every_declaration_cites_its_passage_or_says_it_has_none():
     text = open(HEADER).read()
     pages = ("teenygrad", "llm-systems-cookbook", "triton-cuda-lab", "Fast matrix multiplication")
     for name in declared_functions():
-        decl = re.search(r"\n(?:tg_status|const char\s*\*|int32_t)\s+" + name + r"\s*\(", text)
+        decl = re.search(r"\n(?:tg_status\s+|const char\s*\*\s*|int32_t\s+)" + name + r"\s*\(", text)
         assert decl, name
         comment = text[:decl.start()].rsplit("/*", 1)[1]
         assert "*/" in comment and text[:decl.start()].rstrip().endswith("*/"), name
