@@ -12,9 +12,9 @@ Measurement:
   * inputs are resident in HBM before the timed region; each step uses the
     next of R rotating (A, B, C) sets whose total exceeds twice the L2 size, so
     no step finds its operands in L2;
-  * the timed region is K back-to-back steps between a barrier +
-    torch.cuda.synchronize() on both sides, timed with CUDA events recorded on
-    the stream the kernels are launched on (max over ranks);
+  * the timed region is K back-to-back steps with torch.cuda.synchronize() on
+    both sides, timed with CUDA events recorded on the stream the kernels are
+    launched on;
   * ``roofline.achieved`` divides the algorithmic FLOPs of one launch (2MNK) by
     the average duration of a launch in the timed region (its length over K;
     no events between launches, which would block the overlap of consecutive
@@ -24,13 +24,15 @@ Measurement:
     (pipelined with the multiply by the library) are inside its timed region;
   * SM clocks and throttle reasons are sampled with nvidia-smi during the timed
     region;
-  * ``cpu_baseline`` times the CPU FP64 oracle (rank 0, N = 1 only) on a
+  * ``cpu_baseline`` times the CPU FP64 oracle on a
     bounded sample of output rows of the same problem.
 
 ``--impl reference`` runs the CPU oracle arm instead (rank 0 only under
 torchrun); each step is a bounded sample of output rows of the same workload.
-Multi-GPU runs are independent replicas (the GEMM is not sharded): value is
-the total FLOP rate of all ranks.
+
+One GPU only.  The library's tile kernels share A tiles between the CTAs of
+a cluster by TMA multicast, which is only used in single-GPU processes: the
+GPU arm refuses ``--gpus`` > 1 and a torchrun launch with WORLD_SIZE > 1.
 """
 from __future__ import annotations
 
@@ -135,33 +137,18 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world, local):
-    import torch
-    import torch.distributed as dist
-    if world > 1 and not dist.is_initialized():
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    return world > 1
+ONE_GPU_ONLY = ("the GPU arm runs on one GPU only: its tile kernels share A tiles inside a "
+                "cluster by TMA multicast, which this library uses only in single-GPU "
+                "processes (got {what})")
 
 
-def barrier(on):
-    if on:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x: float, on: bool) -> float:
-    if not on:
-        return x
-    import torch
-    import torch.distributed as dist
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def refuse_multi_gpu(gpus: int, world: int):
+    """The reason the GPU arm refuses this launch, or None for one GPU."""
+    if gpus > 1:
+        return ONE_GPU_ONLY.format(what=f"--gpus {gpus}")
+    if world > 1:
+        return ONE_GPU_ONLY.format(what=f"WORLD_SIZE={world}")
+    return None
 
 
 def peaks():
@@ -355,7 +342,7 @@ def run_reference(args, world, rank):
 
 # --------------------------------------------------------------- GPU arm
 
-def run_ours(args, world, rank, local):
+def run_ours(args, local):
     import numpy as np
     import torch
 
@@ -363,7 +350,6 @@ def run_ours(args, world, rank, local):
     from tiled_matrix_multiplication_gb300 import build as tgbuild
     from tiled_matrix_multiplication_gb300 import inputs
 
-    dist_on = init_dist(world, local)
     torch.cuda.set_device(local)
     tgbuild.build()
     tg.load()
@@ -444,7 +430,6 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)                                   # let nvidia-smi start sampling
-    barrier(dist_on)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     ev_start.record(stream)
@@ -453,15 +438,14 @@ def run_ours(args, world, rank, local):
     ev_end.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
-    barrier(dist_on)
     clocks = sampler.stop()
     tg.check_device_error()
-    region_ms = max_over_ranks(ev_start.elapsed_time(ev_end), dist_on)
+    region_ms = ev_start.elapsed_time(ev_end)
     kernel_ms = region_ms / K_steps
 
     flops = 2.0 * M * N * K * nb
     ms_per_step = region_ms / K_steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e_steps = max(3, min(K_steps, 50))
@@ -501,7 +485,6 @@ def run_ours(args, world, rank, local):
 
     for i in range(2):
         e2e_step(i)
-    barrier(dist_on)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -512,16 +495,10 @@ def run_ours(args, world, rank, local):
     stream.wait_stream(e2e_streams[1])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist_on)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
     tg.check_device_error()
     h2d = nb * (M * K + K * N) * ESIZE[din]
     d2h = nb * M * N * ESIZE[dout]
-
-    if rank != 0:
-        if dist_on:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return 0
 
     pk, pk_kind = peaks()
     skinny = M <= 128
@@ -543,20 +520,20 @@ def run_ours(args, world, rank, local):
                       + ("" if plan["kernels"] == 1 else " (+ helper kernels)"),
             "launch_ms": round(kernel_ms, 5)}
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": din,
         "data": "synthetic",
         "config": {"workload": desc, "M": M, "N": N, "K": K, "batch": nb, "dtype_in": din,
-                   "dtype_out": dout, "accumulate": "f32", "parallelism": "replicas" if world > 1 else "single",
+                   "dtype_out": dout, "accumulate": "f32", "parallelism": "single",
                    "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> 2x L2 {l2 / 1e6:.0f} MB)",
                    "tile": f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}",
                    "splits": plan["splits"], "ctas": plan["ctas"],
                    "multicast": plan["multicast"], "options": opts or None},
-        "pct_of_peak": round(100.0 * value / world / peak, 2) if not skinny else None,
+        "pct_of_peak": round(100.0 * value / peak, 2) if not skinny else None,
         "clocks": clocks,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
                 "how": ("tg_gemm_fused after host->device copies, result copied back"
@@ -568,12 +545,9 @@ def run_ours(args, world, rank, local):
         "wall_s": round(t_wall, 3),
         "gpu": props.name,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(M, N, K, din, dist, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
-    if dist_on:
-        import torch.distributed as dist
-        dist.destroy_process_group()
     return 0
 
 
@@ -595,7 +569,11 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
-    return run_ours(args, world, rank, local)
+    why = refuse_multi_gpu(args.gpus, world)
+    if why is not None:
+        log("bench.py: " + why)
+        return 2
+    return run_ours(args, local)
 
 
 if __name__ == "__main__":

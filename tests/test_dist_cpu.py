@@ -1,8 +1,11 @@
-"""The multi-process side of bench.py on CPU (gloo, world size 2): ranks
-rendezvous on 127.0.0.1, the timed value is the maximum over ranks, and under
-torchrun the reference arm runs on rank 0 alone and prints exactly one JSON
-line while the other rank exits 0.  The GEMM itself is not sharded (each rank
-is an independent replica), so this covers all the N > 1 logic there is."""
+"""bench.py's launch rules on CPU.
+
+The GPU arm runs on one GPU only: the library's tile kernels share A tiles
+inside a thread-block cluster by TMA multicast, which is used only in
+single-GPU processes, so ``--gpus N`` with N > 1 and a torchrun launch with
+WORLD_SIZE > 1 are refused before any GPU work.  The reference arm (the CPU
+oracle) still runs under torchrun: rank 0 prints exactly one JSON line and the
+other ranks exit 0 without work."""
 from __future__ import annotations
 
 import json
@@ -14,6 +17,7 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
 
 
 def free_port() -> int:
@@ -22,27 +26,27 @@ def free_port() -> int:
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, out_dir):
-    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
-                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
-    sys.path.insert(0, ROOT)
+def test_refusal_rule():
     import bench
-    on = bench.init_dist(world, rank)
-    assert on
-    bench.barrier(on)
-    m = bench.max_over_ranks(1.5 + rank, on)
-    with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
-        f.write(repr(m))
-    import torch.distributed as dist
-    dist.destroy_process_group()
+    assert bench.refuse_multi_gpu(1, 1) is None
+    assert "--gpus 2" in bench.refuse_multi_gpu(2, 1)
+    assert "WORLD_SIZE=4" in bench.refuse_multi_gpu(1, 4)
+    assert "multicast" in bench.refuse_multi_gpu(8, 8)
 
 
-def test_max_over_ranks_gloo(tmp_path):
-    import torch.multiprocessing as mp
-    port = free_port()
-    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
-    for r in range(2):
-        assert float((tmp_path / f"rank{r}.txt").read_text()) == 2.5
+@pytest.mark.parametrize("argv,env", [
+    (["--gpus", "2"], {}),
+    (["--gpus", "1"], {"WORLD_SIZE": "2", "RANK": "0", "LOCAL_RANK": "0"}),
+])
+def test_gpu_arm_refuses_more_than_one_gpu(argv, env):
+    # refused before torch, the library or a GPU is touched: exit code 2 and
+    # the reason on stderr, no JSON line
+    r = subprocess.run([sys.executable, "bench.py", *argv, "--steps", "2", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=120,
+                       env={**os.environ, **env})
+    assert r.returncode == 2, (r.returncode, r.stderr[-2000:])
+    assert "one GPU only" in r.stderr
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
 
 
 @pytest.mark.timeout(300)

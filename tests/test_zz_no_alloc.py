@@ -51,10 +51,19 @@ def _bits(t, dout):
     (64, 8192, 4096, "f16", "f16", 4),
     (128, 4096, 2048, "bf16", "f32", 3),
     (100, 1000, 777 + 7, "bf16", "bf16", 5),
+    # more than 128 rows: the planner picks 224-wide tiles, whose B boxes are
+    # 64-byte swizzled (112 of them are 448 bytes per K row); ragged N
+    (896, 2000, 1024, "bf16", "bf16", 2),
+    (1024, 2048, 1024, "f16", "f16", 2),   # 256-wide tiles; the array exactly full
 ])
 def test_noalloc_matches_existing_entry_point(tg, M, N, K, din, dout, splits):
     import torch
     import oracle
+    if M > 128:
+        p = tg.plan(M, N, K, din, dout, num_sms=torch.cuda.get_device_properties(0).multi_processor_count,
+                    path=tg.TG_PATH_TC, splits=splits)
+        assert p["block_n"] != 128 and p["splits"] == splits, p
+        assert splits * M * N * 4 <= tg.NOALLOC_SCRATCH_BYTES
     tdo = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dout]
     stream = torch.cuda.current_stream().cuda_stream
     opt = tg.make_options(path=tg.TG_PATH_TC, splits=splits)

@@ -21,14 +21,7 @@
 // every partial element it later reads, so nothing needs clearing between
 // calls, but two calls whose kernels overlap on the GPU (different streams
 // without ordering between them) race on the array.
-#include <cuda.h>
-#include <cuda_runtime.h>
-
-#include <cstring>
-#include <mutex>
-
-#include "tg_gemm.h"
-#include "tg_internal.h"
+#include "tg_host_api.h"
 
 namespace {
 
@@ -36,7 +29,7 @@ constexpr int64_t kScratchFloats = static_cast<int64_t>(TG_NOALLOC_SCRATCH_BYTES
 
 static __device__ __align__(256) float g_splitk_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
+using tgh::kMaxDevices;
 
 struct NoAllocDevice {
     bool init = false;
@@ -110,10 +103,6 @@ tg_status encode(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, in
     return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
 }
 
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-int in_kind_of_noalloc(tg_dtype t) { return t == TG_F16 ? tg::IN_F16 : tg::IN_BF16; }
-
 }  // namespace
 
 extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, const void *a,
@@ -126,56 +115,60 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     std::memset(&opt, 0, sizeof(opt));
     opt.path = TG_PATH_TC;
     opt.splits = splits;
-    tg_plan plan;
-    // Host-only validation and planning (same rules as tg_gemm_ex).
-    tg_status st = tg_plan_gemm(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, 148, &opt,
-                                &plan);
+    // Host-only validation (the rules of tg_gemm_ex).
+    tg_status st = tgh::validate(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, &opt);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
     NoAllocDevice *dev = nullptr;
     st = setup_current_device(&dev);
     if (st != TG_OK) return st;
+    st = tgh::operands_local({c, K > 0 ? a : nullptr, K > 0 ? b : nullptr});
+    if (st != TG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int eo = dtype_out == TG_F32 ? 4 : 2;
+    const int eo = tgh::esize_of(dtype_out);
     if (K == 0)
         return cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
-    st = tg_plan_gemm(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, &opt, &plan);
-    if (st != TG_OK) return st;
+    // The planner's choice for this device; K tiles per split, tile width,
+    // multicast and the wait bound are all taken from it.
+    tgh::Plan pl;
+    tgh::make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, &opt, &pl);
+    if (!pl.valid) return TG_ERR_UNSUPPORTED;
+    const tg_plan &plan = pl.pub;
     // A and B are read in place: no packed copies (that would need more memory).
     if (plan.pack_a || plan.pack_b) return TG_ERR_UNSUPPORTED;
     if (plan.splits > 1 && static_cast<int64_t>(plan.splits) * M * N > kScratchFloats)
         return TG_ERR_UNSUPPORTED;   // partials exceed TG_NOALLOC_SCRATCH_BYTES
 
-    const int64_t k_tiles = cdiv(K, plan.block_k);
-    const int64_t kps = cdiv(k_tiles, splits);
+    const int in_kind = tgh::in_kind_of(dtype_in);
+    const int mc = std::max(plan.multicast, 1);
+    // with A multicast each CTA loads half of its 128 rows of A
+    const int a_rows = mc == 2 ? tgh::kBlockM / 2 : tgh::kBlockM;
     CUtensorMap tmA, tmB;
-    if (encode(&tmA, dtype_in, a, M, K, lda, plan.block_k, plan.block_m) != TG_OK ||
+    if (encode(&tmA, dtype_in, a, M, K, lda, plan.block_k, a_rows) != TG_OK ||
         encode(&tmB, dtype_in, b, K, N, ldb,
-               tg::tc_b_swizzle_bytes(in_kind_of_noalloc(dtype_in), plan.block_n, false) / 2,
-               plan.block_k) != TG_OK)
+               tg::tc_b_swizzle_bytes(in_kind, plan.block_n, false) / 2, plan.block_k) != TG_OK)
         return TG_ERR_CUDA;
     tg::TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
     tp.M = static_cast<int32_t>(M);
     tp.N = static_cast<int32_t>(N);
     tp.K = static_cast<int32_t>(K);
-    tp.tiles_m = static_cast<int32_t>(cdiv(M, plan.block_m));
-    tp.tiles_n = static_cast<int32_t>(cdiv(N, plan.block_n));
-    tp.k_tiles = static_cast<int32_t>(k_tiles);
-    tp.k_tiles_per_split = static_cast<int32_t>(kps);
+    tp.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    tp.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    tp.k_tiles = static_cast<int32_t>(pl.k_tiles);
+    tp.k_tiles_per_split = static_cast<int32_t>(pl.k_per_split);
     tp.splits = plan.splits;
     tp.group_m = plan.group_m;
     tp.out_kind = dtype_out == TG_F16 ? tg::OUT_F16 : (dtype_out == TG_BF16 ? tg::OUT_BF16 : tg::OUT_F32);
     tp.c_vector = plan.c_vector;
-    tp.mc = 1;
+    tp.mc = mc;
     tp.ldc = ldc;
     tp.c = c;
     tp.partial = plan.splits > 1 ? dev->scratch : nullptr;
     tp.status = dev->status;
-    tp.timeout_ns = 2000ull * 1000000ull;
+    tp.timeout_ns = pl.timeout_ns;
     tp.batch = 1;
-    const int in_kind = dtype_in == TG_F16 ? tg::IN_F16 : tg::IN_BF16;
-    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, 1, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
+    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, mc, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
         return TG_ERR_CUDA;
     if (plan.splits > 1 &&
         tg::launch_splitk_reduce(dev->scratch, plan.splits, M, N, c, ldc, tp.out_kind,

@@ -97,6 +97,31 @@ static tg_status encode_2d(CUtensorMap *map, tg_dtype t, const void *ptr, int64_
     return r == CUDA_SUCCESS ? TG_OK : TG_ERR_CUDA;
 }
 
+// Operands must be device memory of the current device: the tile kernels read
+// A through TMA loads multicast to the CTAs of a cluster of this GPU, and no
+// kernel of the library is meant to read host memory or a peer GPU's memory
+// over the interconnect.  Memory from cudaMalloc, a stream-ordered pool or a
+// mapping backed by this device qualifies; host, managed and peer memory do
+// not.  Null pointers (absent epilogue vectors) are skipped.
+tg_status operands_local(std::initializer_list<const void *> ptrs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+    for (const void *p : ptrs) {
+        if (p == nullptr) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            (void)cudaGetLastError();   // not a pointer the runtime knows
+            return TG_ERR_INVALID_VALUE;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != dev) return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+static tg_status epilogue_local(const tg_epilogue *ep) {
+    return ep ? operands_local({ep->residual, ep->scale, ep->bias}) : TG_OK;
+}
+
 tg_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return TG_OK;
     if (e == cudaErrorMemoryAllocation) return TG_ERR_OUT_OF_MEMORY;
@@ -287,6 +312,8 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda
     DeviceState *dev = nullptr;
     st = device_state(&dev);
     if (st != TG_OK) return st;
+    st = operands_local({c, K > 0 ? a : nullptr, K > 0 ? b : nullptr});
+    if (st != TG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int eo = esize_of(dtype_out);
     if (K == 0)
@@ -309,6 +336,9 @@ tg_status tg_gemm_fused(int64_t M, int64_t N, int64_t K, const void *a, int64_t 
     if (M == 0 || N == 0) return TG_OK;
     DeviceState *dev = nullptr;
     st = device_state(&dev);
+    if (st != TG_OK) return st;
+    st = operands_local({c, K > 0 ? a : nullptr, K > 0 ? b : nullptr});
+    if (st == TG_OK) st = epilogue_local(epilogue);
     if (st != TG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)   // the epilogue of the empty sum
@@ -337,6 +367,8 @@ tg_status tg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
         return tg_gemm_ex(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, stream, opt);
     DeviceState *dev = nullptr;
     st = device_state(&dev);
+    if (st != TG_OK) return st;
+    st = operands_local({c, K > 0 ? a : nullptr, K > 0 ? b : nullptr});
     if (st != TG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int ei = esize_of(dtype_in), eo = esize_of(dtype_out);
@@ -382,6 +414,14 @@ tg_status tg_gemm_strided_batched_fused(int64_t batch, int64_t M, int64_t N, int
                                        stride_c, dtype_in, dtype_out, stream, opt);
     if (batch == 0 || M == 0 || N == 0) return TG_OK;
     const int ei = esize_of(dtype_in), eo = esize_of(dtype_out);
+    {
+        DeviceState *dev = nullptr;
+        st = device_state(&dev);
+        if (st != TG_OK) return st;
+        st = operands_local({c, K > 0 ? a : nullptr, K > 0 ? b : nullptr});
+        if (st == TG_OK) st = epilogue_local(epilogue);
+        if (st != TG_OK) return st;
+    }
     if (K > 0 && batch > 1 && batch_in_one_launch(dtype_in, a, lda, stride_a, b, ldb, stride_b)) {
         DeviceState *dev = nullptr;
         st = device_state(&dev);

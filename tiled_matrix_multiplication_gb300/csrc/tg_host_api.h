@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <initializer_list>
 #include <cstring>
 #include <mutex>
 
@@ -128,6 +129,9 @@ tg_status validate_epilogue(int64_t M, int64_t N, const void *c, int64_t ldc, tg
 
 // tg_api.cu
 tg_status device_state(DeviceState **out);
+// TG_OK if every non-null pointer is device memory of the current device,
+// else TG_ERR_INVALID_VALUE (TG_ERR_CUDA if there is no current device).
+tg_status operands_local(std::initializer_list<const void *> ptrs);
 tg_status cuda_status(cudaError_t e);
 tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                   int64_t ldb, void *c, int64_t ldc, tg_dtype dtype_in, tg_dtype dtype_out,
