@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 8
+#define TG_ABI_VERSION 9
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -103,17 +103,15 @@ typedef struct tg_options {
     int32_t splits;       /* number of K splits (>= 1); the small-M kernel splits K
                              over a cluster of 1, 2, 4 or 8 CTAs */
     int32_t block_n;      /* output tile width: 128, 192, 224 or 256 for the tile
-                             kernels, 128, 256 or 512 for the small-M kernel */
+                             kernels, also 512 for CTA pairs; 128, 256 or 512
+                             for the small-M kernel */
     int32_t group_m;      /* grouped raster height in tiles (default 8) */
     int32_t max_ctas;     /* cap on the persistent grid (default: one per SM) */
     int32_t timeout_ms;   /* bound on every device-side wait (default 2000) */
-    int32_t tail_splits;  /* split each tile of a short last wave over this many K
-                             ranges (2..8; partials summed in the kernel); 0 = no */
     int32_t multicast;    /* 2 = two neighbouring tiles share their A tile by TMA
-                             multicast: clusters of two CTA pairs (192-, 224- or
-                             256-wide tiles), of two single CTAs (128 or 256), or
-                             in the small-M kernel two column tiles (K split over
-                             at most 4); 1 = no sharing; 0 = planner */
+                             multicast inside a cluster of two CTA pairs (192-,
+                             224- or 256-wide tiles; the pair path); 1 = no
+                             sharing; 0 = planner */
     int32_t f32_mode;     /* FP32 operands only (tg_f32_mode): TG_F32_TF32 (0) or
                              TG_F32_3XTF32 (1) */
     int32_t reserved;     /* must be 0 */
@@ -150,16 +148,16 @@ typedef struct tg_plan {
     int32_t ctas;          /* grid size (persistent for the tile kernels) */
     int32_t pack_a;        /* 1 if A is first copied to an aligned workspace */
     int32_t pack_b;        /* 1 if B is first copied to an aligned workspace,
-                              2 if B is first transposed into it (TF32 operands),
-                              3 if B^T is split into TF32 parts (TG_F32_3XTF32;
+                              3 if B is split into TF32 parts (TG_F32_3XTF32;
                               pack_a is then 3 as well) */
-    int32_t c_vector;      /* 1 if C gets 16-byte vector stores */
+    int32_t c_vector;      /* 1 if C's base and row pitch are 16-byte multiples:
+                              the tile kernels then write C with TMA stores
+                              when N x the output size is one too, else with
+                              16-byte vector stores */
     int32_t kernels;       /* kernel launches per call */
     int64_t tiles;         /* work units: output tiles, or groups of `multicast`
                               neighbouring tiles; over all products of a batch */
     int64_t workspace_bytes;
-    int32_t tail_tiles;    /* last tiles split over K to balance the last wave */
-    int32_t tail_splits;   /* K ranges per tail tile (partials summed in-kernel) */
     int32_t multicast;     /* tiles sharing one A tile (1 or 2) */
     int32_t per_batch;     /* strided batches only: 1 if each product of the batch
                               is run as its own call (kernels counts them all), 0
@@ -325,7 +323,7 @@ tg_status tg_gemm_host(int64_t M, int64_t N, int64_t K,
  *                      must not overlap the whole of A or of B.
  *   opt                as for tg_gemm_ex; with batch > 1, opt->splits > 1 is
  *                      only accepted with opt->path == TG_PATH_SKINNY (the
- *                      on-chip K split), and opt->tail_splits is unsupported.
+ *                      on-chip K split).
  *
  * One launch covers every product when the operands are 16-bit, A and B are
  * 16-byte aligned with 16-byte row pitches and 16-byte batch strides.
@@ -432,12 +430,12 @@ int32_t tg_abi_version(void);
  * allocator, or a code path that must not enter the allocator at all.
  *
  *   M, N, K, a, lda, b, ldb, c, ldc, dtype_out, stream  as for tg_gemm
- *   dtype_in   TG_F16 or TG_BF16 (TF32 needs a transposed copy of B: unsupported)
+ *   dtype_in   TG_F16 or TG_BF16
  *   splits     1 .. 128 K ranges; the planner may use fewer when K is short
  *
  * Returns TG_ERR_UNSUPPORTED when splits x M x N x 4 bytes exceeds
  * TG_NOALLOC_SCRATCH_BYTES, when A or B is not 16-byte aligned in base and row
- * pitch (they are read in place), or for TF32 operands; argument errors as for
+ * pitch (they are read in place), or for other operand types; argument errors as for
  * tg_gemm.  The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call outside
  * any stream capture.  Every call on a device shares the one array: calls

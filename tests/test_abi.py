@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert tg.tg_abi_version() == 8
+    assert tg.tg_abi_version() == 9
     assert tg.tg_status_string(tg.TG_OK) == "TG_OK"
     assert tg.tg_status_string(tg.TG_ERR_TIMEOUT) == "TG_ERR_TIMEOUT"
     assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
@@ -99,26 +99,28 @@ def test_plan_square_4096(lib):
     # the resident grid: 74 pairs, or 35 four-CTA clusters when two pairs share A
     assert p["ctas"] == (148 if p["multicast"] == 1 else 4 * (148 * 19 // 80))
     assert p["pack_a"] == 0 and p["pack_b"] == 0 and p["c_vector"] == 1
-    assert p["kernels"] == 1 and p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
+    assert p["kernels"] == 1 and p["workspace_bytes"] == 0
 
 
-def test_plan_tail_split_rules(lib):
-    # 256 tiles on 74 pairs: the 34 tiles of the short last wave split over K
-    st, p = plan(4096, 4096, 4096, sms=148, tail_splits=2)
-    assert st == tg.TG_OK and p["tail_tiles"] == 256 % 74 and p["tail_splits"] == 2
-    assert p["workspace_bytes"] >= p["tail_tiles"] * 2 * 256 * p["block_n"] * 4
-    # a full last wave: nothing to split
-    st, p = plan(8192, 4096, 4096, "bf16", sms=128, tail_splits=4)
-    assert st == tg.TG_OK and p["tiles"] % 64 == 0 and p["tail_tiles"] == 0
-    # a K split replaces the tail split
-    st, p = plan(4096, 4096, 4096, sms=148, splits=2, path=tg.TG_PATH_TC_PAIR, tail_splits=2)
-    assert st == tg.TG_OK and p["tail_tiles"] == 0 and p["splits"] == 2
-    # short K: ranges would be under 8 K tiles
-    st, p = plan(4096, 4096, 256, sms=148, tail_splits=4)
-    assert st == tg.TG_OK and p["tail_tiles"] == 0
-    for bad in (1, 9, -1):
-        st, _ = plan(512, 512, 512, tail_splits=bad)
-        assert st == tg.TG_ERR_INVALID_VALUE
+def test_plan_wide_tiles(lib):
+    # 512-wide tiles: CTA pairs only (two N = 256 MMAs per K step), every
+    # operand type, no A multicast
+    for din, dout in (("f16", "f16"), ("bf16", "f32"), ("e4m3", "f16"), ("f32", "f32")):
+        st, p = plan(4096, 4096, 4096, din, dout, sms=148, path=tg.TG_PATH_TC_PAIR, block_n=512)
+        assert st == tg.TG_OK and p["block_n"] == 512 and p["block_m"] == 256, (din, p)
+        assert p["multicast"] == 1 and p["tiles"] == 16 * 8 and p["stages"] == 4
+    st, p = plan(4096, 4096, 4096, block_n=512, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR
+    for bad in (dict(path=tg.TG_PATH_TC, block_n=512), dict(block_n=512, multicast=2)):
+        st, _ = plan(4096, 4096, 4096, sms=148, **bad)
+        assert st == tg.TG_ERR_UNSUPPORTED, bad
+
+
+def test_plan_tf32_reads_b_in_place(lib):
+    # B is read N-major by the TF32 MMA (32-byte-atom swizzle): no transposed copy
+    st, p = plan(2048, 2048, 2048, "f32", "f32", sms=148)
+    assert st == tg.TG_OK and p["pack_a"] == 0 and p["pack_b"] == 0 and p["kernels"] == 1
+    assert p["workspace_bytes"] == 0
 
 
 def test_plan_config1_needs_pack(lib):
@@ -133,11 +135,12 @@ def test_plan_config1_needs_pack(lib):
 def test_plan_tf32(lib):
     st, p = plan(2048, 2048, 2048, "f32", "f32")
     assert st == tg.TG_OK and p["block_k"] == 32
-    assert p["pack_a"] == 0 and p["pack_b"] == 2          # B^T for the K-major TF32 MMA
-    assert p["workspace_bytes"] >= 2048 * 2048 * 4 and p["kernels"] == 2
+    assert p["pack_a"] == 0 and p["pack_b"] == 0          # B read in place, N-major
+    assert p["workspace_bytes"] == 0 and p["kernels"] == 1
+    # 777 and 1999 floats are not 16-byte pitches: both operands are packed
     st, p = plan(1000, 1999, 777, "f32", "f32")
-    assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 2
-    assert p["workspace_bytes"] >= 1000 * 780 * 4 + 1999 * 780 * 4
+    assert st == tg.TG_OK and p["pack_a"] == 1 and p["pack_b"] == 1
+    assert p["workspace_bytes"] >= 1000 * 780 * 4 + 777 * 2000 * 4
 
 
 @pytest.mark.parametrize("M", [1, 16, 64])
@@ -192,19 +195,16 @@ def test_plan_multicast_rules(lib):
     assert st == tg.TG_OK and p["multicast"] == 2 and p["ctas"] % 4 == 0
     st, p = plan(4096, 4096, 4096, multicast=1, sms=148)
     assert st == tg.TG_OK and p["multicast"] == 1
-    # single CTAs share A in clusters of two (128- or 256-wide tiles); pairs in
-    # clusters of two pairs (192, 224, 256); either may split K
-    st, p = plan(4096, 4096, 4096, multicast=2, path=tg.TG_PATH_TC, sms=148)
-    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC and p["ctas"] % 2 == 0
-    st, p = plan(4096, 4096, 4096, multicast=2, path=tg.TG_PATH_TC, block_n=128, sms=148)
-    assert st == tg.TG_OK and p["block_n"] == 128 and p["multicast"] == 2
-    st, p = plan(128, 8192, 8192, multicast=2, path=tg.TG_PATH_TC, splits=4, sms=148)
-    assert st == tg.TG_OK and p["splits"] == 4 and p["kernels"] == 2
+    # pairs share A in clusters of two pairs (192, 224, 256) and may split K;
+    # a few-row product asked to share A goes to the pair kernel
     st, p = plan(4096, 4096, 4096, multicast=2, splits=2, sms=148)
-    assert st == tg.TG_OK and p["splits"] == 2
-    for bad in (dict(multicast=2, path=tg.TG_PATH_TC, block_n=192),
+    assert st == tg.TG_OK and p["splits"] == 2 and p["multicast"] == 2
+    st, p = plan(64, 8192, 8192, multicast=2, sms=148)
+    assert st == tg.TG_OK and p["path"] == tg.TG_PATH_TC_PAIR and p["multicast"] == 2
+    for bad in (dict(multicast=2, path=tg.TG_PATH_TC), dict(multicast=2, path=tg.TG_PATH_TC,
+                                                             block_n=128),
                 dict(multicast=2, path=tg.TG_PATH_TC_PAIR, block_n=128),
-                dict(multicast=2, tail_splits=2), dict(multicast=2, path=tg.TG_PATH_SKINNY)):
+                dict(multicast=2, block_n=512), dict(multicast=2, path=tg.TG_PATH_SKINNY)):
         st, _ = plan(4096, 4096, 4096, **bad)
         assert st == tg.TG_ERR_UNSUPPORTED, bad
     st, _ = plan(4096, 4096, 4096, multicast=3)
@@ -212,7 +212,7 @@ def test_plan_multicast_rules(lib):
 
 
 def test_plan_width_limits(lib):
-    for bn in (128, 192, 224, 256):
+    for bn in (128, 192, 224, 256, 512):
         st, p = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=bn)
         assert st == tg.TG_OK and p["block_n"] == bn
     st, _ = plan(512, 512, 512, path=tg.TG_PATH_TC_PAIR, block_n=160)

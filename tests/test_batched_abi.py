@@ -43,7 +43,6 @@ def single(M, N, K, din="f16", **opts):
     (dict(sc=0), tg.TG_ERR_INVALID_VALUE),            # every product writes the same C
     (dict(sc=64 * 128 - 1), tg.TG_ERR_INVALID_VALUE),  # last row of C_z meets C_{z+1}
     (dict(batch=2 ** 31), tg.TG_ERR_UNSUPPORTED),
-    (dict(tail_splits=2), tg.TG_ERR_UNSUPPORTED),
     (dict(splits=2), tg.TG_ERR_UNSUPPORTED),           # K split across kernels
     (dict(splits=2, path=tg.TG_PATH_TC_PAIR), tg.TG_ERR_UNSUPPORTED),
     (dict(din="f16", dout="bf16"), tg.TG_ERR_UNSUPPORTED),
@@ -91,7 +90,7 @@ def test_one_launch_counts_tiles_of_every_product():
     assert st == st1 == tg.TG_OK
     assert p["per_batch"] == 0 and p["kernels"] == 1 and p["workspace_bytes"] == 0
     assert p["tiles"] == 16 * p1["tiles"]
-    assert p["splits"] == 1 and p["tail_tiles"] == 0
+    assert p["splits"] == 1
     assert p["ctas"] == 152                           # every pair resident
 
 

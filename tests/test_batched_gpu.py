@@ -196,10 +196,7 @@ def test_bench_batch_32_small_m():
     _sampled_batch_check(32, 64, 8192, 8192, "f16", "f16", "uniform", 64, 13)
 
 
-def test_single_cta_multicast_batched():
-    check_all(3, 300, 520, 256, "f16", "f16", path=tg.TG_PATH_TC, multicast=2, block_n=128)
-
-
-def test_small_m_shared_a_batched():
-    check_all(5, 48, 1100, 640, "f16", "f16", path=tg.TG_PATH_SKINNY, multicast=2, splits=2)
-    check_all(3, 64, 1024, 512, "bf16", "bf16", path=tg.TG_PATH_SKINNY, multicast=2, sa=0)
+def test_wide_tiles_batched():
+    # 512-wide pair tiles over a batch: rank-3 tensor maps for A, B and C
+    check_all(3, 520, 1100, 256, "f16", "f16", path=tg.TG_PATH_TC_PAIR, block_n=512)
+    check_all(4, 300, 600, 300, "bf16", "f32", path=tg.TG_PATH_TC_PAIR, block_n=512, sb=0)

@@ -1,7 +1,8 @@
 """GPU parity of the fused epilogue C = act(alpha * scale * (A B) + bias) +
-beta * R on every kernel path (single CTA, CTA pair, pairs sharing A by
-multicast, the small-M kernel, K split summed by the reduce kernel, tail
-split summed in-kernel, TF32), each activation, with and without residual,
+beta * R on every kernel path (single CTA, CTA pair, 512-wide pair tiles,
+pairs sharing A by multicast, the small-M kernel, K split summed by the
+reduce kernel, TF32; C through TMA stores or the warps' own stores), each
+activation, with and without residual,
 in place (R = C), K = 0, scalar and vector loads of the epilogue operands.
 The oracle's epilogue reference and tolerance (oracle/epilogue.py) decide.
 """
@@ -84,17 +85,15 @@ PATHS = {
     "pair": dict(path=tg.TG_PATH_TC_PAIR, multicast=1, block_n=256),
     "pair_multicast": dict(path=tg.TG_PATH_TC_PAIR, multicast=2, block_n=256),
     "split_k": dict(path=tg.TG_PATH_TC_PAIR, splits=3, multicast=1),
-    "tail_split": dict(path=tg.TG_PATH_TC, block_n=128, max_ctas=10, tail_splits=4),
+    "pair_wide": dict(path=tg.TG_PATH_TC_PAIR, block_n=512),
+    "pair_wide_small_grid": dict(path=tg.TG_PATH_TC_PAIR, block_n=512, max_ctas=2),
 }
 
 
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_paths_and_activations(path, act):
-    M, N, K = (1000, 1000, 1100) if path == "tail_split" else (300, 520, 200)
-    if path == "tail_split":
-        p = tg.plan(M, N, K, "f16", num_sms=152, **PATHS[path])
-        assert p["tail_tiles"] > 0 and p["tail_splits"] >= 2
+    M, N, K = (1000, 1100, 600) if path == "pair_wide_small_grid" else (300, 520, 200)
     run_fused(M, N, K, "f16", "f16", act=act, alpha=0.75, beta=-0.5, **PATHS[path])
 
 
@@ -163,13 +162,9 @@ def test_torch_helper():
     assert ok, rep
 
 
-def test_single_cta_multicast_epilogue():
+def test_epilogue_with_unaligned_c_pitch():
+    # C's pitch is not a 16-byte multiple: the warps store C themselves
     run_fused(300, 1100, 512, "f16", "f16", act="gelu_tanh", alpha=0.5, beta=1.0,
-              path=tg.TG_PATH_TC, multicast=2, block_n=256)
-    run_fused(128, 2048, 2048, "bf16", "bf16", act="silu", beta=0.5,
-              path=tg.TG_PATH_TC, multicast=2, block_n=128, splits=4)
-
-
-def test_small_m_shared_a_epilogue():
-    run_fused(64, 1100, 1024, "f16", "f16", act="silu", alpha=0.5, beta=1.0,
-              path=tg.TG_PATH_SKINNY, multicast=2, splits=4)
+              path=tg.TG_PATH_TC_PAIR, block_n=512, ldc=1103, ldr=1104)
+    run_fused(257, 520, 512, "bf16", "f32", act="silu", beta=0.5,
+              path=tg.TG_PATH_TC, block_n=128, ldc=521)

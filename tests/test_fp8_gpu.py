@@ -24,6 +24,7 @@ VARIANTS = {
     "pair_multicast": dict(path=tg.TG_PATH_TC_PAIR, block_n=256, multicast=2),
     "pair_multicast_224": dict(path=tg.TG_PATH_TC_PAIR, block_n=224, multicast=2),
     "split_k": dict(path=tg.TG_PATH_TC_PAIR, splits=3, multicast=1),
+    "pair_512": dict(path=tg.TG_PATH_TC_PAIR, block_n=512),
 }
 
 
@@ -54,11 +55,9 @@ def test_padded_and_packed_operands(lda, ldb):
     compare(a, b, c, M, N, K, "e4m3", "f32", exact=True)
 
 
-def test_tail_split():
+def test_wide_tiles_small_grid():
     M, N, K = 1000, 1000, 2200
-    opts = dict(path=tg.TG_PATH_TC, block_n=128, max_ctas=10, tail_splits=4)
-    p = tg.plan(M, N, K, "e4m3", "f16", num_sms=152, **opts)
-    assert p["tail_tiles"] > 0
+    opts = dict(path=tg.TG_PATH_TC_PAIR, block_n=512, max_ctas=4)
     a, b, c = run_gemm(M, N, K, "e4m3", "f16", dist="int", **opts)
     compare(a, b, c, M, N, K, "e4m3", "f16", exact=True)
 

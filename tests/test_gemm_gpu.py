@@ -103,13 +103,19 @@ PATHS = {"tc": 1, "pair": 2}
 
 
 @pytest.mark.parametrize("path", ["tc", "pair"])
-@pytest.mark.parametrize("block_n", [128, 192, 224, 256])
+@pytest.mark.parametrize("block_n", [128, 192, 224, 256, 512])
 @pytest.mark.parametrize("din,dout", [("f16", "f16"), ("bf16", "f32"), ("f32", "f32")])
 @pytest.mark.parametrize("M,N,K", [(100, 300, 200), (300, 520, 333), (513, 257, 1000),
                                    (1024, 1024, 64)])
 def test_forced_paths_exact(path, block_n, din, dout, M, N, K):
     """Each kernel variant on its own, with ragged tiles: for a pair, M = 100 leaves
-    the peer CTA's rows entirely out of range and M = 300 leaves a partial peer."""
+    the peer CTA's rows entirely out of range and M = 300 leaves a partial peer.
+    FP32 operands (TF32) read B N-major like the others."""
+    if path == "tc" and block_n == 512:   # pairs only: refused on the host
+        import tiled_matrix_multiplication_gb300 as tg
+        with pytest.raises(tg.TgError):
+            tg.plan(M, N, K, din, dout, num_sms=152, path=1, block_n=512)
+        return
     a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=PATHS[path], block_n=block_n)
     compare(a, b, c, M, N, K, din, dout, exact=True)
 
@@ -187,35 +193,49 @@ def test_skinny_two_ctas_per_sm_exact(M):
 
 
 
-@pytest.mark.parametrize("path,block_n,max_ctas", [(1, 128, 10), (1, 256, 7), (2, 256, 14),
-                                                   (2, 128, 10), (2, 224, 6)])
-@pytest.mark.parametrize("M,N,K", [(1024, 1024, 2048), (1000, 700, 1500), (777, 1500, 4100)])
-def test_tail_split_exact(path, block_n, max_ctas, M, N, K):
-    """A short last wave split over K: partial tiles, last-arriving range sums
-    them (forced by a small CTA budget so that the tail is a few tiles)."""
+@pytest.mark.parametrize("din,dout", [("f16", "f16"), ("bf16", "f32"), ("f32", "f32"),
+                                      ("e4m3", "bf16")])
+@pytest.mark.parametrize("M,N,K,max_ctas", [(256, 512, 192, 0), (300, 1100, 700, 0),
+                                            (1000, 1500, 1000, 4), (2048, 2048, 256, 2),
+                                            (600, 300, 2000, 0)])
+def test_wide_tiles_exact(din, dout, M, N, K, max_ctas):
+    """512-wide pair tiles (two N = 256 MMAs per K step into one 512-column
+    accumulator): ragged M, N and K, a tile whose second MMA's columns lie
+    wholly beyond N (N = 300), and grids of 1-2 pairs that reuse the single
+    accumulator buffer for many tiles."""
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=2, block_n=512, max_ctas=max_ctas)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+
+
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f16", "f32")])
+def test_wide_tiles_uniform(din, dout):
+    M, N, K = 1536, 2560, 1200
+    a, b, c = run_gemm(M, N, K, din, dout, dist="uniform", path=2, block_n=512, ldc=N + 8)
+    compare(a, b, c, M, N, K, din, dout)
+    assert padding_untouched(c, N, dout)
+
+
+@pytest.mark.parametrize("path,block_n", [(1, 128), (1, 224), (2, 256), (2, 512)])
+@pytest.mark.parametrize("dout", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("M,N,ldc_pad", [(200, 300, 8), (257, 1001, 7), (129, 33, 31),
+                                         (513, 700, 0)])
+def test_tma_store_epilogue_edges(path, block_n, dout, M, N, ldc_pad):
+    """C leaves through TMA stores of 32-row boxes when its base, pitch and
+    row length are 16-byte multiples, else through the warps' own stores: both
+    give the oracle's bits on ragged M and N, boxes partly or wholly outside C
+    (the store clips them), and C's padding (poisoned) is never written --
+    also where a row of C ends inside a 16-byte piece (N = 1001, 33), which a
+    TMA store would overwrite up to the next 16-byte boundary."""
     import tiled_matrix_multiplication_gb300 as tg
-    p = tg.plan(M, N, K, "f16", "f16", num_sms=152, path=path, block_n=block_n, max_ctas=max_ctas,
-                tail_splits=8)
-    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=path, block_n=block_n,
-                       max_ctas=max_ctas, tail_splits=8)
-    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
-    a, b, c = run_gemm(M, N, K, "bf16", "f32", dist="uniform", path=path, block_n=block_n,
-                       max_ctas=max_ctas, ldc=N + 4, tail_splits=3)
-    compare(a, b, c, M, N, K, "bf16", "f32")
-    assert padding_untouched(c, N, "f32")
-    assert p["tail_tiles"] >= 0
-
-
-def test_tail_split_is_exercised():
-    """The forced configurations above really do split a tail."""
-    import tiled_matrix_multiplication_gb300 as tg
-    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=1, block_n=128, max_ctas=10,
-                tail_splits=8)
-    assert p["tail_tiles"] == 64 % 10 and p["tail_splits"] >= 2
-    p = tg.plan(1024, 1024, 2048, "f16", num_sms=152, path=2, block_n=256, max_ctas=14,
-                tail_splits=8)
-    assert p["tail_tiles"] == 16 % 7 and p["tail_splits"] >= 2
-
+    din = "bf16" if dout == "bf16" else "f16"
+    K = 300
+    ldc = N + ldc_pad
+    eo = 4 if dout == "f32" else 2
+    p = tg.plan(M, N, K, din, dout, num_sms=152, path=path, block_n=block_n, ldc=ldc)
+    assert p["c_vector"] == int((ldc * eo) % 16 == 0), p
+    a, b, c = run_gemm(M, N, K, din, dout, dist="int", path=path, block_n=block_n, ldc=ldc)
+    compare(a, b, c, M, N, K, din, dout, exact=True)
+    assert padding_untouched(c, N, dout)
 
 
 @pytest.mark.parametrize("block_n", [192, 224, 256])
@@ -238,46 +258,3 @@ def test_multicast_pairs_uniform(din, dout):
                        ldc=N + 8)
     compare(a, b, c, M, N, K, din, dout)
     assert padding_untouched(c, N, dout)
-
-
-@pytest.mark.parametrize("block_n", [128, 256])
-@pytest.mark.parametrize("M,N,K,splits", [(300, 1100, 512, 0), (128, 8192, 2048, 4),
-                                          (513, 640, 300, 2), (130, 2000, 777, 0)])
-def test_single_cta_multicast_exact(block_n, M, N, K, splits):
-    """Clusters of two single CTAs on adjacent tiles sharing A by multicast,
-    with and without a K split; odd tile counts leave a half-empty unit."""
-    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=1, block_n=block_n, multicast=2,
-                       splits=splits)
-    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
-
-
-@pytest.mark.parametrize("din,dout", [("bf16", "f32"), ("e4m3", "bf16"), ("f32", "f32")])
-def test_single_cta_multicast_types(din, dout):
-    a, b, c = run_gemm(300, 1100, 640, din, dout, path=1, block_n=128, multicast=2, ldc=1104)
-    compare(a, b, c, 300, 1100, 640, din, dout)
-    assert padding_untouched(c, 1100, dout)
-
-
-@pytest.mark.parametrize("M", [16, 37, 64, 128])
-@pytest.mark.parametrize("N,K,splits", [(1100, 1000, 4), (1000, 700, 2), (384, 513, 1)])
-def test_skinny_shared_a_exact(M, N, K, splits):
-    """The small-M kernel with A^T shared by two adjacent column tiles
-    (multicast); odd tile counts leave the last CTA of a pair past N."""
-    a, b, c = run_gemm(M, N, K, "f16", "f16", dist="int", path=3, multicast=2, splits=splits)
-    compare(a, b, c, M, N, K, "f16", "f16", exact=True)
-
-
-@pytest.mark.parametrize("din,dout", [("bf16", "f32"), ("e4m3", "f16"), ("e5m2", "bf16")])
-def test_skinny_shared_a_types(din, dout):
-    a, b, c = run_gemm(64, 2100, 1536, din, dout, path=3, multicast=2, ldc=2104)
-    compare(a, b, c, 64, 2100, 1536, din, dout)
-    assert padding_untouched(c, 2100, dout)
-
-
-def test_skinny_shared_a_full_size():
-    # 64 x 8192 x 8192 with two CTAs per SM in clusters of 8 (4 K ranges x 2 tiles)
-    import tiled_matrix_multiplication_gb300 as tg
-    p = tg.plan(64, 8192, 8192, "f16", num_sms=152, path=3, multicast=2)
-    assert p["path"] == tg.TG_PATH_SKINNY and p["multicast"] == 2 and p["ctas"] == 256
-    a, b, c = run_gemm(64, 8192, 8192, "f16", "f16", dist="int", path=3, multicast=2)
-    compare(a, b, c, 64, 8192, 8192, "f16", "f16", exact=True)

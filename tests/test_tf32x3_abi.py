@@ -26,8 +26,8 @@ def test_split_operands_and_three_k():
     st1, p1 = plan(2048, 2048, 2048)
     assert st == st1 == tg.TG_OK
     assert p["pack_a"] == 3 and p["pack_b"] == 3 and p["kernels"] == 3
-    assert p1["pack_a"] == 0 and p1["pack_b"] == 2
-    # A' [M, 3K] and B'^T [N, 3K] in FP32
+    assert p1["pack_a"] == 0 and p1["pack_b"] == 0
+    # A' [M, 3K] and B' [3K, N] in FP32
     assert p["workspace_bytes"] >= (2048 + 2048) * 3 * 2048 * 4
 
 

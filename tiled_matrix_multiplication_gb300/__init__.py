@@ -69,7 +69,7 @@ def gemm(a, b, out_dtype=None, out=None, stream=None, **options):
     column stride (any row stride).  ``out_dtype`` defaults to the input dtype;
     ``out`` may be a preallocated [M, N] tensor with unit column stride.
     ``options`` are tg_options fields (path, splits, block_n, group_m, max_ctas,
-    timeout_ms, tail_splits, multicast, f32_mode).  Raises ``ValueError`` on a
+    timeout_ms, multicast, f32_mode).  Raises ``ValueError`` on a
     shape mismatch and ``TgError`` on any status other than TG_OK.
     """
     import torch

@@ -45,8 +45,8 @@ class tg_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("block_n", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("tail_splits", ctypes.c_int32), ("multicast", ctypes.c_int32),
-                ("f32_mode", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("multicast", ctypes.c_int32), ("f32_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class tg_epilogue(ctypes.Structure):
@@ -64,7 +64,6 @@ class tg_plan(ctypes.Structure):
                 ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
                 ("c_vector", ctypes.c_int32), ("kernels", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("tail_tiles", ctypes.c_int32), ("tail_splits", ctypes.c_int32),
                 ("multicast", ctypes.c_int32), ("per_batch", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
@@ -141,10 +140,10 @@ TG_F32_TF32, TG_F32_3XTF32 = 0, 1
 
 
 def make_options(path=0, splits=0, block_n=0, group_m=0, max_ctas=0, timeout_ms=0,
-                 tail_splits=0, multicast=0, f32_mode=0):
+                 multicast=0, f32_mode=0):
     o = tg_options()
     o.path, o.splits, o.block_n, o.group_m = path, splits, block_n, group_m
-    o.max_ctas, o.timeout_ms, o.tail_splits = max_ctas, timeout_ms, tail_splits
+    o.max_ctas, o.timeout_ms = max_ctas, timeout_ms
     o.multicast, o.f32_mode, o.reserved = multicast, f32_mode, 0
     return o
 

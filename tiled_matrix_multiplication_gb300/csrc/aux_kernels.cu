@@ -1,4 +1,4 @@
-// aux_kernels.cu -- the two memory-bound helper kernels of the GEMM path.
+// aux_kernels.cu -- the memory-bound helper kernels of the GEMM path.
 //
 // pack_rows: copies a row-major block whose base or row pitch is not
 //   16-byte aligned into a workspace with an aligned pitch.  The tensor-memory
@@ -6,8 +6,8 @@
 //   ("Matrix Multiplication", section "The real tiled loop") imposes exactly
 //   this alignment on its source; the padded columns are never read because
 //   the descriptor's logical width stays the original one.
-// pack_transpose: writes B^T ([N, K], K contiguous) into the workspace for
-//   operand types whose MMA wants B K-major.
+// split3_rows / split3_stack: the TF32 hi / lo parts of FP32 operands for the
+//   3xTF32 mode.
 // splitk_reduce: C[m,n] = round(epilogue(sum_{s=0}^{S-1} P[s,m,n])) in increasing s --
 //   the K-chunk sum of the lesson-6 walk-through ("the accumulator must survive
 //   both steps"), finished across work units instead of inside one.
@@ -47,49 +47,6 @@ __global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *_
     }
 }
 
-// dst[c * ld_dst + r] = src[r * ld_src + c] for a rows x cols block.  One
-// block per 32-row x 128-column tile (four 32 x 32 shared-memory sub-tiles,
-// padded against bank conflicts): each thread issues its 16 loads before any
-// store, so a warp keeps 16 row segments of 128 bytes in flight, and both the
-// reads of src and the writes of dst are whole 128-byte rows.
-constexpr int kTrRows = 32, kTrCols = 128;
-
-template <typename T>
-__global__ void __launch_bounds__(256) pack_transpose_kernel(const T *__restrict__ src,
-                                                             int64_t ld_src, T *__restrict__ dst,
-                                                             int64_t ld_dst, int64_t rows,
-                                                             int64_t cols) {
-    __shared__ T tile[kTrCols / 32][32][33];
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTrRows; r0 < rows;
-         r0 += static_cast<int64_t>(gridDim.y) * kTrRows) {
-    T v[kTrCols / 32][4];
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t r = r0 + ty + 8 * i, c = c0 + 32 * sb + tx;
-            v[sb][i] = (r < rows && c < cols) ? src[r * ld_src + c] : T(0);
-        }
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tile[sb][ty + 8 * i][tx] = v[sb][i];
-    __syncthreads();
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t c = c0 + 32 * sb + ty + 8 * i, r = r0 + tx;
-            if (r < rows && c < cols) dst[c * ld_dst + r] = tile[sb][tx][ty + 8 * i];
-        }
-    __syncthreads();   // the tile is refilled by the next row tile
-    }
-}
-
 // x = hi + lo + r with hi and lo TF32 values (10 fraction bits; the
 // cvt.rna.tf32.f32 instruction: round to nearest, ties away from zero) and
 // |r| <= 2^-11 |lo| <= about 2^-22 |x|; x - hi is exact in FP32.  A non-finite
@@ -125,48 +82,22 @@ __global__ void split3_rows_kernel(const float *__restrict__ a, int64_t lda, flo
     }
 }
 
-// B'^T = [hi(B)^T | hi(B)^T | lo(B)^T], [N, 3K] with pitch ld_dst: the
-// transpose above (32 K rows x 128 N columns per block, 16 loads in flight
-// per thread) with each element split on the way.
-__global__ void __launch_bounds__(256) split3_transpose_kernel(const float *__restrict__ b,
-                                                               int64_t ldb,
-                                                               float *__restrict__ dst,
-                                                               int64_t ld_dst, int64_t K,
-                                                               int64_t N) {
-    __shared__ float hi_t[kTrCols / 32][32][33], lo_t[kTrCols / 32][32][33];
+// B' = [hi(B); hi(B); lo(B)] stacked along K: [3K, N] with pitch ld_dst,
+// read by the TF32 kernel N-major like B itself.
+__global__ void split3_stack_kernel(const float *__restrict__ b, int64_t ldb, float *__restrict__ dst,
+                                    int64_t ld_dst, int64_t K, int64_t N) {
     grid_dependency_wait();
     grid_launch_dependents();
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTrRows; k0 < K;
-         k0 += static_cast<int64_t>(gridDim.y) * kTrRows) {
-    float v[kTrCols / 32][4];
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t k = k0 + ty + 8 * i, n = n0 + 32 * sb + tx;
-            v[sb][i] = (k < K && n < N) ? b[k * ldb + n] : 0.f;
-        }
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            split_tf32(v[sb][i], hi_t[sb][ty + 8 * i][tx], lo_t[sb][ty + 8 * i][tx]);
-    __syncthreads();
-#pragma unroll
-    for (int sb = 0; sb < kTrCols / 32; ++sb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t n = n0 + 32 * sb + ty + 8 * i, k = k0 + tx;
-            if (k < K && n < N) {
-                float *row = dst + n * ld_dst;
-                row[k] = hi_t[sb][tx][ty + 8 * i];
-                row[K + k] = hi_t[sb][tx][ty + 8 * i];
-                row[2 * K + k] = lo_t[sb][tx][ty + 8 * i];
-            }
-        }
-    __syncthreads();   // the tiles are refilled by the next row tile
+    const int64_t total = K * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t k = i / N;
+        const int64_t n = i - k * N;
+        float hi, lo;
+        split_tf32(b[k * ldb + n], hi, lo);
+        dst[k * ld_dst + n] = hi;
+        dst[(K + k) * ld_dst + n] = hi;
+        dst[(2 * K + k) * ld_dst + n] = lo;
     }
 }
 
@@ -279,24 +210,6 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
-                                  int64_t rows, int64_t cols, int esize, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t gx = (cols + kTrCols - 1) / kTrCols;
-    const int64_t gy = std::min<int64_t>((rows + kTrRows - 1) / kTrRows, 65535);   // + row loop
-    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
-    if (esize == 2)
-        return launch_pdl(pack_transpose_kernel<uint16_t>, grid, block, stream,
-                          static_cast<const uint16_t *>(src), ld_src,
-                          static_cast<uint16_t *>(dst), ld_dst, rows, cols);
-    if (esize == 4)
-        return launch_pdl(pack_transpose_kernel<uint32_t>, grid, block, stream,
-                          static_cast<const uint32_t *>(src), ld_src,
-                          static_cast<uint32_t *>(dst), ld_dst, rows, cols);
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream) {
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
     return cudaGetLastError();
@@ -311,16 +224,13 @@ cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld
                       K);
 }
 
-cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
-                                    int64_t K, int64_t N, cudaStream_t stream) {
+cudaError_t launch_split3_stack(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
+                                int64_t K, int64_t N, cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
-    const int64_t gx = (N + kTrCols - 1) / kTrCols;
-    const int64_t gy = std::min<int64_t>((K + kTrRows - 1) / kTrRows, 65535);   // + row loop
-    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    return launch_pdl(split3_transpose_kernel,
-                      dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8),
-                      stream, static_cast<const float *>(b), ldb, static_cast<float *>(dst),
-                      ld_dst, K, N);
+    const int threads = 256;
+    return launch_pdl(split3_stack_kernel, dim3(grid_for(K * N, threads)), dim3(threads), stream,
+                      static_cast<const float *>(b), ldb, static_cast<float *>(dst), ld_dst, K,
+                      N);
 }
 
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N, void *c,

@@ -33,8 +33,9 @@ cudaError_t set_smem_once(const void *kern, int bytes) {
     return e;
 }
 
-bool tc_supported_block_n(int block_n, bool pair) {
-    (void)pair;
+bool tc_supported_block_n(int in_kind, int block_n, bool pair) {
+    (void)in_kind;
+    if (block_n == 512) return pair;
     return block_n == 128 || block_n == 192 || block_n == 224 || block_n == 256;
 }
 
@@ -56,30 +57,32 @@ int tc_stages(int in_kind, int block_n, bool pair) {
 
 int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair) {
     const int es = in_esize(in_kind);
-    const int cols = pair ? block_n / 2 : block_n;
+    if (in_kind == IN_TF32) return 128;                       // 32-byte-atom swizzle
+    const int mma_n = block_n > 256 ? 256 : block_n;          // N of one MMA
+    const int cols = pair ? mma_n / 2 : mma_n;                // its B columns per CTA
     return ((cols * es) % 128 != 0 && (cols * es) % 64 == 0) ? 64 : 128;
 }
 
 bool tc_supported_mc(int block_n, int mc, bool pair) {
     if (mc == 1) return true;
     if (mc != 2) return false;
-    return pair ? (block_n == 192 || block_n == 224 || block_n == 256)
-                : (block_n == 128 || block_n == 256);
+    return pair && (block_n == 192 || block_n == 224 || block_n == 256);
 }
 
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
-                           const CUtensorMap &tmB, const TcParams &p, int ctas,
-                           cudaStream_t stream) {
-    if (!tc_supported_mc(block_n, mc, pair)) return cudaErrorInvalidValue;
+                           const CUtensorMap &tmB, const CUtensorMap &tmC, const TcParams &p,
+                           int ctas, cudaStream_t stream) {
+    if (!tc_supported_mc(block_n, mc, pair) || !tc_supported_block_n(in_kind, block_n, pair))
+        return cudaErrorInvalidValue;
     switch (in_kind) {
     case IN_F16:
     case IN_BF16:
-        return launch_gemm_tc_16bit(in_kind, block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_gemm_tc_16bit(in_kind, block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     case IN_TF32:
-        return launch_gemm_tc_tf32(block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_gemm_tc_tf32(block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     case IN_E4M3:
     case IN_E5M2:
-        return launch_gemm_tc_fp8(in_kind, block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_gemm_tc_fp8(in_kind, block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     default: return cudaErrorInvalidValue;
     }
 }

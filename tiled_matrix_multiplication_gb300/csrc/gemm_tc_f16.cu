@@ -7,11 +7,12 @@ namespace tg {
 
 cudaError_t launch_gemm_tc_16bit(int in_kind, int block_n, bool pair, int mc,
                                  const CUtensorMap &tmA, const CUtensorMap &tmB,
-                                 const TcParams &p, int ctas, cudaStream_t stream) {
+                                 const CUtensorMap &tmC, const TcParams &p, int ctas,
+                                 cudaStream_t stream) {
     if (in_kind == IN_F16)
-        return launch_variant<IN_F16>(block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_variant<IN_F16>(block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     if (in_kind == IN_BF16)
-        return launch_variant<IN_BF16>(block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_variant<IN_BF16>(block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     return cudaErrorInvalidValue;
 }
 

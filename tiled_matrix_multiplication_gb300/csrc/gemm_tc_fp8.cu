@@ -6,11 +6,12 @@ namespace tg {
 
 cudaError_t launch_gemm_tc_fp8(int in_kind, int block_n, bool pair, int mc,
                                const CUtensorMap &tmA, const CUtensorMap &tmB,
-                               const TcParams &p, int ctas, cudaStream_t stream) {
+                               const CUtensorMap &tmC, const TcParams &p, int ctas,
+                               cudaStream_t stream) {
     if (in_kind == IN_E4M3)
-        return launch_variant<IN_E4M3>(block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_variant<IN_E4M3>(block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     if (in_kind == IN_E5M2)
-        return launch_variant<IN_E5M2>(block_n, pair, mc, tmA, tmB, p, ctas, stream);
+        return launch_variant<IN_E5M2>(block_n, pair, mc, tmA, tmB, tmC, p, ctas, stream);
     return cudaErrorInvalidValue;
 }
 

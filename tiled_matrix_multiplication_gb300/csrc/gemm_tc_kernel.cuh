@@ -23,34 +23,42 @@
 //   * acc = dot(a, b, acc) on the tensor cores, accumulator on chip for the
 //     whole K loop
 //       -> one thread issues tcgen05.mma into an FP32 accumulator in tensor
-//          memory (128 lanes x BN columns per CTA), double buffered so the
-//          epilogue of tile i overlaps the main loop of tile i+1;
-//   * cast and masked store of the tile, written once
+//          memory (128 lanes x BN columns per CTA), double buffered up to 256
+//          columns so the epilogue of tile i overlaps the main loop of tile i+1;
+//   * cast and store of the tile through its output descriptor, written once
 //       -> four epilogue warps read the accumulator with tcgen05.ld, round to
-//          the output type and store only in-range rows and columns.
+//          the output type, stage 32-row boxes in shared memory and write them
+//          with TMA stores, which leave out everything outside C ("The real
+//          tiled loop": the result leaves through the output descriptor).
+//          Where C's base or row pitch is not 16-byte aligned, or for split-K
+//          partials, the warps store their rows directly instead.
 //   * Split-K (several work units per tile, each over a K range) writes FP32
 //     partial tiles that a separate kernel sums in a fixed order.
 //
-// Two variants:
+// Variants:
 //   PAIR = false: one CTA owns a 128 x BN tile (tcgen05 cta_group::1).
 //   PAIR = true : a cluster of two CTAs owns a 256 x BN tile (cta_group::2).
-//     Each CTA loads its own 128 rows of A and half (BN/2 columns) of B; the
-//     leader CTA (rank 0) issues the MMAs, which read A and B from both CTAs'
-//     shared memory and leave rows 0..127 of the accumulator in the leader's
-//     tensor memory and rows 128..255 in the peer's.  Per SM this halves the
-//     B bytes that have to be staged per FLOP.
+//     Each CTA loads its own 128 rows of A and half of the B columns of every
+//     MMA; the leader CTA (rank 0) issues the MMAs, which read A and B from
+//     both CTAs' shared memory and leave rows 0..127 of the accumulator in the
+//     leader's tensor memory and rows 128..255 in the peer's.  Per SM this
+//     halves the B bytes that have to be staged per FLOP.
 //     Synchronisation of the pair:
 //       full[s]   leader's only: one arrive (leader, expect_tx of both CTAs'
 //                 bytes) + the TMA completions of both CTAs;
 //       empty[s]  in both CTAs: the leader's MMA commit, multicast to both;
 //       tfull[b]  in both CTAs: the leader's commit after a tile's last MMA;
 //       tempty[b] leader's only: one arrive per epilogue warp of both CTAs.
-//   MC = 2 (with PAIR): a cluster of two pairs works on two horizontally
-//     adjacent tiles, which read the same A rows.  Each CTA loads half of its
-//     128 rows of A and multicasts them to the CTA in the same position of the
-//     other pair, so A is read from L2 once per two pairs.  A stage may then
-//     be refilled only after both pairs' MMAs are done with it: empty[s]
-//     counts one commit from each pair leader.
+//   BN = 512 (pairs only): two N = 256 MMAs per K step on one A tile, into
+//     the two halves of a 512-column accumulator that fills the tensor memory
+//     (one accumulator buffer); a stage then holds 48 bytes per SM-clock of MMA
+//     work instead of the 64 of a 256-wide pair tile.
+//   MC = 2 (pairs, BN <= 256): a cluster of two pairs works on two
+//     horizontally adjacent tiles, which read the same A rows.  Each CTA loads
+//     half of its 128 rows of A and multicasts them to the CTA in the same
+//     position of the other pair, so A is read from L2 once per two pairs.  A
+//     stage may then be refilled only after both pairs' MMAs are done with it:
+//     empty[s] counts one commit from each pair leader.
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = epilogue (warp w may read TMEM lanes 32*(w%4) .. +31).
@@ -76,20 +84,38 @@ namespace tg {
 namespace {
 
 constexpr int kThreads = 192;
-// Dynamic shared memory for the stage ring: the 227 KB a CTA may use, less
-// the alignment slack and the barriers.
+// Dynamic shared memory for the stage ring and the output staging: the
+// 227 KB a CTA may use, less the alignment slack and the barriers.
 constexpr int kSmemBudget = 232448 - 1024 - 256;
+// Output staging: per epilogue warp, kOutBufs boxes of 32 rows x 64 bytes
+// (32 columns of a 16-bit type or 16 of FP32), 64-byte swizzled.
+constexpr int kOutBox = 32 * 64;
+constexpr int kOutBufs = 4;
+constexpr int kOutStaging = 4 * kOutBufs * kOutBox;
 
 template <int IN_KIND, int BN, bool PAIR, int MC = 1>
 struct TcCfg {
     static constexpr int ESIZE = in_esize(IN_KIND);
     static constexpr int BK = 128 / ESIZE;        // one 128-byte swizzle row of K
     static constexpr int UMMA_K = 32 / ESIZE;     // K of one tcgen05.mma
-    // N-major B: 128-byte swizzled rows, or 64-byte ones when those tile the
-    // CTA's columns exactly and 128-byte ones do not (96 columns per CTA); 32-byte
-    // rows measured much slower than loading a partly unused 128-byte box.
-    static constexpr int BN_CTA_ = PAIR ? BN / 2 : BN;
-    static constexpr int B_SW = ((BN_CTA_ * ESIZE) % 128 != 0 && (BN_CTA_ * ESIZE) % 64 == 0) ? 64 : 128;
+    static constexpr int CTA_GROUP = PAIR ? 2 : 1;
+    static constexpr int CLUSTER = CTA_GROUP * MC;      // CTAs per cluster
+    static constexpr int CTA_M = 128;             // accumulator rows held by one CTA
+    static constexpr int TILE_M = PAIR ? 256 : 128;
+    // N of one MMA; a 512-wide tile issues two per K step
+    static constexpr int MMA_N = BN > 256 ? 256 : BN;
+    static constexpr int N_MMAS = BN / MMA_N;
+    static constexpr int MMA_N_CTA = PAIR ? MMA_N / 2 : MMA_N;   // B columns of one MMA per CTA
+    static constexpr int BN_CTA = N_MMAS * MMA_N_CTA;            // B columns staged by one CTA
+    // B is read N-major, straight from row-major memory, for every operand
+    // type.  TF32 (4-byte elements) takes 128-byte rows swizzled in 32-byte
+    // atoms (smem_desc_mn_tf32).  16-bit and 8-bit operands take 128-byte
+    // swizzled rows, or 64-byte ones when those tile the CTA's columns of one
+    // MMA exactly and 128-byte ones do not (96 columns per CTA); 32-byte rows
+    // measured much slower than loading a partly unused 128-byte box.
+    static constexpr bool B_TF32 = IN_KIND == IN_TF32;
+    static constexpr int B_SW =
+        (!B_TF32 && (MMA_N_CTA * ESIZE) % 128 != 0 && (MMA_N_CTA * ESIZE) % 64 == 0) ? 64 : 128;
     static constexpr int CHUNK_N = B_SW / ESIZE;  // N elements in one B row of a box
     // 0: kind::f16, 1: kind::tf32, 2: kind::f8f6f4
     static constexpr int KIND = IN_KIND == IN_TF32 ? 1 : (ESIZE == 1 ? 2 : 0);
@@ -97,43 +123,41 @@ struct TcCfg {
     // kind::f16, tf32 2, and e4m3 0 / e5m2 1 under kind::f8f6f4
     static constexpr uint32_t FMT = IN_KIND == IN_TF32 ? 2u
                                     : (IN_KIND == IN_BF16 || IN_KIND == IN_E5M2) ? 1u : 0u;
-    static constexpr int CTA_GROUP = PAIR ? 2 : 1;
-    static constexpr int CLUSTER = CTA_GROUP * MC;      // CTAs per cluster
-    static constexpr int CTA_M = 128;             // accumulator rows held by one CTA
-    static constexpr int TILE_M = PAIR ? 256 : 128;
-    static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
-    // B operand layout in shared memory.  16-bit and 8-bit operands are
-    // consumed N-major, straight from row-major B.  kind::tf32 is given a
-    // K-major B (the host transposes B into the workspace first): N-major B
-    // tiles gave wrong products with kind::tf32 on this hardware (all zeros
-    // with one descriptor variant; with the N-major descriptors that are exact
-    // for FP16 and FP8, errors of 10-20 % of sum |a b|).
-    static constexpr bool B_KMAJOR = IN_KIND == IN_TF32;
     static constexpr int A_STAGE = CTA_M * 128;   // bytes
     static constexpr int B_BOX = BK * B_SW;       // one CHUNK_N-wide N-major TMA box
-    static constexpr int B_CHUNKS = (BN_CTA + CHUNK_N - 1) / CHUNK_N;   // last may run past
-    // N-major: B_CHUNKS boxes; K-major (TF32): BN_CTA rows of 128 bytes.
-    static constexpr int B_STAGE = B_KMAJOR ? BN_CTA * 128 : B_CHUNKS * B_BOX;
+    // boxes per MMA (the last may run past the MMA's columns)
+    static constexpr int CHUNKS_PER_MMA = (MMA_N_CTA + CHUNK_N - 1) / CHUNK_N;
+    static constexpr int B_CHUNKS = N_MMAS * CHUNKS_PER_MMA;
+    static constexpr int B_MMA_STRIDE = CHUNKS_PER_MMA * B_BOX;  // bytes between MMAs' B
+    static constexpr int B_STAGE = B_CHUNKS * B_BOX;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
     static constexpr int TX_BYTES = STAGE_BYTES * CTA_GROUP;   // per full-barrier phase
-    static constexpr int STAGES = kSmemBudget / STAGE_BYTES > 8 ? 8 : kSmemBudget / STAGE_BYTES;
-    static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;   // TMEM columns per buffer
-    static constexpr int TMEM_COLS = 2 * ACC_STRIDE;           // two accumulator buffers
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int STAGES_FIT = (kSmemBudget - kOutStaging) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int ACC_STRIDE = BN <= 128 ? 128 : (BN <= 256 ? 256 : 512);  // TMEM columns
+    static constexpr int NUM_ACC = ACC_STRIDE == 512 ? 1 : 2;  // accumulator buffers
+    static constexpr int TMEM_COLS = NUM_ACC * ACC_STRIDE;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int SMEM_BYTES =
+        1024 + STAGES * STAGE_BYTES + kOutStaging + NUM_BARS * 8 + 16;
     static constexpr uint32_t IDESC =
-        make_idesc(FMT, 0u, B_KMAJOR ? 0u : 1u, TILE_M, BN);
+        make_idesc(FMT, 0u, 1u, TILE_M, MMA_N);
     static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
-    static_assert(BN_CTA % 16 == 0, "each CTA stages whole 16-column groups of B");
+    static_assert(MMA_N_CTA % 16 == 0, "each CTA stages whole 16-column groups of B");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM alloc size");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-    static_assert(MC == 1 || MC == 2, "A is shared by at most two tiles");
+    static_assert(STAGES >= 2, "a ring needs two stages");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM alloc size");
+    static_assert(MMA_N % 16 == 0 && MMA_N >= 16 && MMA_N <= 256, "MMA N");
+    static_assert(BN <= 256 || (PAIR && BN == 512 && MC == 1),
+                  "512-wide tiles: CTA pairs without multicast");
+    // one MMA reads K rows kk*UMMA_K .. +UMMA_K-1 of each of its boxes: in bounds
+    static_assert((BK / UMMA_K) * UMMA_K * B_SW <= B_BOX, "MMA reads stay inside the box");
+    static_assert(MC == 1 || (MC == 2 && PAIR), "A is shared by two CTA pairs at most");
 };
 
 struct Work {
     int tm, tn, split, kt0, kt1;
-    int tail;   // index among the tail-split tiles, or -1
     int z;      // batch index
 };
 
@@ -147,30 +171,20 @@ __device__ __forceinline__ int units_per_batch(const TcParams &p) {
 }
 
 __device__ __forceinline__ int total_units(const TcParams &p) {
-    return p.tail_tiles > 0 ? p.tail_start + p.tail_tiles * p.tail_splits
-                            : units_per_batch(p) * p.batch;
+    return units_per_batch(p) * p.batch;
 }
 
 // `q`: which tile of a multicast unit this CTA's pair works on.
 __device__ __forceinline__ Work decode_work(const TcParams &p, int w, int q = 0) {
     Work r;
-    int t;
     r.z = 0;
-    if (p.batch > 1) {   // batches are the slowest dimension (no tail split)
+    if (p.batch > 1) {   // batches are the slowest dimension
         const int per = units_per_batch(p);
         r.z = w / per;
         w -= r.z * per;
     }
-    if (p.tail_tiles > 0 && w >= p.tail_start) {
-        const int u = w - p.tail_start;
-        r.tail = u / p.tail_splits;
-        r.split = u - r.tail * p.tail_splits;
-        t = p.tail_start + r.tail;
-    } else {
-        t = w / p.splits;
-        r.split = w - t * p.splits;
-        r.tail = -1;
-    }
+    const int t = w / p.splits;
+    r.split = w - t * p.splits;
     const int per_group = p.group_m * unit_cols(p);
     const int g = t / per_group;
     const int first_m = g * p.group_m;
@@ -178,17 +192,14 @@ __device__ __forceinline__ Work decode_work(const TcParams &p, int w, int q = 0)
     const int pos = t - g * per_group;
     r.tm = first_m + pos % size_m;
     r.tn = (pos / size_m) * p.mc + q;
-    const int kps = r.tail >= 0 ? p.tail_kps : p.k_tiles_per_split;
-    r.kt0 = r.split * kps;
-    r.kt1 = min(r.kt0 + kps, p.k_tiles);
+    r.kt0 = r.split * p.k_tiles_per_split;
+    r.kt1 = min(r.kt0 + p.k_tiles_per_split, p.k_tiles);
     return r;
 }
 
-__device__ __forceinline__ void epilogue_bar_sync() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-}
-
-// Store 32 consecutive accumulator values (columns col .. col+31 of `row`).
+// Store 32 consecutive accumulator values (columns col .. col+31 of `row`)
+// straight from registers: the split-K partials, and C where its base or row
+// pitch rules out TMA stores.
 __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int row, int col,
                                             uint32_t (&r)[32], int z = 0) {
     const int ncols = min(32, p.N - col);
@@ -247,13 +258,27 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
     }
 }
 
+// Writes 16 bytes (four 32-bit words) as chunk `chunk` (0..3) of this lane's
+// 64-byte row of an output staging box, with the 64-byte swizzle a TMA store
+// of that box expects (16-byte chunk index XOR address bits 7..8).  Eight
+// consecutive lanes hit eight different 16-byte bank groups.
+__device__ __forceinline__ void stage_chunk(uint32_t box, int lane, int chunk, uint32_t a,
+                                            uint32_t b, uint32_t c, uint32_t d) {
+    const uint32_t addr = box + static_cast<uint32_t>(lane) * 64u +
+                          (static_cast<uint32_t>(chunk ^ ((lane >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 template <int IN_KIND, int BN, bool PAIR, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     using Cfg = TcCfg<IN_KIND, BN, PAIR, MC>;
     constexpr int S = Cfg::STAGES;
     constexpr int CG = Cfg::CTA_GROUP;
+    constexpr int NACC = Cfg::NUM_ACC;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -261,17 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t sA = base;                            // S x A_STAGE
     const uint32_t sB = base + S * Cfg::A_STAGE;         // S x B_STAGE
-    const uint32_t bars = sB + S * Cfg::B_STAGE;
+    const uint32_t sOut = sB + S * Cfg::B_STAGE;         // output staging boxes
+    const uint32_t bars = sOut + kOutStaging;
     uint8_t *gbars = gbase + (bars - base);
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * S + b); };
-    auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
-    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * S + NACC + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 2 * NACC);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbars + 8 * Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ int never_abort;
-    __shared__ int tail_last;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -289,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), MC);   // one MMA commit per pair sharing the stage
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4 * CG);
         }
@@ -301,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        if (p.c_tma) tma_prefetch_map(&tmC);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
@@ -328,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = unit0; w < total && ok; w += unit_step) {
                 const Work wk = decode_work(p, w, q);
                 const int row0 = wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M;
-                const int col0 = wk.tn * BN + static_cast<int>(rank) * Cfg::BN_CTA;
+                // this CTA's B columns of MMA 0; MMA h adds h * MMA_N
+                const int colb = wk.tn * BN + static_cast<int>(rank) * Cfg::MMA_N_CTA;
                 for (int kt = wk.kt0; kt < wk.kt1; ++kt) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
                         ok = false;
@@ -358,29 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
                         const uint32_t dst = sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2);
                         const int ya = row0 + q * (Cfg::CTA_M / 2);
-                        if constexpr (PAIR) {
-                            if (p.a_batched)
-                                tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
-                            else
-                                tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
-                        } else {
-                            if (p.a_batched)
-                                tma_load_3d_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
-                            else
-                                tma_load_2d_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
-                        }
+                        if (p.a_batched)
+                            tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
+                        else
+                            tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
                     } else {
                         load(sA + stage * Cfg::A_STAGE, &tmA, p.a_batched, kt * Cfg::BK, row0);
                     }
-                    if constexpr (Cfg::B_KMAJOR) {
-                        // B^T tile [BN_CTA rows of N] x [BK of K], one box
-                        load(sB + stage * Cfg::B_STAGE, &tmB, p.b_batched, kt * Cfg::BK, col0);
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < Cfg::B_CHUNKS; ++j)
-                            load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB, p.b_batched,
-                                 col0 + j * Cfg::CHUNK_N, kt * Cfg::BK);
-                    }
+                    for (int j = 0; j < Cfg::B_CHUNKS; ++j)
+                        load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB, p.b_batched,
+                             colb + (j / Cfg::CHUNKS_PER_MMA) * Cfg::MMA_N +
+                                 (j % Cfg::CHUNKS_PER_MMA) * Cfg::CHUNK_N,
+                             kt * Cfg::BK);
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -416,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int w = unit0; w < total && ok; w += unit_step) {
                 const Work wk = decode_work(p, w, q);
-                const uint32_t buf = acc_count & 1u;
-                const uint32_t acc_phase = (acc_count >> 1) & 1u;
+                const uint32_t buf = NACC == 2 ? (acc_count & 1u) : 0u;
+                const uint32_t acc_phase = NACC == 2 ? ((acc_count >> 1) & 1u) : (acc_count & 1u);
                 if (!mbar_wait<PAIR>(tempty_bar(buf), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -435,18 +452,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            Cfg::B_KMAJOR
-                                ? smem_desc_sw128(b0 + kk * 32, 16, 1024)
-                                : smem_desc_mn<Cfg::B_SW>(b0 + kk * Cfg::UMMA_K * Cfg::B_SW,
-                                                          Cfg::B_BOX);
-                        umma_ss<Cfg::KIND, CG>(d_tmem, ad, bd, Cfg::IDESC,
-                                               (kt > wk.kt0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < Cfg::N_MMAS; ++h) {
+                            const uint32_t bs =
+                                b0 + h * Cfg::B_MMA_STRIDE + kk * Cfg::UMMA_K * Cfg::B_SW;
+                            const uint64_t bd = Cfg::B_TF32
+                                                    ? smem_desc_mn_tf32(bs, Cfg::B_BOX)
+                                                    : smem_desc_mn<Cfg::B_SW>(bs, Cfg::B_BOX);
+                            umma_ss<Cfg::KIND, CG>(d_tmem + h * Cfg::MMA_N, ad, bd, Cfg::IDESC,
+                                                   (kt > wk.kt0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     if constexpr (PAIR)   // every CTA whose stage this pair read from
                         umma_commit_pair(empty_bar(stage), MC == 2 ? 0xF : 0x3);
-                    else if constexpr (MC == 2)   // both CTAs filled this stage's A
-                        umma_commit_mc(empty_bar(stage), 0x3);
                     else
                         umma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -477,11 +495,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
+        const bool f32_out = p.out_kind == OUT_F32;
+        // this warp's staging boxes; boxes are used round-robin, and a box is
+        // rewritten only after the TMA store issued kOutBufs boxes earlier has
+        // finished reading it
+        const uint32_t my_boxes = sOut + static_cast<uint32_t>(quad * kOutBufs * kOutBox);
+        uint32_t nbox = 0;
+        auto next_box = [&]() {
+            if (nbox >= kOutBufs) {
+                if (lane == 0) bulk_wait_group_read<kOutBufs - 1>();
+                __syncwarp();
+            }
+            return my_boxes + (nbox % kOutBufs) * kOutBox;
+        };
+        auto store_box = [&](uint32_t box, int x, int y, int z, bool in_range) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (in_range) {
+                    if (p.batch > 1)
+                        tma_store_3d(&tmC, box, x, y, z);
+                    else
+                        tma_store_2d(&tmC, box, x, y);
+                }
+                bulk_commit_group();
+            }
+            ++nbox;
+        };
         uint32_t acc_count = 0;
         for (int w = unit0; w < total; w += unit_step) {
             const Work wk = decode_work(p, w, q);
-            const uint32_t buf = acc_count & 1u;
-            const uint32_t acc_phase = (acc_count >> 1) & 1u;
+            const uint32_t buf = NACC == 2 ? (acc_count & 1u) : 0u;
+            const uint32_t acc_phase = NACC == 2 ? ((acc_count >> 1) & 1u) : (acc_count & 1u);
             const bool got = mbar_wait<PAIR>(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
@@ -489,33 +534,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int trow = static_cast<int>(rank) * Cfg::CTA_M + quad * 32 + lane;  // in tile
-            const int row = wk.tm * Cfg::TILE_M + trow;
+            const int wrow0 = wk.tm * Cfg::TILE_M + static_cast<int>(rank) * Cfg::CTA_M + quad * 32;
+            const int row = wrow0 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_STRIDE;
-            // tail-split unit: this range's FP32 partial tile, laid out as
-            // [BN/4 column quads][TILE_M rows][4] so that one store or load of
-            // a warp (32 consecutive rows, one column quad) covers 512
-            // contiguous bytes
-            float *ptile = nullptr;
-            if (wk.tail >= 0)
-                ptile = p.tail_partial +
-                        (static_cast<int64_t>(wk.tail) * p.tail_splits + wk.split) * Cfg::TILE_M * BN;
+            const bool tma = p.c_tma != 0;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;
-                if (ptile != nullptr) {
+                if (!tma) {
+                    if (row < p.M && col < p.N) store_chunk(p, wk.split, row, col, r, wk.z);
+                    continue;
+                }
+                const bool in_range = wrow0 < p.M && col < p.N;   // the box holds valid C
+                if (p.epi.on && row < p.M && col < p.N)
+                    epi_chunk32(p.epi, p.out_kind, row, col, min(32, p.N - col), r, wk.z);
+                if (f32_out) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<uint4 *>(
-                            ptile + ((static_cast<int64_t>(c0 + j) >> 2) * Cfg::TILE_M + trow) * 4) =
-                            make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
-                } else if (row < p.M && col < p.N) {
-                    store_chunk(p, wk.split, row, col, r, wk.z);
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t box = next_box();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            stage_chunk(box, lane, j, r[16 * half + 4 * j], r[16 * half + 4 * j + 1],
+                                        r[16 * half + 4 * j + 2], r[16 * half + 4 * j + 3]);
+                        store_box(box, col + 16 * half, wrow0, wk.z,
+                                  in_range && col + 16 * half < p.N);
+                    }
+                } else {
+                    const uint32_t box = next_box();
+                    const bool bf = p.out_kind == OUT_BF16;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t h[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            h[t] = bf ? pack_bf162(r[8 * j + 2 * t], r[8 * j + 2 * t + 1])
+                                      : pack_half2(r[8 * j + 2 * t], r[8 * j + 2 * t + 1]);
+                        stage_chunk(box, lane, j, h[0], h[1], h[2], h[3]);
+                    }
+                    store_box(box, col, wrow0, wk.z, in_range);
                 }
             }
+            // every tcgen05.ld of this accumulator has completed (each waited):
+            // hand the buffer back to the MMA issuer; the TMA stores still in
+            // flight read shared memory only
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -524,52 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_arrive(tempty_bar(buf));
             }
-            if (wk.tail >= 0) {
-                // The range that completes the tile last sums all ranges'
-                // partials, in range order, and writes C.  No range waits for
-                // another, so the order in which ranges run does not matter.
-                epilogue_bar_sync();                 // this CTA's partial rows written
-                if (threadIdx.x == 64) {
-                    __threadfence();
-                    const unsigned int old =
-                        atomicAdd(p.tail_count + wk.tail * Cfg::CTA_GROUP + rank, 1u);
-                    tail_last = (old == static_cast<unsigned int>(p.tail_splits - 1)) ? 1 : 0;
-                    __threadfence();
-                }
-                epilogue_bar_sync();
-                if (tail_last && row < p.M) {
-                    const float *base = p.tail_partial +
-                                        static_cast<int64_t>(wk.tail) * p.tail_splits * Cfg::TILE_M * BN;
-                    const int64_t split_stride = static_cast<int64_t>(Cfg::TILE_M) * BN;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < BN; c0 += 32) {
-                        const int col = wk.tn * BN + c0;
-                        if (col >= p.N) break;
-                        float acc[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-                        for (int sidx = 0; sidx < p.tail_splits; ++sidx) {
-                            const float *src = base + sidx * split_stride;
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                    src + ((static_cast<int64_t>(c0 + j) >> 2) * Cfg::TILE_M + trow) * 4));
-                                acc[j] += v.x;
-                                acc[j + 1] += v.y;
-                                acc[j + 2] += v.z;
-                                acc[j + 3] += v.w;
-                            }
-                        }
-                        uint32_t r[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
-                        store_chunk(p, 0, row, col, r);
-                    }
-                }
-                epilogue_bar_sync();                 // tail_last is reused by the next unit
-            }
             ++acc_count;
         }
+        // the stores of this warp are complete (global writes done, staging
+        // no longer read) before the CTA exits
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -589,8 +613,8 @@ struct ClusterCache {
 };
 
 template <int IN_KIND, int BN, bool PAIR, int MC>
-cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const TcParams &p,
-                        int ctas, cudaStream_t stream) {
+cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                        const TcParams &p, int ctas, cudaStream_t stream) {
     using Cfg = TcCfg<IN_KIND, BN, PAIR, MC>;
     auto kern = gemm_tc_kernel<IN_KIND, BN, PAIR, MC>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES);
@@ -632,43 +656,49 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tc
     } else {
         cfg.gridDim = dim3(ctas, 1, 1);
     }
-    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// 512-wide tiles exist for CTA pairs (every operand type).
+template <int IN_KIND>
+constexpr bool has_wide_tile() {
+    return true;
+}
+
 template <int IN_KIND, bool PAIR, int MC>
 cudaError_t launch_kind(int block_n, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const TcParams &p, int ctas, cudaStream_t stream) {
+                        const CUtensorMap &tmC, const TcParams &p, int ctas, cudaStream_t stream) {
     if constexpr (MC == 2 && PAIR) {
         switch (block_n) {
-        case 192: return launch_impl<IN_KIND, 192, true, 2>(tmA, tmB, p, ctas, stream);
-        case 224: return launch_impl<IN_KIND, 224, true, 2>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, true, 2>(tmA, tmB, p, ctas, stream);
-        default: return cudaErrorInvalidValue;
-        }
-    } else if constexpr (MC == 2) {
-        switch (block_n) {
-        case 128: return launch_impl<IN_KIND, 128, false, 2>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, false, 2>(tmA, tmB, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, true, 2>(tmA, tmB, tmC, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, true, 2>(tmA, tmB, tmC, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, true, 2>(tmA, tmB, tmC, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
     } else if constexpr (PAIR) {
         switch (block_n) {
-        case 128: return launch_impl<IN_KIND, 128, true, 1>(tmA, tmB, p, ctas, stream);
-        case 192: return launch_impl<IN_KIND, 192, true, 1>(tmA, tmB, p, ctas, stream);
-        case 224: return launch_impl<IN_KIND, 224, true, 1>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, true, 1>(tmA, tmB, p, ctas, stream);
+        case 128: return launch_impl<IN_KIND, 128, true, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, true, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, true, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, true, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 512:
+            if constexpr (has_wide_tile<IN_KIND>())
+                return launch_impl<IN_KIND, 512, true, 1>(tmA, tmB, tmC, p, ctas, stream);
+            return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;
+        }
+    } else if constexpr (MC == 1) {
+        switch (block_n) {
+        case 128: return launch_impl<IN_KIND, 128, false, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 192: return launch_impl<IN_KIND, 192, false, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 224: return launch_impl<IN_KIND, 224, false, 1>(tmA, tmB, tmC, p, ctas, stream);
+        case 256: return launch_impl<IN_KIND, 256, false, 1>(tmA, tmB, tmC, p, ctas, stream);
         default: return cudaErrorInvalidValue;
         }
     } else {
-        switch (block_n) {
-        case 128: return launch_impl<IN_KIND, 128, false, 1>(tmA, tmB, p, ctas, stream);
-        case 192: return launch_impl<IN_KIND, 192, false, 1>(tmA, tmB, p, ctas, stream);
-        case 224: return launch_impl<IN_KIND, 224, false, 1>(tmA, tmB, p, ctas, stream);
-        case 256: return launch_impl<IN_KIND, 256, false, 1>(tmA, tmB, p, ctas, stream);
-        default: return cudaErrorInvalidValue;
-        }
+        return cudaErrorInvalidValue;
     }
 }
 
@@ -679,6 +709,9 @@ int stages_kind(int block_n) {
     case 192: return TcCfg<IN_KIND, 192, PAIR>::STAGES;
     case 224: return TcCfg<IN_KIND, 224, PAIR>::STAGES;
     case 256: return TcCfg<IN_KIND, 256, PAIR>::STAGES;
+    case 512:
+        if constexpr (PAIR && has_wide_tile<IN_KIND>()) return TcCfg<IN_KIND, 512, true>::STAGES;
+        return 0;
     default: return 0;
     }
 }
@@ -687,13 +720,13 @@ int stages_kind(int block_n) {
 // Kernel variants of one operand type: A-multicast pairs, pairs, single CTAs.
 template <int IN_KIND>
 cudaError_t launch_variant(int block_n, bool pair, int mc, const CUtensorMap &tmA,
-                           const CUtensorMap &tmB, const TcParams &p, int ctas,
-                           cudaStream_t stream) {
+                           const CUtensorMap &tmB, const CUtensorMap &tmC, const TcParams &p,
+                           int ctas, cudaStream_t stream) {
     if (mc == 2)
-        return pair ? launch_kind<IN_KIND, true, 2>(block_n, tmA, tmB, p, ctas, stream)
-                    : launch_kind<IN_KIND, false, 2>(block_n, tmA, tmB, p, ctas, stream);
-    return pair ? launch_kind<IN_KIND, true, 1>(block_n, tmA, tmB, p, ctas, stream)
-                : launch_kind<IN_KIND, false, 1>(block_n, tmA, tmB, p, ctas, stream);
+        return pair ? launch_kind<IN_KIND, true, 2>(block_n, tmA, tmB, tmC, p, ctas, stream)
+                    : cudaErrorInvalidValue;
+    return pair ? launch_kind<IN_KIND, true, 1>(block_n, tmA, tmB, tmC, p, ctas, stream)
+                : launch_kind<IN_KIND, false, 1>(block_n, tmA, tmB, tmC, p, ctas, stream);
 }
 
 }  // namespace

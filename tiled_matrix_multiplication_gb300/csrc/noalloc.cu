@@ -86,7 +86,7 @@ tg_status setup_current_device(NoAllocDevice **out) {
 
 tg_status encode(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
                  int64_t ld, int box_cols, int box_rows) {
-    const int es = t == TG_F32 ? 4 : 2;
+    const int es = tgh::esize_of(t);
     const int row_bytes = box_cols * es;
     const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -95,8 +95,9 @@ tg_status encode(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, in
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        t == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = t == TG_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : t == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = g_encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -128,8 +129,8 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     const int eo = tgh::esize_of(dtype_out);
     if (K == 0)
         return cudaMemset2DAsync(c, ldc * eo, 0, N * eo, M, s) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
-    // The planner's choice for this device; K tiles per split, tile width,
-    // multicast and the wait bound are all taken from it.
+    // The planner's choice for this device; K tiles per split, tile width and
+    // the wait bound are all taken from it.
     tgh::Plan pl;
     tgh::make_plan(M, N, K, a, lda, b, ldb, c, ldc, dtype_in, dtype_out, dev->sms, &opt, &pl);
     if (!pl.valid) return TG_ERR_UNSUPPORTED;
@@ -140,14 +141,18 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
         return TG_ERR_UNSUPPORTED;   // partials exceed TG_NOALLOC_SCRATCH_BYTES
 
     const int in_kind = tgh::in_kind_of(dtype_in);
-    const int mc = std::max(plan.multicast, 1);
-    // with A multicast each CTA loads half of its 128 rows of A
-    const int a_rows = mc == 2 ? tgh::kBlockM / 2 : tgh::kBlockM;
+    const int mc = 1;   // single CTAs (TG_PATH_TC) never share A
     CUtensorMap tmA, tmB;
-    if (encode(&tmA, dtype_in, a, M, K, lda, plan.block_k, a_rows) != TG_OK ||
+    if (encode(&tmA, dtype_in, a, M, K, lda, plan.block_k, tgh::kBlockM) != TG_OK ||
         encode(&tmB, dtype_in, b, K, N, ldb,
                tg::tc_b_swizzle_bytes(in_kind, plan.block_n, false) / 2, plan.block_k) != TG_OK)
         return TG_ERR_CUDA;
+    // without a split (K too short to split) the kernel writes C itself, by
+    // TMA stores when C allows them
+    CUtensorMap tmC;
+    std::memset(&tmC, 0, sizeof(tmC));
+    const bool c_tma = plan.splits == 1 && plan.c_vector && (N * eo) % 16 == 0 &&
+                       encode(&tmC, dtype_out, c, M, N, ldc, 64 / eo, 32) == TG_OK;
     tg::TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
     tp.M = static_cast<int32_t>(M);
@@ -168,7 +173,9 @@ extern "C" tg_status tg_gemm_splitk_noalloc(int64_t M, int64_t N, int64_t K, con
     tp.status = dev->status;
     tp.timeout_ns = pl.timeout_ns;
     tp.batch = 1;
-    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, mc, tmA, tmB, tp, plan.ctas, s) != cudaSuccess)
+    tp.c_tma = c_tma ? 1 : 0;
+    if (tg::launch_gemm_tc(in_kind, plan.block_n, false, mc, tmA, tmB, tmC, tp, plan.ctas, s) !=
+        cudaSuccess)
         return TG_ERR_CUDA;
     if (plan.splits > 1 &&
         tg::launch_splitk_reduce(dev->scratch, plan.splits, M, N, c, ldc, tp.out_kind,

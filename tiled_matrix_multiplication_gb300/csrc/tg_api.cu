@@ -75,12 +75,15 @@ static CUtensorMapDataType tma_type(tg_dtype t) {
 
 // Row-major [rows, cols] with pitch `ld` elements; boxes of box_cols x box_rows
 // whose rows (box_cols * esize bytes = 128, 64 or 32) are swizzled at that
-// size; zero fill out of range.  With nb > 1 the map has a third dimension of
-// nb matrices `stride` elements apart (boxes one matrix deep).
+// size -- in 32-byte atoms for `atom32` (4-byte elements read N-major by the
+// TF32 MMA); zero fill out of range.  With nb > 1 the map has a third
+// dimension of nb matrices `stride` elements apart (boxes one matrix deep).
 static tg_status encode_2d(CUtensorMap *map, tg_dtype t, const void *ptr, int64_t rows, int64_t cols,
-                    int64_t ld, int box_cols, int box_rows, int64_t nb = 1, int64_t stride = 0) {
+                    int64_t ld, int box_cols, int box_rows, int64_t nb = 1, int64_t stride = 0,
+                    bool atom32 = false) {
     const int row_bytes = box_cols * esize_of(t);
-    const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+    const CUtensorMapSwizzle sw = atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B
+                                : row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                                                    : CU_TENSOR_MAP_SWIZZLE_32B;
     const cuuint32_t rank = nb > 1 ? 3 : 2;
@@ -175,19 +178,15 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     if (p.pack_b) {
         B = ws + pl.off_b;
         st = cuda_status(
-            p.pack_b == 3 ? tg::launch_split3_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, s)
-            : p.pack_b == 2
-                ? tg::launch_pack_transpose(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s)
-                : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
+            p.pack_b == 3 ? tg::launch_split3_stack(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, s)
+                          : tg::launch_pack_rows(b, ldb, ws + pl.off_b, pl.ldb_p, K, N, ei, s));
         if (st != TG_OK) return fail(st);
     }
     const int64_t Ke = pl.k_eff;   // K of the kernel's operands
     CUtensorMap tmA, tmB;
     const int chunk = 128 / ei;
     if (p.path == TG_PATH_SKINNY) {
-        // with A^T shared by two CTAs each loads half of its rows
-        const int a_box_rows = p.multicast == 2 ? p.block_m / 2 : p.block_m;
-        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, a_box_rows, nb_a, bt.sa) != TG_OK ||
+        if (encode_2d(&tmA, dtype_in, A, M, K, pl.lda_p, p.block_k, p.block_m, nb_a, bt.sa) != TG_OK ||
             encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, chunk, p.block_k, nb_b, bt.sb) != TG_OK)
             return fail(map_error());
         tg::SkParams sp;
@@ -205,7 +204,7 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
         sp.two_per_sm = pl.skinny_two ? 1 : 0;
-        sp.a_share = p.multicast == 2 ? 2 : 1;
+        sp.a_share = 1;
         sp.batch = static_cast<int32_t>(bt.count);
         sp.a_batched = nb_a > 1;
         sp.b_batched = nb_b > 1;
@@ -219,17 +218,29 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         return TG_OK;
     }
     const bool pair = p.path == TG_PATH_TC_PAIR;
-    const int bn_cta = pair ? p.block_n / 2 : p.block_n;   // B columns staged per CTA
+    // B N-major in boxes of b_chunk columns x block_k rows (B' [3K, N] for 3xTF32)
     const int b_chunk = tg::tc_b_swizzle_bytes(in_kind_of(dtype_in), p.block_n, pair) / ei;
-    const tg_status sb = p.pack_b >= 2
-                             ? encode_2d(&tmB, dtype_in, B, N, Ke, pl.ldb_p, p.block_k, bn_cta)
-                             : encode_2d(&tmB, dtype_in, B, K, N, pl.ldb_p, b_chunk, p.block_k,
-                                         nb_b, bt.sb);
+    const tg_status sb = encode_2d(&tmB, dtype_in, B, Ke, N, pl.ldb_p, b_chunk, p.block_k, nb_b,
+                                   bt.sb, dtype_in == TG_F32);
     // with A multicast each CTA loads half of its 128 rows of A
     const int a_rows = p.multicast == 2 ? kBlockM / 2 : kBlockM;
     if (encode_2d(&tmA, dtype_in, A, M, Ke, pl.lda_p, p.block_k, a_rows, nb_a, bt.sa) != TG_OK ||
         sb != TG_OK)
         return fail(map_error());
+    // C through TMA stores: [N, M] (x batch) in boxes of 64 bytes x 32 rows,
+    // when C's base, pitch and batch stride are 16-byte multiples, the kernel
+    // writes C itself (no split-K partials) and each row of C ends on a
+    // 16-byte boundary: a TMA store leaves out what lies beyond the tensor's
+    // last column only in whole 16-byte pieces (measured on GB300: with N = 300
+    // BF16 columns it wrote columns 300..303 of a padded C)
+    CUtensorMap tmC;
+    std::memset(&tmC, 0, sizeof(tmC));
+    const int eo = esize_of(dtype_out);
+    bool c_tma = p.c_vector && p.splits == 1 && (N * eo) % 16 == 0;
+    if (c_tma) {
+        const int64_t nb_c = batched ? bt.count : 1;
+        c_tma = encode_2d(&tmC, dtype_out, c, M, N, ldc, 64 / eo, 32, nb_c, bt.sc) == TG_OK;
+    }
 
     tg::TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
@@ -254,21 +265,11 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
     tp.a_batched = nb_a > 1;
     tp.b_batched = nb_b > 1;
     tp.stride_c = bt.sc;
+    tp.c_tma = c_tma ? 1 : 0;
     // with a K split the epilogue runs where the partials are summed
     if (epi && p.splits == 1) tp.epi = *epi;
-    if (p.tail_tiles > 0) {
-        tp.tail_start = static_cast<int32_t>(pl.tail_start);
-        tp.tail_tiles = p.tail_tiles;
-        tp.tail_splits = p.tail_splits;
-        tp.tail_kps = static_cast<int32_t>(pl.tail_kps);
-        tp.tail_partial = reinterpret_cast<float *>(ws + pl.off_tail);
-        tp.tail_count = reinterpret_cast<unsigned int *>(ws + pl.off_cnt);
-        const size_t cnt_bytes = static_cast<size_t>(p.tail_tiles) * (pair ? 2 : 1) * 4;
-        st = cuda_status(cudaMemsetAsync(tp.tail_count, 0, cnt_bytes, s));
-        if (st != TG_OK) return fail(st);
-    }
     st = cuda_status(tg::launch_gemm_tc(in_kind_of(dtype_in), p.block_n, pair,
-                                        std::max(p.multicast, 1), tmA, tmB, tp, p.ctas, s));
+                                        std::max(p.multicast, 1), tmA, tmB, tmC, tp, p.ctas, s));
     if (st != TG_OK) return fail(st);
     if (p.splits > 1) {
         st = cuda_status(tg::launch_splitk_reduce(tp.partial, p.splits, M, N, c, ldc,

@@ -90,8 +90,6 @@ struct Plan {
     int64_t k_tiles = 0, k_per_split = 0, tiles_m = 0, tiles_n = 0;
     int64_t lda_p = 0, ldb_p = 0;              // pitches after packing
     int64_t off_a = 0, off_b = 0, off_p = 0;   // workspace offsets
-    int64_t off_tail = 0, off_cnt = 0;         // tail-split partials and counters
-    int64_t tail_start = 0, tail_kps = 0;
     bool skinny_two = false;                   // small-M kernel: two CTAs per SM
     uint64_t timeout_ns = 0;
     int64_t stride_c = 0;                      // C batch stride (set before make_plan)

@@ -54,15 +54,11 @@ struct TcParams {
     float *partial;             // [splits][M][N] when splits > 1
     int *status;                // device status word (2 ints)
     uint64_t timeout_ns;
-    // Tail split (splits == 1 only): the last `tail_tiles` tiles in raster
-    // order are each split into `tail_splits` K ranges of `tail_kps` K tiles,
-    // addressed by unit indices >= tail_start.  Each range writes an FP32
-    // partial tile to `tail_partial` ([tail_tiles][tail_splits][BN/4][TILE_M][4]);
-    // the range that finishes a tile last (counted per tile and CTA of a pair
-    // in `tail_count`, zero before the launch) sums them in range order into C.
-    int32_t tail_start, tail_tiles, tail_splits, tail_kps;
-    float *tail_partial;
-    unsigned int *tail_count;
+    // 1: C is written by TMA stores through the tensor map tmC ([N, M] or, for
+    // a batch, [N, M, batch]; boxes of 64 bytes x 32 rows, 64-byte swizzle);
+    // 0: by the epilogue warps' own stores (split-K partials, or C whose base,
+    // row pitch, row length or batch stride is not a multiple of 16 bytes)
+    int32_t c_tma, pad1_;
     // Strided batch: `batch` independent products; A / B use rank-3 tensor maps
     // (z = batch index) when a_batched / b_batched, else one 2-D map shared by
     // every batch (stride 0); C of batch z starts at c + z * stride_c.
@@ -108,11 +104,11 @@ cudaError_t launch_gemm_skinny_fp8(int in_kind, int mp, int nt, const CUtensorMa
 
 // gemm_tc.cu
 // `pair`: the CTA-pair (cta_group::2, 256-row tile) variant; `mc` = 2: clusters
-// of two pairs (or two single CTAs) sharing A by multicast; `ctas` counts CTAs.
+// of two pairs sharing A by multicast; `ctas` counts CTAs.
 int tc_stages(int in_kind, int block_n, bool pair);
-bool tc_supported_block_n(int block_n, bool pair);
-// A-multicast clusters (mc = 2): pairs with 192-, 224- or 256-wide tiles,
-// single CTAs with 128- or 256-wide tiles.
+// Tile widths: 128, 192, 224, 256 for single CTAs and pairs; 512 for pairs.
+bool tc_supported_block_n(int in_kind, int block_n, bool pair);
+// A-multicast clusters (mc = 2): pairs with 192-, 224- or 256-wide tiles.
 bool tc_supported_mc(int block_n, int mc, bool pair);
 // Swizzle (row bytes of a TMA box) of the N-major B tile of a variant.
 int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair);
@@ -120,39 +116,39 @@ int tc_b_swizzle_bytes(int in_kind, int block_n, bool pair);
 // once on the current device (0 if the query fails).
 int tc_max_clusters(int cluster_size);
 cudaError_t launch_gemm_tc(int in_kind, int block_n, bool pair, int mc, const CUtensorMap &tmA,
-                           const CUtensorMap &tmB, const TcParams &p, int ctas,
-                           cudaStream_t stream);
+                           const CUtensorMap &tmB, const CUtensorMap &tmC, const TcParams &p,
+                           int ctas, cudaStream_t stream);
 // The instantiations behind launch_gemm_tc, one translation unit per operand
 // type (gemm_tc_f16.cu, gemm_tc_tf32.cu, gemm_tc_fp8.cu).
 cudaError_t launch_gemm_tc_16bit(int in_kind, int block_n, bool pair, int mc,
                                  const CUtensorMap &tmA, const CUtensorMap &tmB,
-                                 const TcParams &p, int ctas, cudaStream_t stream);
+                                 const CUtensorMap &tmC, const TcParams &p, int ctas,
+                                 cudaStream_t stream);
 cudaError_t launch_gemm_tc_tf32(int block_n, bool pair, int mc, const CUtensorMap &tmA,
-                                const CUtensorMap &tmB, const TcParams &p, int ctas,
-                                cudaStream_t stream);
+                                const CUtensorMap &tmB, const CUtensorMap &tmC,
+                                const TcParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_gemm_tc_fp8(int in_kind, int block_n, bool pair, int mc,
                                const CUtensorMap &tmA, const CUtensorMap &tmB,
-                               const TcParams &p, int ctas, cudaStream_t stream);
+                               const CUtensorMap &tmC, const TcParams &p, int ctas,
+                               cudaStream_t stream);
 cudaError_t status_word_address(int **out);
 cudaError_t set_smem_once(const void *kernel, int bytes);
 
 // aux_kernels.cu
 cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int esize, cudaStream_t stream);
-cudaError_t launch_pack_transpose(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
-                                  int64_t rows, int64_t cols, int esize, cudaStream_t stream);
 // One CTA waits, bounded by timeout_ns, on an mbarrier that nothing arrives
 // on, and records TG_ERR_TIMEOUT in `status` the way the GEMM kernels do.
 cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream);
 // C = the sum of the `splits` partial planes, through the epilogue `epi`
 // (splits == 0: the empty sum, i.e. the epilogue of zero).
 // 3xTF32 operand splitting (x = hi + lo with both parts TF32 values):
-// dst[m, 0:K) = hi(A), [K, 2K) = lo(A), [2K, 3K) = hi(A)      (A' rows)
-// dst[n, 0:K) = hi(B)^T, [K, 2K) = hi(B)^T, [2K, 3K) = lo(B)^T  (B'^T rows)
+// dst[m, 0:K) = hi(A), [K, 2K) = lo(A), [2K, 3K) = hi(A)   (A' rows, [M, 3K])
+// dst rows [0, K) = hi(B), [K, 2K) = hi(B), [2K, 3K) = lo(B)  (B', [3K, N])
 cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld_dst, int64_t M,
                                int64_t K, cudaStream_t stream);
-cudaError_t launch_split3_transpose(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
-                                    int64_t K, int64_t N, cudaStream_t stream);
+cudaError_t launch_split3_stack(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
+                                int64_t K, int64_t N, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N,
                                  void *c, int64_t ldc, int out_kind, int c_vector,
                                  cudaStream_t stream, const EpiParams *epi = nullptr);

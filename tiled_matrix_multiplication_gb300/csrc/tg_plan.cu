@@ -22,20 +22,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             return TG_ERR_INVALID_VALUE;
         if (opt->f32_mode == TG_F32_3XTF32 && (din != TG_F32 || 3 * K > kMaxDim))
             return TG_ERR_UNSUPPORTED;
-        if (opt->multicast == 2) {
-            const bool pair_ok = opt->path != TG_PATH_TC &&
-                                 (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, true));
-            const bool single_ok = opt->path != TG_PATH_TC_PAIR &&
-                                   (!opt->block_n || tg::tc_supported_mc(opt->block_n, 2, false));
-            // the small-M kernel shares A^T between two column tiles, in
-            // clusters of at most 8 CTAs (K split over at most 4)
-            const bool skinny_ok = opt->splits <= 4;
-            if (opt->tail_splits || (opt->path == TG_PATH_SKINNY && !skinny_ok) ||
-                (opt->path != TG_PATH_SKINNY && !pair_ok && !single_ok))
-                return TG_ERR_UNSUPPORTED;
-        }
-        if (opt->tail_splits < 0 || opt->tail_splits == 1 || opt->tail_splits > 8)
-            return TG_ERR_INVALID_VALUE;
+        // A multicast: clusters of two CTA pairs (192-, 224- or 256-wide tiles)
+        if (opt->multicast == 2 &&
+            (opt->path == TG_PATH_TC || opt->path == TG_PATH_SKINNY ||
+             (opt->block_n && !tg::tc_supported_mc(opt->block_n, 2, true))))
+            return TG_ERR_UNSUPPORTED;
         if (opt->path < TG_PATH_AUTO || opt->path > TG_PATH_SKINNY) return TG_ERR_INVALID_VALUE;
         if (opt->splits < 0 || opt->block_n < 0 || opt->group_m < 0 || opt->max_ctas < 0 ||
             opt->timeout_ms < 0)
@@ -53,8 +44,9 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
             if (s > 1 && (s - 1) * cdiv(kt, s) >= kt) return TG_ERR_UNSUPPORTED;
         }
         if (opt->block_n && opt->path != TG_PATH_SKINNY) {
-            const bool one = tg::tc_supported_block_n(opt->block_n, false);
-            const bool two = tg::tc_supported_block_n(opt->block_n, true);
+            const int ik = in_kind_of(static_cast<tg_dtype>(din));
+            const bool one = tg::tc_supported_block_n(ik, opt->block_n, false);
+            const bool two = tg::tc_supported_block_n(ik, opt->block_n, true);
             if ((opt->path == TG_PATH_TC && !one) || (opt->path == TG_PATH_TC_PAIR && !two) ||
                 (!one && !two))
                 return TG_ERR_UNSUPPORTED;
@@ -79,24 +71,11 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
     return TG_OK;
 }
 
-// K ranges for each tile of a short last wave (1 = no tail split): at most
-// `want`, no more than fill the idle slots, and at least 8 K tiles per range.
-// (On GB300 the in-kernel sum of the partials currently costs more than the
-// balanced wave saves, so the planner only splits a tail when asked to.)
-static int64_t tail_split_for(int64_t tiles, int64_t slots, int64_t k_tiles, int64_t want) {
-    if (slots < 2 || want < 2) return 1;
-    const int64_t tail = tiles % slots;
-    if (tail == 0 || tail * 2 > slots) return 1;
-    int64_t ts = std::min<int64_t>(want, slots / tail);
-    ts = std::min<int64_t>(ts, k_tiles / 8);
-    return std::max<int64_t>(ts, 1);
-}
-
 // `pair_slots` / `quad_slots`: clusters of 2 / 4 CTAs resident at once
 // (0: estimate from the SM count).
 // `batch` > 1: that many products with 16-byte aligned operands (no packing,
-// no K split across kernels, no tail split) in one launch; the batch index is
-// the slowest dimension of the work list.
+// no K split across kernels) in one launch; the batch index is the slowest
+// dimension of the work list.
 void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
                int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
                const tg_options *opt, Plan *pl, int pair_slots, int quad_slots,
@@ -122,16 +101,13 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // an FP32 partial tile that a second kernel sums (about 24 K tiles' worth
     // for 128 rows, less for fewer rows).  Ties go to the earlier candidate.
     // Relative efficiencies (percent of the best variant) measured on GB300 at
-    // 8192^3 and on the prefill shapes; single-CTA clusters sharing A measured
-    // about 5 % slower than unshared single CTAs at 128 to 2048 rows.
-    // mc = 2: clusters of two pairs (or two single CTAs) sharing A by multicast
-    // (two tiles per unit).
+    // 8192^3 and on the prefill shapes.  mc = 2: clusters of two pairs sharing
+    // A by multicast (two tiles per unit).
     struct Cand { bool pair; int mc; int bn; int eff; };
     static const Cand kCands[] = {
-        {true, 2, 256, 105}, {true, 1, 256, 100}, {true, 2, 224, 90}, {true, 2, 192, 86},
-        {true, 1, 224, 92}, {true, 1, 192, 84}, {false, 1, 256, 90}, {false, 2, 256, 85},
-        {false, 1, 192, 82}, {false, 1, 224, 80}, {false, 1, 128, 62}, {true, 1, 128, 62},
-        {false, 2, 128, 58}};
+        {true, 1, 512, 98}, {true, 2, 256, 105}, {true, 1, 256, 100}, {true, 2, 224, 90},
+        {true, 2, 192, 86}, {true, 1, 224, 92}, {true, 1, 192, 84}, {false, 1, 256, 90},
+        {false, 1, 192, 82}, {false, 1, 224, 80}, {false, 1, 128, 62}, {true, 1, 128, 62}};
     // At most 128 rows the product streams B (memory-bound): single-CTA tiles
     // 128 wide, with the K split below, measured fastest (pair tiles would be
     // half empty; wider tiles give fewer concurrent streams).
@@ -146,7 +122,6 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
         const int64_t cl = (cd.pair ? 2 : 1) * cd.mc;   // CTAs per cluster
         if (cap < cl) continue;
         if (opt && opt->multicast && opt->multicast != cd.mc) continue;
-        if (cd.mc == 2 && opt && opt->tail_splits) continue;
         const int64_t tile_m = cd.pair ? 2 * kBlockM : kBlockM;
         // resident clusters: 4-CTA clusters can leave SMs of a GPC unused
         int64_t resident = cap;
@@ -174,13 +149,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             // at a quarter: fewer busy CTAs run faster (less contention for L2
             // bandwidth and power), so an idle slot costs less than a busy one.
             const double used = static_cast<double>(units) / static_cast<double>(std::max<int64_t>(1, std::min(units, slots)));
-            double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
-            // A requested tail split (below) turns a short last wave into 1/ts
-            // of a wave plus the partials' round trip.
-            if (se == 1 && opt && opt->tail_splits && !opt->splits && batch == 1) {
-                const int64_t ts = tail_split_for(tiles, slots, pl->k_tiles, opt->tail_splits);
-                if (ts > 1) waves = static_cast<double>(tiles / slots) + 1.15 / static_cast<double>(ts);
-            }
+            const double waves = units > 0 ? used + 0.25 * (static_cast<double>(cdiv(units, std::min(units, slots))) - used) : 0.0;
             const int64_t rows = std::min<int64_t>(M, kBlockM);
             const int64_t partial = se > 1 ? std::max<int64_t>(1, 24 * rows / kBlockM) : 0;
             const double cost =
@@ -205,7 +174,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     // the tile kernel with a K split, E4M3 20.8 vs 24.7 us).
     const int64_t skinny_rows_max = 128;
     const bool skinny_ok = din != TG_F32 && M <= skinny_rows_max &&
-                           (forced_skinny || !(opt && opt->block_n)) &&
+                           (forced_skinny || !(opt && (opt->block_n || opt->multicast == 2))) &&
                            !(opt && (opt->path == TG_PATH_TC || opt->path == TG_PATH_TC_PAIR)) &&
                            batch <= kMaxGridY;
     if (skinny_ok) {
@@ -233,7 +202,6 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             // with two ranges of one k-tile each)
             if (kps < 4) continue;
             if (opt && opt->splits && opt->splits != sc) continue;
-            if (opt && opt->multicast == 2 && sc > 4) continue;   // clusters of <= 8 CTAs
             if (tiles * sc <= cap) {
                 best_s = sc;
                 two = false;
@@ -251,11 +219,7 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             two = nt == 128 && tiles * best_s > cap;
         }
         pl->skinny_two = two;
-        // A^T shared by the CTAs of two adjacent column tiles (multicast = 2,
-        // clusters of 2 x splits <= 8) halves the re-reads of A, but measured
-        // no faster on GB300 at 16 to 128 rows (N = K = 8192), so only on
-        // request.
-        p.multicast = (opt && opt->multicast) ? opt->multicast : 1;
+        p.multicast = 1;
         p.path = TG_PATH_SKINNY;
         p.block_m = mp;
         p.block_n = nt;
@@ -279,8 +243,8 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     const int64_t splits = p.splits;
     const int64_t units = p.tiles * splits;   // (tiles = work units: tile pairs when mc = 2)
     if (p.path == TG_PATH_SKINNY) {
-        // not persistent: one CTA per unit, whole sharing groups of column tiles
-        p.ctas = static_cast<int32_t>(round_up(p.tiles, std::max(p.multicast, 1)) * splits);
+        // not persistent: one CTA per (column tile, K range)
+        p.ctas = static_cast<int32_t>(p.tiles * splits);
     } else if (pair || p.multicast == 2) {
         const int64_t cl = (pair ? 2 : 1) * std::max(p.multicast, 1);
         int64_t resident = cap / cl;
@@ -293,51 +257,23 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     }
     p.pack_a = !(aligned16(a) && (lda * ei) % 16 == 0);
     p.pack_b = !(aligned16(b) && (ldb * ei) % 16 == 0);
-    if (din == TG_F32) p.pack_b = 2;   // kind::tf32 reads B K-major: B^T into the workspace
-    if (x3) p.pack_a = p.pack_b = 3;   // hi / lo TF32 parts of A and of B^T
+    if (x3) p.pack_a = p.pack_b = 3;   // hi / lo TF32 parts of A and of B
     p.c_vector = aligned16(c) && (ldc * eo) % 16 == 0 && (batch == 1 || (pl->stride_c * eo) % 16 == 0);
     pl->lda_p = p.pack_a ? round_up(pl->k_eff, align_elems) : lda;
-    pl->ldb_p = p.pack_b >= 2 ? round_up(pl->k_eff, align_elems)
-                              : (p.pack_b ? round_up(N, align_elems) : ldb);
+    pl->ldb_p = p.pack_b ? round_up(N, align_elems) : ldb;
     int64_t ws = 0;
     if (p.pack_a) {
         pl->off_a = ws;
         ws = round_up(ws + M * pl->lda_p * ei, 256);
     }
-    if (p.pack_b) {
+    if (p.pack_b) {   // B [K, N], or B' [3K, N] of the 3xTF32 parts
         pl->off_b = ws;
-        ws = round_up(ws + (p.pack_b >= 2 ? N : K) * pl->ldb_p * ei, 256);
+        ws = round_up(ws + pl->k_eff * pl->ldb_p * ei, 256);
     }
     const bool global_partials = splits > 1 && p.path != TG_PATH_SKINNY;
     if (global_partials) {
         pl->off_p = ws;
         ws = round_up(ws + splits * M * N * 4, 256);
-    }
-    // Tail split of the tensor-core paths (auto plans without a K split).
-    if (p.path != TG_PATH_SKINNY && splits == 1 && opt && opt->tail_splits && !opt->splits &&
-        batch == 1) {
-        const int64_t slots = pair ? std::max<int64_t>(1, cap / 2) : std::max<int64_t>(1, cap);
-        const int64_t ts = tail_split_for(p.tiles, slots, pl->k_tiles, opt->tail_splits);
-        if (ts > 1) {
-            p.tail_tiles = static_cast<int32_t>(p.tiles % slots);
-            pl->tail_start = p.tiles - p.tail_tiles;
-            pl->tail_kps = cdiv(pl->k_tiles, ts);
-            p.tail_splits = static_cast<int32_t>(cdiv(pl->k_tiles, pl->tail_kps));
-            const int64_t cta_group = pair ? 2 : 1;
-            pl->off_tail = ws;
-            ws = round_up(ws + static_cast<int64_t>(p.tail_tiles) * p.tail_splits * p.block_m *
-                                   p.block_n * 4, 256);
-            pl->off_cnt = ws;
-            ws = round_up(ws + static_cast<int64_t>(p.tail_tiles) * cta_group * 4, 256);
-            if (pair) {
-                const int64_t pairs = std::max<int64_t>(
-                    1, std::min<int64_t>(pl->tail_start + p.tail_tiles * p.tail_splits, cap / 2));
-                p.ctas = static_cast<int32_t>(2 * pairs);
-            } else {
-                p.ctas = static_cast<int32_t>(std::max<int64_t>(
-                    1, std::min<int64_t>(pl->tail_start + p.tail_tiles * p.tail_splits, cap)));
-            }
-        }
     }
     p.workspace_bytes = ws;
     p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (global_partials ? 1 : 0);
@@ -354,10 +290,8 @@ tg_status validate_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const
     const tg_status v = validate(M, N, K, a, lda, b, ldb, c, ldc, din, dout, opt);
     if (v != TG_OK) return v;
     if (batch > kMaxDim) return TG_ERR_UNSUPPORTED;
-    if (batch > 1 && opt) {
-        if (opt->tail_splits) return TG_ERR_UNSUPPORTED;
-        if (opt->splits > 1 && opt->path != TG_PATH_SKINNY) return TG_ERR_UNSUPPORTED;
-    }
+    if (batch > 1 && opt && opt->splits > 1 && opt->path != TG_PATH_SKINNY)
+        return TG_ERR_UNSUPPORTED;
     if (batch <= 1 || M == 0 || N == 0) return TG_OK;
     const int64_t lim = int64_t(1) << 46;   // elements spanned by the batch strides
     for (const int64_t st : {sa, sb, sc})
@@ -466,8 +400,6 @@ tg_status tg_plan_gemm(int64_t M, int64_t N, int64_t K, const void *a, int64_t l
     if (M == 0 || N == 0 || K == 0) {   // nothing, or a memset of C: no kernel of the library
         pl.pub.kernels = 0;
         pl.pub.workspace_bytes = 0;
-        pl.pub.tail_tiles = 0;
-        pl.pub.tail_splits = 0;
     }
     *plan = pl.pub;
     return TG_OK;
@@ -498,8 +430,6 @@ tg_status tg_plan_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int6
     if (batch == 0 || M == 0 || N == 0 || K == 0) {
         pl.pub.kernels = 0;
         pl.pub.workspace_bytes = 0;
-        pl.pub.tail_tiles = 0;
-        pl.pub.tail_splits = 0;
     }
     *plan = pl.pub;
     return TG_OK;

@@ -264,6 +264,49 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 2-D / 3-D tiled store shared -> global, tracked as a bulk async-group of
+// the issuing thread.  Elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t x,
+                                             int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Closes the bulk async-group of the stores issued so far by this thread.
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until at most N of this thread's bulk groups are incomplete (their
+// global writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Orders this thread's ordinary shared-memory writes before later reads of
+// the same memory by the async proxy (a TMA store).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------- tcgen05/TMEM
 
 template <int CTA_GROUP>
@@ -403,6 +446,23 @@ __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t lbo_by
     d |= static_cast<uint64_t>(((8u * SW) >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;
     d |= desc_swizzle_mode(SW) << 61;
+    return d;
+}
+
+// MN-major operand of 4-byte elements (kind::tf32): 128-byte rows (32
+// elements) swizzled in 32-byte atoms -- descriptor layout code 1, written by
+// TMA with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B.  The MMA reads K in groups of
+// four 128-byte rows, 512 bytes apart (SBO), and boxes of 32 MN elements
+// `lbo_bytes` apart.  (The plain 128-byte swizzle of the 2-byte and 1-byte
+// operands gives zero products with 4-byte MN-major operands.)  One MMA's
+// K = 8 rows then span 1024 contiguous bytes of its box.
+__device__ __forceinline__ uint64_t smem_desc_mn_tf32(uint32_t saddr, uint32_t lbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 1ull << 61;
     return d;
 }
 
