@@ -23,8 +23,6 @@ cudaError_t launch_gemm_skinny(int in_kind, int mp, int nt, const CUtensorMap &t
                                const CUtensorMap &tmB, const SkParams &p, cudaStream_t stream) {
     if (p.splits != 1 && p.splits != 2 && p.splits != 4 && p.splits != 8)
         return cudaErrorInvalidValue;
-    if (p.a_share > 1 && (p.a_share != 2 || p.splits > 4 || mp < 16))   // clusters of <= 8
-        return cudaErrorInvalidValue;
     switch (in_kind) {
     case IN_F16: return sk_launch_kind<IN_F16>(mp, nt, tmA, tmB, p, stream);
     case IN_BF16: return sk_launch_kind<IN_BF16>(mp, nt, tmA, tmB, p, stream);

@@ -168,31 +168,22 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Cluster = `share` adjacent column tiles x `splits` K ranges; cluster rank
-    // jn * splits + split.  With share = 2 the two CTAs of a K range (one per
-    // column tile) each load half of the A^T rows and multicast them to both.
-    const int share = p.a_share > 1 ? 2 : 1;
-    const int csize = static_cast<int>(cluster_num_ctas());     // splits * share
-    const int splits = csize / share;                            // == p.splits
-    const int crank = static_cast<int>(cluster_cta_rank());
-    const int split = crank % splits;
-    const int jn = crank / splits;
-    const int tn = (static_cast<int>(blockIdx.x) / csize) * share + jn;
-    const uint16_t share_mask =
-        static_cast<uint16_t>((1u << split) | (1u << (splits + split)));   // share == 2
+    // Cluster = the `splits` K ranges of one column tile; cluster rank = K range.
+    const int splits = static_cast<int>(cluster_num_ctas());     // == p.splits
+    const int split = static_cast<int>(cluster_cta_rank());
+    const int tn = static_cast<int>(blockIdx.x) / splits;
     const int kt0 = split * p.k_tiles_per_split;
     const int kt1 = min(kt0 + p.k_tiles_per_split, p.k_tiles);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            // one MMA commit per CTA reading the stage's A^T
-            mbar_init(empty_bar(s), SPLIT ? 1 : share);
+            mbar_init(empty_bar(s), 1);
         }
         if constexpr (SPLIT) {
             for (int s = 0; s < SA; ++s) {
                 mbar_init(afull_bar(s), 1);
-                mbar_init(aempty_bar(s), share);
+                mbar_init(aempty_bar(s), 1);
             }
         }
         mbar_init(tfull_bar, 1);
@@ -215,7 +206,6 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (share > 1) cluster_sync_all();   // the partner's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Prologue done: let the next kernel's prologue start, then wait for the
@@ -242,14 +232,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
             const uint32_t fb = full0 + 8u * stage;
             mbar_arrive_expect_tx(fb, bytes);
             if (with_a) {
-                if (share > 1) {
-                    // rows [jn*MP/2, (jn+1)*MP/2) of A^T, to this CTA and its partner
-                    const uint32_t dst = sAt + stage * Cfg::AT_STAGE + jn * (Cfg::AT_STAGE / 2);
-                    if (p.a_batched)
-                        tma_load_3d_mc(dst, &tmA, fb, kt * Cfg::BK, jn * (MP / 2), z, share_mask);
-                    else
-                        tma_load_2d_mc(dst, &tmA, fb, kt * Cfg::BK, jn * (MP / 2), share_mask);
-                } else if (p.a_batched) {
+                if (p.a_batched) {
                     tma_load_3d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0, z);
                 } else {
                     tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
@@ -323,13 +306,9 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                                               (kt > kt0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                // the slot holding A^T is released to both CTAs that filled it
-                const uint32_t a_release = SPLIT ? aempty_bar(astage) : empty_bar(stage);
-                if (SPLIT) umma_commit(empty_bar(stage));
-                if (share > 1)
-                    umma_commit_mc(a_release, share_mask);
-                else
-                    umma_commit(a_release);
+                // release the stage (and, with separate rings, the A^T slot)
+                umma_commit(empty_bar(stage));
+                if (SPLIT) umma_commit(aempty_bar(astage));
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
@@ -409,7 +388,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                 const int nl = j * kSubN + quad * 32 + lane;   // column within the tile
                 const int owner = nl / cols;
                 const int c = nl - owner * cols;
-                const uint32_t rank = static_cast<uint32_t>(jn * splits + owner);
+                const uint32_t rank = static_cast<uint32_t>(owner);
                 // lanes hold consecutive columns: each push of a warp fills one
                 // contiguous run of 16-byte (4-row) cells at the owner
                 const uint32_t dst = map_to_cta(
@@ -543,8 +522,6 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
             }
         }
         cluster_wait();
-    } else if (share > 1) {
-        cluster_sync_all();   // the partner's last commits to this CTA's barriers have landed
     }
     if (warp == 1) {
         tc_fence_after_sync();
@@ -561,15 +538,13 @@ cudaError_t sk_launch_cfg(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    const int share = p.a_share > 1 ? 2 : 1;
-    const int tiles = (p.tiles_n + share - 1) / share * share;   // whole sharing groups
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * p.splits),
+    cfg.gridDim = dim3(static_cast<unsigned>(p.tiles_n * p.splits),
                        static_cast<unsigned>(p.batch > 0 ? p.batch : 1), 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits * share);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -204,7 +204,6 @@ tg_status enqueue(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, c
         sp.status = dev->status;
         sp.timeout_ns = pl.timeout_ns;
         sp.two_per_sm = pl.skinny_two ? 1 : 0;
-        sp.a_share = 1;
         sp.batch = static_cast<int32_t>(bt.count);
         sp.a_batched = nb_a > 1;
         sp.b_batched = nb_b > 1;

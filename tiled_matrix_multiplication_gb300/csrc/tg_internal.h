@@ -78,7 +78,6 @@ struct SkParams {
     int32_t splits;             // cluster size: 1, 2, 4 or 8
     int32_t out_kind;
     int32_t two_per_sm;         // half-size ring, two CTAs per SM
-    int32_t a_share;            // 2: CTAs on adjacent column tiles share A^T by multicast
     int32_t batch;              // gridDim.y; A / B rank-3 when a_batched / b_batched
     int32_t a_batched, b_batched;
     int32_t c_vector;           // C base, row pitch and batch stride are 16-byte multiples
