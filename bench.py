@@ -65,6 +65,9 @@ WORKLOADS = {
                        "square GEMM 2048^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
     "square4096_f16": (4096, 4096, 4096, "f16", "f16", "uniform",
                        "square GEMM 4096^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
+    "panel1024x4096x4096_f16": (1024, 4096, 4096, "f16", "f16", "uniform",
+                                "row panel 1024x4096x4096 FP16 (the product tg_gemm_host runs "
+                                "per panel of a 4096^3 call)"),
     "square8192_f16": (8192, 8192, 8192, "f16", "f16", "uniform",
                        "square GEMM 8192^3, FP16 in U[-1,1), FP32 accumulate, FP16 out"),
     "square16384_f16": (16384, 16384, 16384, "f16", "f16", "uniform",

@@ -63,41 +63,77 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = __uint_as_float(l);
 }
 
+// Both split kernels take a rows x cols source 4 columns per thread: grid.x
+// over column groups (256 threads x 4 columns per block), grid.y over rows
+// (each block loops over rows gridDim.y apart).  `vec`: the source base and
+// pitch and every destination column block are 16-byte aligned, so a thread
+// moves its 4 columns with one 16-byte load and 16-byte stores.
+
 // A' = [hi(A) | lo(A) | hi(A)], [M, 3K] with pitch ld_dst.
-__global__ void split3_rows_kernel(const float *__restrict__ a, int64_t lda, float *__restrict__ dst,
-                                   int64_t ld_dst, int64_t M, int64_t K) {
+__global__ void __launch_bounds__(256) split3_rows_kernel(const float *__restrict__ a, int64_t lda,
+                                                          float *__restrict__ dst, int64_t ld_dst,
+                                                          int64_t M, int64_t K, int vec) {
     grid_dependency_wait();
     grid_launch_dependents();
-    const int64_t total = M * K;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t m = i / K;
-        const int64_t k = i - m * K;
-        float hi, lo;
-        split_tf32(a[m * lda + k], hi, lo);
+    const int64_t k = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+    if (k >= K) return;
+    for (int64_t m = blockIdx.y; m < M; m += gridDim.y) {
+        const float *src = a + m * lda + k;
         float *row = dst + m * ld_dst;
-        row[k] = hi;
-        row[K + k] = lo;
-        row[2 * K + k] = hi;
+        if (vec) {
+            const float4 x = *reinterpret_cast<const float4 *>(src);
+            float4 hi, lo;
+            split_tf32(x.x, hi.x, lo.x);
+            split_tf32(x.y, hi.y, lo.y);
+            split_tf32(x.z, hi.z, lo.z);
+            split_tf32(x.w, hi.w, lo.w);
+            *reinterpret_cast<float4 *>(row + k) = hi;
+            *reinterpret_cast<float4 *>(row + K + k) = lo;
+            *reinterpret_cast<float4 *>(row + 2 * K + k) = hi;
+        } else {
+            for (int64_t c = k; c < K && c < k + 4; ++c) {
+                float hi, lo;
+                split_tf32(a[m * lda + c], hi, lo);
+                row[c] = hi;
+                row[K + c] = lo;
+                row[2 * K + c] = hi;
+            }
+        }
     }
 }
 
 // B' = [hi(B); hi(B); lo(B)] stacked along K: [3K, N] with pitch ld_dst,
 // read by the TF32 kernel N-major like B itself.
-__global__ void split3_stack_kernel(const float *__restrict__ b, int64_t ldb, float *__restrict__ dst,
-                                    int64_t ld_dst, int64_t K, int64_t N) {
+__global__ void __launch_bounds__(256) split3_stack_kernel(const float *__restrict__ b, int64_t ldb,
+                                                           float *__restrict__ dst, int64_t ld_dst,
+                                                           int64_t K, int64_t N, int vec) {
     grid_dependency_wait();
     grid_launch_dependents();
-    const int64_t total = K * N;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t k = i / N;
-        const int64_t n = i - k * N;
-        float hi, lo;
-        split_tf32(b[k * ldb + n], hi, lo);
-        dst[k * ld_dst + n] = hi;
-        dst[(K + k) * ld_dst + n] = hi;
-        dst[(2 * K + k) * ld_dst + n] = lo;
+    const int64_t n = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+    if (n >= N) return;
+    for (int64_t k = blockIdx.y; k < K; k += gridDim.y) {
+        float *d0 = dst + k * ld_dst + n;
+        float *d1 = d0 + K * ld_dst;
+        float *d2 = d1 + K * ld_dst;
+        if (vec) {
+            const float4 x = *reinterpret_cast<const float4 *>(b + k * ldb + n);
+            float4 hi, lo;
+            split_tf32(x.x, hi.x, lo.x);
+            split_tf32(x.y, hi.y, lo.y);
+            split_tf32(x.z, hi.z, lo.z);
+            split_tf32(x.w, hi.w, lo.w);
+            *reinterpret_cast<float4 *>(d0) = hi;
+            *reinterpret_cast<float4 *>(d1) = hi;
+            *reinterpret_cast<float4 *>(d2) = lo;
+        } else {
+            for (int64_t c = 0; c < 4 && n + c < N; ++c) {
+                float hi, lo;
+                split_tf32(b[k * ldb + n + c], hi, lo);
+                d0[c] = hi;
+                d1[c] = hi;
+                d2[c] = lo;
+            }
+        }
     }
 }
 
@@ -215,22 +251,34 @@ cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream
     return cudaGetLastError();
 }
 
+// 2-D grid of the split kernels: column groups of 1024 (256 threads x 4) on
+// x, rows on y (at most 65535 blocks; the kernels loop over the rest).
+static dim3 split_grid(int64_t rows, int64_t cols) {
+    const int64_t gx = (cols + 1023) / 1024;
+    const int64_t gy = std::min<int64_t>(rows, std::max<int64_t>(1, 4096 / std::max<int64_t>(gx, 1)));
+    return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(gy, 1), 65535)));
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 cudaError_t launch_split3_rows(const void *a, int64_t lda, void *dst, int64_t ld_dst, int64_t M,
                                int64_t K, cudaStream_t stream) {
     if (M <= 0 || K <= 0) return cudaSuccess;
-    const int threads = 256;
-    return launch_pdl(split3_rows_kernel, dim3(grid_for(M * K, threads)), dim3(threads), stream,
+    if ((K + 1023) / 1024 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int vec = aligned16(a) && aligned16(dst) && lda % 4 == 0 && ld_dst % 4 == 0 && K % 4 == 0;
+    return launch_pdl(split3_rows_kernel, split_grid(M, K), dim3(256), stream,
                       static_cast<const float *>(a), lda, static_cast<float *>(dst), ld_dst, M,
-                      K);
+                      K, vec);
 }
 
 cudaError_t launch_split3_stack(const void *b, int64_t ldb, void *dst, int64_t ld_dst,
                                 int64_t K, int64_t N, cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
-    const int threads = 256;
-    return launch_pdl(split3_stack_kernel, dim3(grid_for(K * N, threads)), dim3(threads), stream,
+    if ((N + 1023) / 1024 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int vec = aligned16(b) && aligned16(dst) && ldb % 4 == 0 && ld_dst % 4 == 0 && N % 4 == 0;
+    return launch_pdl(split3_stack_kernel, split_grid(K, N), dim3(256), stream,
                       static_cast<const float *>(b), ldb, static_cast<float *>(dst), ld_dst, K,
-                      N);
+                      N, vec);
 }
 
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t M, int64_t N, void *c,
