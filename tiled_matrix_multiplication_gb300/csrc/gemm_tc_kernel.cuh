@@ -61,7 +61,12 @@
 //     empty[s] counts one commit from each pair leader.
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = epilogue (warp w may read TMEM lanes 32*(w%4) .. +31).
+// warps 2..9 = epilogue.  Warp w may read TMEM lanes 32*(w%4) .. +31, so two
+// warps serve each lane quarter; warps 2..5 drain the first half of the
+// accumulator's 32-column chunks and warps 6..9 the rest.  Per chunk a warp's
+// work is a chain of short dependent steps (TMEM load, convert, stage, fence,
+// TMA store, buffer wait), so two warps per quarter halve the time from a
+// tile's last MMA to its last store.
 //
 // Every mbarrier wait is bounded; on expiry the CTA records TG_ERR_TIMEOUT in
 // the status word, raises a shared abort flag so the other roles stop early,
@@ -83,15 +88,16 @@ namespace tg {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Dynamic shared memory for the stage ring and the output staging: the
 // 227 KB a CTA may use, less the alignment slack and the barriers.
 constexpr int kSmemBudget = 232448 - 1024 - 256;
 // Output staging: per epilogue warp, kOutBufs boxes of 32 rows x 64 bytes
 // (32 columns of a 16-bit type or 16 of FP32), 64-byte swizzled.
 constexpr int kOutBox = 32 * 64;
-constexpr int kOutBufs = 4;
-constexpr int kOutStaging = 4 * kOutBufs * kOutBox;
+constexpr int kOutBufs = 2;
+constexpr int kOutStaging = kEpiWarps * kOutBufs * kOutBox;
 
 template <int IN_KIND, int BN, bool PAIR, int MC = 1>
 struct TcCfg {
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4 * CG);
+            mbar_init(tempty_bar(b), kEpiWarps * CG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -494,12 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
-        const int quad = warp & 3;
+        const int ew = warp - 2;                       // epilogue warp 0..7
+        const int quad = warp & 3;                     // its TMEM lane quarter
+        // its 32-column chunks of the accumulator: the first or second half
+        constexpr int kChunks = BN / 32;
+        constexpr int kHalf = (kChunks + 1) / 2;
+        const int cbeg = (ew / 4) * kHalf * 32;
+        const int cend = min(BN, cbeg + kHalf * 32);
         const bool f32_out = p.out_kind == OUT_F32;
         // this warp's staging boxes; boxes are used round-robin, and a box is
         // rewritten only after the TMA store issued kOutBufs boxes earlier has
         // finished reading it
-        const uint32_t my_boxes = sOut + static_cast<uint32_t>(quad * kOutBufs * kOutBox);
+        const uint32_t my_boxes = sOut + static_cast<uint32_t>(ew * kOutBufs * kOutBox);
         uint32_t nbox = 0;
         auto next_box = [&]() {
             if (nbox >= kOutBufs) {
@@ -529,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc_phase = NACC == 2 ? ((acc_count >> 1) & 1u) : (acc_count & 1u);
             const bool got = mbar_wait<PAIR>(tfull_bar(buf), acc_phase, p.timeout_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | quad);
+                if (lane == 0) record_failure(p.status, 6, (ROLE_EPILOGUE << 16) | ew);
                 *abort_flag = 1;
                 break;
             }
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * Cfg::ACC_STRIDE;
             const bool tma = p.c_tma != 0;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = cbeg; c0 < cend; c0 += 32) {
                 uint32_t r[32];
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;

@@ -55,33 +55,38 @@ __device__ __forceinline__ float epi_one(const EpiParams &e, int out_kind, int64
 // thread that writes it, so R may be C itself.
 __device__ __forceinline__ void epi_chunk32(const EpiParams &e, int out_kind, int row, int col,
                                             int ncols, uint32_t (&r)[32], int z = 0) {
-    float sc[32], bi[32], res[32];
     const bool full = ncols == 32;
-    if (full && e.sb_vector) {
+    const bool vec_sb = full && e.sb_vector;
+    const bool vec_res = full && e.res_vector;
+    const int64_t roff = e.res ? z * e.stride_r + static_cast<int64_t>(row) * e.ldr + col : 0;
+    const bool gelu = e.act == ACT_GELU_TANH;
+    const bool gate = e.act == ACT_SILU || gelu;
+    // eight columns at a time, so that scale, bias and residual values of the
+    // whole chunk are never live at once
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            const float4 s4 = e.scale ? *reinterpret_cast<const float4 *>(e.scale + col + j)
-                                      : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float4 b4 = e.bias ? *reinterpret_cast<const float4 *>(e.bias + col + j)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            sc[j] = s4.x, sc[j + 1] = s4.y, sc[j + 2] = s4.z, sc[j + 3] = s4.w;
-            bi[j] = b4.x, bi[j + 1] = b4.y, bi[j + 2] = b4.z, bi[j + 3] = b4.w;
+    for (int g = 0; g < 32; g += 8) {
+        float sc[8], bi[8], res[8];
+        if (vec_sb) {
+#pragma unroll
+            for (int h = 0; h < 8; h += 4) {
+                const float4 s4 = e.scale ? *reinterpret_cast<const float4 *>(e.scale + col + g + h)
+                                          : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float4 b4 = e.bias ? *reinterpret_cast<const float4 *>(e.bias + col + g + h)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                sc[h] = s4.x, sc[h + 1] = s4.y, sc[h + 2] = s4.z, sc[h + 3] = s4.w;
+                bi[h] = b4.x, bi[h + 1] = b4.y, bi[h + 2] = b4.z, bi[h + 3] = b4.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                sc[j] = (e.scale && g + j < ncols) ? e.scale[col + g + j] : 1.f;
+                bi[j] = (e.bias && g + j < ncols) ? e.bias[col + g + j] : 0.f;
+            }
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            sc[j] = (e.scale && j < ncols) ? e.scale[col + j] : 1.f;
-            bi[j] = (e.bias && j < ncols) ? e.bias[col + j] : 0.f;
-        }
-    }
-    if (e.res) {
-        const int64_t off = z * e.stride_r + static_cast<int64_t>(row) * e.ldr + col;
-        if (full && e.res_vector && out_kind != OUT_F32) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const uint16_t *>(e.res) + off);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 w = src[q];
+        if (e.res) {
+            if (vec_res && out_kind != OUT_F32) {
+                const uint4 w = reinterpret_cast<const uint4 *>(
+                    static_cast<const uint16_t *>(e.res) + roff)[g / 8];
                 const uint32_t h[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
@@ -93,40 +98,41 @@ __device__ __forceinline__ void epi_chunk32(const EpiParams &e, int out_kind, in
                         const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&h[t]);
                         lo = __low2float(v), hi = __high2float(v);
                     }
-                    res[q * 8 + 2 * t] = lo;
-                    res[q * 8 + 2 * t + 1] = hi;
+                    res[2 * t] = lo;
+                    res[2 * t + 1] = hi;
                 }
-            }
-        } else if (full && e.res_vector) {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(e.res) + off);
+            } else if (vec_res) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(static_cast<const float *>(e.res) + roff + g);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = src[q];
-                res[4 * q] = v.x, res[4 * q + 1] = v.y, res[4 * q + 2] = v.z, res[4 * q + 3] = v.w;
-            }
-        } else {
+                for (int q = 0; q < 2; ++q) {
+                    const float4 v = src[q];
+                    res[4 * q] = v.x, res[4 * q + 1] = v.y, res[4 * q + 2] = v.z, res[4 * q + 3] = v.w;
+                }
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) res[j] = j < ncols ? epi_load_res(e, out_kind, off + j) : 0.f;
+                for (int j = 0; j < 8; ++j)
+                    res[j] = g + j < ncols ? epi_load_res(e, out_kind, roff + g + j) : 0.f;
+            }
         }
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = fmaf(__uint_as_float(r[g + j]) * e.alpha, sc[j], bi[j]);
+        // one loop per activation (the choice is uniform), not a branch per element
+        if (e.act == ACT_RELU) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
+        } else if (gate) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = epi_sigmoid_gate(v[j], epi_gate_arg(gelu, v[j]));
+        }
+        if (e.res) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = fmaf(e.beta, res[j], v[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[g + j] = __float_as_uint(v[j]);
     }
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = fmaf(__uint_as_float(r[j]) * e.alpha, sc[j], bi[j]);
-    // one loop per activation (the choice is uniform), not a branch per element
-    if (e.act == ACT_RELU) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
-    } else if (e.act == ACT_SILU || e.act == ACT_GELU_TANH) {
-        const bool gelu = e.act == ACT_GELU_TANH;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = epi_sigmoid_gate(v[j], epi_gate_arg(gelu, v[j]));
-    }
-    if (e.res) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = fmaf(e.beta, res[j], v[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
 }
 
 }  // namespace tg
