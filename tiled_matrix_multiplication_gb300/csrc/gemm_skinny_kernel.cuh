@@ -26,12 +26,13 @@
 // K range).  After its main loop, and a cluster barrier, each CTA pushes the
 // FP32 partial of every column straight from tensor memory to the CTA that
 // owns the column -- CTA r owns columns [r*NT/S, (r+1)*NT/S) -- with
-// asynchronous remote stores (st.async) into the owner's idle ring; the owner
-// waits on one mbarrier for all the bytes, sums the S partials in K-range
-// order, rounds once, stages the tile and writes C in 16-byte pieces.  No
-// partials go to global memory and no
-// second kernel runs; the sum order is fixed, so results do not depend on
-// timing.  (Pulling the partials with remote loads instead cost one cluster
+// asynchronous remote stores (st.async) into the owner's idle ring, and its
+// own columns into its own ring with plain shared-memory stores (the remote
+// stores run at about 40 GB/s per SM, so this saves 1/S of their time); the
+// owner waits on one mbarrier for the peers' bytes, sums the S partials in
+// K-range order, rounds once, stages the tile and writes C in 16-byte
+// pieces.  No partials go to global memory and no second kernel runs; the sum
+// order is fixed, so results do not depend on timing.  (Pulling the partials with remote loads instead cost one cluster
 // round trip per few outputs: 5 to 10 us per call at 64 to 128 rows.)
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
@@ -43,6 +44,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "tg_epilogue.cuh"
 #include "tg_internal.h"
@@ -90,7 +93,7 @@ struct SkCfg {
     static constexpr int A_STAGES = SPLIT ? A_SPLIT : STAGES;
     static constexpr int RING_BYTES = STAGES * BT_STAGE + A_STAGES * AT_STAGE;
     // received K-split partials: [K range][row group of 4][column][4 rows] FP32,
-    // then the finished tile [row][column] in the output type
+    // then the finished tile [row group][column][4 rows] in the output type
     static constexpr int G4 = MP / 4;
     static constexpr int RECV_BYTES = NT * MP * 4;
     static constexpr int OUT_STAGE_MAX = MP * (NT / 2) * 4;   // K split >= 2, FP32 out
@@ -191,10 +194,10 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
         *abort_flag = 0;
         never_abort = 0;
         fence_mbar_init();
-        // one phase: the partials of this CTA's columns, rows rounded up to 4
-        // (peers push them after the cluster barrier that follows the main loop)
+        // one phase: the peers' partials of this CTA's columns, rows rounded
+        // up to 4 (pushed after the cluster barrier that follows the main loop)
         if (splits > 1)
-            mbar_arrive_expect_tx(recv_bar, NT * 16 * ((min(p.M, MP) + 3) / 4));
+            mbar_arrive_expect_tx(recv_bar, (NT - NT / splits) * 16 * ((min(p.M, MP) + 3) / 4));
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
@@ -373,9 +376,10 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
     if (splits > 1) {
         // ------------------------ K-split reduction through distributed smem
         // CTA r of the K ranges owns columns [r*cols, (r+1)*cols) of the tile.
-        // Each CTA pushes every column's FP32 partial to its owner with
-        // asynchronous remote stores into the owner's (now idle) ring; the
-        // owner waits on one barrier for all the bytes, sums the S partials in
+        // Each CTA pushes every other CTA's columns of its FP32 partial to
+        // their owner with asynchronous remote stores into the owner's (now
+        // idle) ring, and stores its own columns into its own ring; the owner
+        // waits on one barrier for the peers' bytes, sums the S partials in
         // K-range order and writes C.
         cluster_sync_all();   // every ring of the cluster is idle from here on
         const int cols = NT / splits;
@@ -389,12 +393,20 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                 const int owner = nl / cols;
                 const int c = nl - owner * cols;
                 const uint32_t rank = static_cast<uint32_t>(owner);
+                const bool self = owner == split;   // this CTA's own columns
                 // lanes hold consecutive columns: each push of a warp fills one
                 // contiguous run of 16-byte (4-row) cells at the owner
-                const uint32_t dst = map_to_cta(
-                    recv_base + static_cast<uint32_t>((split * Cfg::G4 * cols + c) * 16), rank);
+                const uint32_t off =
+                    recv_base + static_cast<uint32_t>((split * Cfg::G4 * cols + c) * 16);
+                const uint32_t dst = self ? off : map_to_cta(off, rank);
                 const uint32_t gstep = static_cast<uint32_t>(cols * 16);   // next row group
                 const uint32_t rbar = map_to_cta(recv_bar, rank);
+                auto put = [&](uint32_t a, uint32_t x, uint32_t y, uint32_t zz, uint32_t w) {
+                    if (self)
+                        st_shared_v4(a, x, y, zz, w);
+                    else
+                        st_async_v4(a, x, y, zz, w, rbar);
+                };
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                        j * Cfg::ACC_COLS;
                 // only the groups of 4 rows that hold rows < M are sent
@@ -404,8 +416,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
 #pragma unroll
                     for (int g = 0; g < 4; ++g)
                         if (g < push_groups)
-                            st_async_v4(dst + gstep * g, r[4 * g], r[4 * g + 1], r[4 * g + 2],
-                                        r[4 * g + 3], rbar);
+                            put(dst + gstep * g, r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
                 } else {
 #pragma unroll 1
                     for (int c0 = 0; c0 < 4 * push_groups; c0 += 32) {
@@ -414,8 +425,8 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
                             if (c0 / 4 + g < push_groups)
-                                st_async_v4(dst + gstep * (c0 / 4 + g), r[4 * g], r[4 * g + 1],
-                                            r[4 * g + 2], r[4 * g + 3], rbar);
+                                put(dst + gstep * (c0 / 4 + g), r[4 * g], r[4 * g + 1],
+                                    r[4 * g + 2], r[4 * g + 3]);
                     }
                 }
             }
@@ -432,93 +443,59 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
         // mbarriers -- so the arrive is relaxed and need not wait for them.
         tc_fence_before_sync();
         cluster_arrive_relaxed();
+        __syncthreads();   // this CTA's own partial (plain stores) is visible
         // Sum the S partials of each (row group, column) cell in K-range order,
-        // apply the epilogue, round, and stage the cells [row group][column][4
-        // rows] behind the received partials ...
-        const int eo = p.out_kind == OUT_F32 ? 4 : 2;
-        uint8_t *out_tile = gbase + Cfg::RECV_BYTES;
+        // apply the epilogue, round, and write the cell's 4 rows to C.  Lanes
+        // take consecutive cells (columns), so each load of a warp reads 512
+        // contiguous bytes and each store writes 32 consecutive columns of one
+        // row.
+        const bool all_got = __syncthreads_and(got);
         const int n_base = tn * NT + split * cols;
         const int z = static_cast<int>(blockIdx.y);
-        if (got) {
-            for (int i = threadIdx.x; i < push_groups * cols; i += kThreads) {
-                const int g = i / cols;
-                const int c = i - g * cols;
+        const int rows = min(p.M, MP);
+        // (S a compile-time constant: a cell's S loads issue back to back)
+        auto sum_write = [&](auto s_const) {
+            constexpr int SS = decltype(s_const)::value;
+            constexpr int COLS = NT / SS;
+            for (int i = threadIdx.x; i < push_groups * COLS; i += kThreads) {
+                const int g = i / COLS;
+                const int c = i - g * COLS;
                 const int n = n_base + c;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int s = 0; s < splits; ++s) {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        gbase + ((s * Cfg::G4 + g) * cols + c) * 16);
-                    acc[0] += v.x;
-                    acc[1] += v.y;
-                    acc[2] += v.z;
-                    acc[3] += v.w;
-                }
-                if (p.epi.on) {
+                float4 v[SS];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (4 * g + u < p.M && n < p.N)
-                            acc[u] = epi_one(p.epi, p.out_kind, 4 * g + u, n, acc[u], z);
+                for (int s = 0; s < SS; ++s)
+                    v[s] = *reinterpret_cast<const float4 *>(gbase + ((s * Cfg::G4 + g) * COLS + c) * 16);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < SS; ++s) {
+                    acc[0] += v[s].x;
+                    acc[1] += v[s].y;
+                    acc[2] += v[s].z;
+                    acc[3] += v[s].w;
                 }
-                // one store per cell: its 4 rows side by side (shared-memory
-                // stores are expensive here, one wide store beats four narrow)
-                uint8_t *cell = out_tile + (g * cols + c) * 4 * eo;
-                if (p.out_kind == OUT_F32) {
-                    *reinterpret_cast<float4 *>(cell) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                } else if (p.out_kind == OUT_F16) {
-                    const __half2 lo = __floats2half2_rn(acc[0], acc[1]);
-                    const __half2 hi = __floats2half2_rn(acc[2], acc[3]);
-                    *reinterpret_cast<uint2 *>(cell) =
-                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
-                                   *reinterpret_cast<const uint32_t *>(&hi));
-                } else {
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
-                    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
-                    *reinterpret_cast<uint2 *>(cell) =
-                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
-                                   *reinterpret_cast<const uint32_t *>(&hi));
+                if (n >= p.N) continue;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int m = 4 * g + u;
+                    if (m >= rows) break;
+                    float x = acc[u];
+                    if (p.epi.on) x = epi_one(p.epi, p.out_kind, m, n, x, z);
+                    const int64_t off = static_cast<int64_t>(z) * p.stride_c +
+                                        static_cast<int64_t>(m) * p.ldc + n;
+                    if (p.out_kind == OUT_F32)
+                        static_cast<float *>(p.c)[off] = x;
+                    else if (p.out_kind == OUT_F16)
+                        static_cast<__half *>(p.c)[off] = __float2half_rn(x);
+                    else
+                        static_cast<__nv_bfloat16 *>(p.c)[off] = __float2bfloat16_rn(x);
                 }
             }
-        }
-        // ... then write it to C in 16-byte pieces (element by element where C
-        // is not 16-byte aligned or a piece runs past column N).
-        if (__syncthreads_and(got)) {
-            const int per = 16 / eo;                 // elements per piece
-            const int pieces = cols / per;           // per row (cols >= 16)
-            const int rows = min(p.M, MP);
-            uint8_t *cz = static_cast<uint8_t *>(p.c) + static_cast<int64_t>(z) * p.stride_c * eo;
-            for (int i = threadIdx.x; i < rows * pieces; i += kThreads) {
-                const int m = i / pieces;
-                const int c = (i - m * pieces) * per;
-                const int n = n_base + c;
-                // the piece's elements sit 4 elements apart in consecutive cells
-                const uint8_t *src = out_tile + (((m >> 2) * cols + c) * 4 + (m & 3)) * eo;
-                uint8_t *dst = cz + (static_cast<int64_t>(m) * p.ldc + n) * eo;
-                if (p.c_vector && n + per <= p.N) {
-                    uint32_t w[4];
-                    if (eo == 4) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = *reinterpret_cast<const uint32_t *>(src + e * 16);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = static_cast<uint32_t>(
-                                       *reinterpret_cast<const uint16_t *>(src + 16 * e)) |
-                                   (static_cast<uint32_t>(
-                                        *reinterpret_cast<const uint16_t *>(src + 16 * e + 8))
-                                    << 16);
-                    }
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-                } else {
-                    for (int e = 0; e < per && n + e < p.N; ++e) {
-                        if (eo == 4)
-                            *reinterpret_cast<uint32_t *>(dst + e * 4) =
-                                *reinterpret_cast<const uint32_t *>(src + e * 16);
-                        else
-                            *reinterpret_cast<uint16_t *>(dst + e * 2) =
-                                *reinterpret_cast<const uint16_t *>(src + e * 8);
-                    }
-                }
+        };
+        if (all_got) {
+            switch (splits) {
+            case 2: sum_write(std::integral_constant<int, 2>{}); break;
+            case 4: sum_write(std::integral_constant<int, 4>{}); break;
+            default: sum_write(std::integral_constant<int, 8>{}); break;
             }
         }
         cluster_wait();
