@@ -208,7 +208,12 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
             } else if (nt == 128 && tiles * sc <= 2 * cap) {
                 // more CTAs than SMs: two half-size CTAs per SM keep them all
                 // resident (measured faster than one full-size CTA per SM for
-                // every M from 1 to 128 at N = K = 8192)
+                // every M from 1 to 64 at N = K = 8192).  At 128 rows a K split
+                // already spread over the SMs one CTA each is kept instead: the
+                // doubled split sends twice the partial bytes over the cluster
+                // network (N = K = 8192: FP16 27.6 vs 28.1 us, E4M3 17.7 vs
+                // 18.6 us for 2 against 4 ranges)
+                if (mp == 128 && best_s > 1) break;
                 best_s = sc;
                 two = true;
                 break;
