@@ -37,8 +37,9 @@
 //
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = TMEM epilogue (direct stores, or the pushes), and at 128 rows
-// (two CTAs per SM) warp 6 = a second TMA producer for a separate A^T ring;
-// all warps then sum the received partials.  Every mbarrier wait is bounded
+// with two CTAs per SM warp 6 = a second TMA producer for a separate A^T
+// ring; with one CTA per SM warps 6..11 wait for the K-split sum.  All warps
+// then sum the received partials.  Every mbarrier wait is bounded
 // (status word + abort flag, as in gemm_tc.cu).
 #pragma once
 
@@ -82,7 +83,10 @@ struct SkCfg {
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
     static constexpr bool SPLIT = TWO && MP == 128;
-    static constexpr int THREADS = SPLIT ? 224 : 192;   // + the A^T producer warp
+    // + the A^T producer warp when SPLIT; one CTA per SM: six more warps,
+    // idle until the K-split sum, where they double the warps on that
+    // latency-bound pass (2048 cells of 4 rows per CTA at 128 rows, S = 2)
+    static constexpr int THREADS = SPLIT ? 224 : (TWO ? 192 : 384);
     static constexpr int PAD = SPLIT ? 0 : 1024;        // room to align the ring
     static constexpr int BUDGET =
         TWO ? (SPLIT ? kTwoSmemPerCta - 512 : 112 * 1024) : kSmemBudget;
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                 record_failure(p.status, 6, (ROLE_DRAIN << 16) | 2);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------- epilogue: wait for TMEM
         // Thread (quad, lane) owns column n = quad*32 + lane of each 128-column
         // accumulator.  Without a K split it writes C here; with one it pushes
