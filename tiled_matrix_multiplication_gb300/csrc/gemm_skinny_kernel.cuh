@@ -38,7 +38,7 @@
 // Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = TMEM epilogue (direct stores, or the pushes), and at 128 rows
 // with two CTAs per SM warp 6 = a second TMA producer for a separate A^T
-// ring; with one CTA per SM warps 6..11 wait for the K-split sum.  All warps
+// ring; with one CTA per SM warps 6..15 wait for the K-split sum.  All warps
 // then sum the received partials.  Every mbarrier wait is bounded
 // (status word + abort flag, as in gemm_tc.cu).
 #pragma once
@@ -83,10 +83,10 @@ struct SkCfg {
     static constexpr int AT_STAGE = MP * 128;     // MP rows of A
     static constexpr int STAGE_BYTES = BT_STAGE + AT_STAGE;
     static constexpr bool SPLIT = TWO && MP == 128;
-    // + the A^T producer warp when SPLIT; one CTA per SM: six more warps,
-    // idle until the K-split sum, where they double the warps on that
-    // latency-bound pass (2048 cells of 4 rows per CTA at 128 rows, S = 2)
-    static constexpr int THREADS = SPLIT ? 224 : (TWO ? 192 : 384);
+    // + the A^T producer warp when SPLIT; one CTA per SM: ten more warps,
+    // idle until the K-split sum, where they add warps to that latency-bound
+    // pass (2048 cells of 4 rows per CTA at 128 rows, S = 2)
+    static constexpr int THREADS = SPLIT ? 224 : (TWO ? 192 : 512);
     static constexpr int PAD = SPLIT ? 0 : 1024;        // room to align the ring
     static constexpr int BUDGET =
         TWO ? (SPLIT ? kTwoSmemPerCta - 512 : 112 * 1024) : kSmemBudget;
