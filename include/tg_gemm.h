@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define TG_ABI_VERSION 9
+#define TG_ABI_VERSION 10
 
 typedef enum tg_dtype {
     TG_F16 = 0,   /* IEEE 754 binary16 */
@@ -84,7 +84,9 @@ typedef enum tg_status {
     TG_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
     TG_ERR_ARCH = 5,             /* current device is not an sm_103 GPU */
     TG_ERR_TIMEOUT = 6,          /* a kernel's bounded wait ran out */
-    TG_ERR_NOT_IMPLEMENTED = 7
+    TG_ERR_NOT_IMPLEMENTED = 7,
+    TG_ERR_BOUNDS = 8            /* checked builds: a device-side bounds or
+                                    alignment check failed (access skipped) */
 } tg_status;
 
 /* Execution paths the planner chooses between. */
@@ -399,9 +401,38 @@ const char *tg_status_string(tg_status status);
  * failure since the last call, TG_ERR_TIMEOUT if a bounded wait ran out, or
  * TG_ERR_CUDA if the synchronisation itself failed or a kernel found its
  * shared memory not aligned as it requires (it then returns without writing
- * C).  No counterpart in the pages, which report no device-side failures.
+ * C), or, in a checked build, TG_ERR_BOUNDS if a device-side check failed.  No counterpart in the pages, which report no device-side failures.
  */
 tg_status tg_last_device_error(void *stream);
+
+/*
+ * Checked builds.  `python -m tiled_matrix_multiplication_gb300.build --checked`
+ * builds libtg_gemm_checked.so: the same library compiled with device-side
+ * checks in front of the tensor-core kernels' shared-memory, tensor-memory,
+ * TMA and cluster-remote accesses (each box of a TMA load or store inside its
+ * ring or staging area with a 16-byte aligned innermost coordinate and no
+ * negative store coordinate, each MMA's operands inside the ring, each
+ * tensor-memory load inside its accumulator, each remote store and received
+ * cell inside the receive area).  A failed check records TG_ERR_BOUNDS and the
+ * check site in the status word and the access is skipped -- nothing traps;
+ * the kernel ends through its bounded waits and tg_last_device_error()
+ * returns TG_ERR_BOUNDS.  Python loads it instead of libtg_gemm.so when
+ * TG_CHECKED=1 is set.  No counterpart in the pages.
+ *
+ * tg_checked_build -- 1 in a checked build, 0 otherwise.
+ */
+int32_t tg_checked_build(void);
+
+/*
+ * tg_selftest_bounds -- check of the checked-build mechanism: enqueues on
+ * `stream` a one-warp kernel that makes one checked store to element `index`
+ * of a 32-element device array; an index outside 0 .. 31 fails the check, so
+ * the store is skipped and TG_ERR_BOUNDS is recorded (tg_last_device_error
+ * then returns it and clears it).  TG_ERR_INVALID_VALUE for index < 0 or
+ * index > 1024; TG_ERR_NOT_IMPLEMENTED in a normal build (no checks compiled
+ * in).  No counterpart in the pages.
+ */
+tg_status tg_selftest_bounds(int32_t index, void *stream);
 
 /*
  * tg_selftest_timeout -- failure-detection check: enqueues on `stream` a

@@ -42,10 +42,20 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert tg.tg_abi_version() == 9
+    assert tg.tg_abi_version() == 10
     assert tg.tg_status_string(tg.TG_OK) == "TG_OK"
     assert tg.tg_status_string(tg.TG_ERR_TIMEOUT) == "TG_ERR_TIMEOUT"
+    assert tg.tg_status_string(tg.TG_ERR_BOUNDS) == "TG_ERR_BOUNDS"
     assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
+
+
+def test_normal_build_has_no_device_checks(lib):
+    # the device-side checks exist only in the checked build; the normal one
+    # says so without touching the device
+    assert tg.tg_checked_build() == 0 and not tg.CHECKED
+    assert tg.tg_selftest_bounds(40, 0) == tg.TG_ERR_NOT_IMPLEMENTED
+    assert tg.tg_selftest_bounds(-1, 0) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_selftest_bounds(1025, 0) == tg.TG_ERR_INVALID_VALUE
 
 
 def plan(M, N, K, din="f16", dout=None, lda=None, ldb=None, ldc=None, a=A, b=B, c=C, sms=148,

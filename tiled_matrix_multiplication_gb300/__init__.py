@@ -19,6 +19,7 @@ from ._lib import (DTYPE_CODES, EXPORTS, LIB_PATH, TG_BF16, TG_E4M3, TG_E5M2, TG
                    TG_F32_3XTF32, TG_F32_TF32,
                    TG_ERR_CUDA,
                    TG_ERR_INVALID_VALUE, TG_ERR_NOT_IMPLEMENTED, TG_ERR_OUT_OF_MEMORY,
+                   TG_ERR_BOUNDS, CHECKED, tg_checked_build, tg_selftest_bounds,
                    TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F16, TG_F32, TG_OK, TG_PATH_AUTO,
                    TG_PATH_SKINNY, TG_PATH_TC, TG_PATH_TC_PAIR, NOALLOC_SCRATCH_BYTES, TgError,
                    load, make_options, status_name, tg_abi_version, tg_gemm, tg_gemm_ex,
@@ -40,6 +41,7 @@ __all__ = [
     "TG_F16", "TG_BF16", "TG_F32", "TG_E4M3", "TG_E5M2", "TG_F32_TF32", "TG_F32_3XTF32", "TG_OK", "TG_ERR_INVALID_VALUE", "TG_ERR_UNSUPPORTED",
     "TG_ERR_OUT_OF_MEMORY", "TG_ERR_CUDA", "TG_ERR_ARCH", "TG_ERR_TIMEOUT",
     "TG_ERR_NOT_IMPLEMENTED", "TG_PATH_AUTO", "TG_PATH_TC", "TG_PATH_TC_PAIR", "TG_PATH_SKINNY",
+    "TG_ERR_BOUNDS", "CHECKED", "tg_checked_build", "tg_selftest_bounds",
 ]
 
 

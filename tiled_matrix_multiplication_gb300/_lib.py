@@ -11,7 +11,10 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
+# TG_CHECKED=1 selects the checked build (device-side bounds and alignment
+# checks compiled in; built with ``python -m tiled_matrix_multiplication_gb300.build --checked``)
+CHECKED = os.environ.get("TG_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_PKG, "libtg_gemm_checked.so" if CHECKED else "libtg_gemm.so")
 
 TG_F16, TG_BF16, TG_F32, TG_E4M3, TG_E5M2 = 0, 1, 2, 3, 4
 DTYPE_CODES = {"f16": TG_F16, "bf16": TG_BF16, "f32": TG_F32, "e4m3": TG_E4M3, "e5m2": TG_E5M2}
@@ -24,6 +27,7 @@ TG_ERR_CUDA = 4
 TG_ERR_ARCH = 5
 TG_ERR_TIMEOUT = 6
 TG_ERR_NOT_IMPLEMENTED = 7
+TG_ERR_BOUNDS = 8
 
 TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 
@@ -31,7 +35,8 @@ TG_PATH_AUTO, TG_PATH_TC, TG_PATH_TC_PAIR, TG_PATH_SKINNY = 0, 1, 2, 3
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_plan_gemm", "tg_status_string",
            "tg_last_device_error", "tg_abi_version", "tg_gemm_splitk_noalloc",
            "tg_gemm_strided_batched", "tg_plan_gemm_strided_batched", "tg_gemm_fused",
-           "tg_gemm_host", "tg_selftest_timeout", "tg_gemm_strided_batched_fused")
+           "tg_gemm_host", "tg_selftest_timeout", "tg_gemm_strided_batched_fused",
+           "tg_checked_build", "tg_selftest_bounds")
 
 TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_ACT_GELU_TANH = 0, 1, 2, 3
 ACT_CODES = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "silu": TG_ACT_SILU,
@@ -127,6 +132,10 @@ def load(path: str | None = None):
         lib.tg_gemm_host.restype = ctypes.c_int
         lib.tg_selftest_timeout.argtypes = [i32, vp]
         lib.tg_selftest_timeout.restype = ctypes.c_int
+        lib.tg_checked_build.argtypes = []
+        lib.tg_checked_build.restype = i32
+        lib.tg_selftest_bounds.argtypes = [i32, vp]
+        lib.tg_selftest_bounds.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -266,3 +275,14 @@ def tg_selftest_timeout(timeout_ms, stream) -> int:
     """Enqueue the failure-detection check (a bounded wait that always runs
     out); tg_last_device_error then reports TG_ERR_TIMEOUT."""
     return int(load().tg_selftest_timeout(timeout_ms, stream))
+
+
+def tg_checked_build() -> int:
+    """1 if the loaded library has the device-side checks compiled in."""
+    return int(load().tg_checked_build())
+
+
+def tg_selftest_bounds(index, stream) -> int:
+    """Enqueue the checked-build check: one checked store to element `index`
+    of a 32-element array (outside 0..31: skipped, TG_ERR_BOUNDS recorded)."""
+    return int(load().tg_selftest_bounds(index, stream))

@@ -197,6 +197,19 @@ __global__ void selftest_timeout_kernel(int *status, uint64_t timeout_ns) {
     }
 }
 
+#ifdef TG_CHECKED
+// Checked builds: lane 0 makes one checked store to element `index` of a
+// 32-element shared array; outside 0 .. 31 the check fails, the store is
+// skipped and TG_ERR_BOUNDS is recorded.
+__global__ void selftest_bounds_kernel(int *status, int index) {
+    volatile __shared__ int cells[32];
+    cells[threadIdx.x] = 0;
+    __syncwarp();
+    if (threadIdx.x == 0 && tg_check(status, index >= 0 && index < 32, CHK_SELFTEST, index))
+        cells[index] = 1;
+}
+#endif
+
 int grid_for(int64_t work, int threads) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -250,6 +263,13 @@ cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
     return cudaGetLastError();
 }
+
+#ifdef TG_CHECKED
+cudaError_t launch_selftest_bounds(int *status, int index, cudaStream_t stream) {
+    selftest_bounds_kernel<<<1, 32, 0, stream>>>(status, index);
+    return cudaGetLastError();
+}
+#endif
 
 // 2-D grid of the split kernels: column groups of 1024 (256 threads x 4) on
 // x, rows on y (at most 65535 blocks; the kernels loop over the rest).

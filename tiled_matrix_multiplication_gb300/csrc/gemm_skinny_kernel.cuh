@@ -238,14 +238,23 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
             }
             const uint32_t fb = full0 + 8u * stage;
             mbar_arrive_expect_tx(fb, bytes);
-            if (with_a) {
+            // (checked builds: every box lies in its ring, x 16-byte aligned)
+            const bool a_ok = tg_check(p.status,
+                                       sAt + (stage + 1) * Cfg::AT_STAGE <= bars &&
+                                           tma_x_aligned(kt * Cfg::BK, Cfg::ESIZE),
+                                       CHK_SK_LOAD, stage);
+            const bool b_ok = tg_check(p.status,
+                                       sBt + (stage + 1) * Cfg::BT_STAGE <= sAt &&
+                                           tma_x_aligned(tn * NT, Cfg::ESIZE),
+                                       CHK_SK_LOAD, 0x100 | stage);
+            if (with_a && a_ok) {
                 if (p.a_batched) {
                     tma_load_3d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0, z);
                 } else {
                     tma_load_2d(sAt + stage * Cfg::AT_STAGE, &tmA, fb, kt * Cfg::BK, 0);
                 }
             }
-            if (with_b) {
+            if (with_b && b_ok) {
 #pragma unroll
                 for (int j = 0; j < NT / Cfg::CHUNK_N; ++j) {
                     const uint32_t dst = sBt + stage * Cfg::BT_STAGE + j * Cfg::BT_BOX;
@@ -364,6 +373,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 32) {
                         uint32_t r[32];
+                        if (!tg_check(p.status, c0 + 32 <= Cfg::ACC_COLS, CHK_SK_TMEM, c0)) break;
                         tmem_load_32cols_sync(taddr + c0, r);
 #pragma unroll
                         for (int q = 0; q < 32; ++q)
@@ -405,6 +415,13 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                 const uint32_t dst = self ? off : map_to_cta(off, rank);
                 const uint32_t gstep = static_cast<uint32_t>(cols * 16);   // next row group
                 const uint32_t rbar = map_to_cta(recv_bar, rank);
+                // (checked builds: the column's cells lie in the receive area)
+                if (!tg_check(p.status,
+                              off >= recv_base &&
+                                  off + gstep * (push_groups - 1) + 16 <= recv_base + Cfg::RECV_BYTES &&
+                                  owner < splits,
+                              CHK_SK_PUSH, nl))
+                    continue;
                 auto put = [&](uint32_t a, uint32_t x, uint32_t y, uint32_t zz, uint32_t w) {
                     if (self)
                         st_shared_v4(a, x, y, zz, w);
@@ -425,6 +442,7 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
 #pragma unroll 1
                     for (int c0 = 0; c0 < 4 * push_groups; c0 += 32) {
                         uint32_t r[32];
+                        if (!tg_check(p.status, c0 + 32 <= Cfg::ACC_COLS, CHK_SK_TMEM, c0)) break;
                         tmem_load_32cols_sync(taddr + c0, r);
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
@@ -465,6 +483,10 @@ __global__ void __launch_bounds__(SkCfg<IN_KIND, MP, NT, TWO>::THREADS, TWO ? 2 
                 const int g = i / COLS;
                 const int c = i - g * COLS;
                 const int n = n_base + c;
+                // (checked builds: the cell's last partial lies in the receive area)
+                if (!tg_check(p.status, ((SS - 1) * Cfg::G4 + g) * COLS + c < Cfg::RECV_BYTES / 16,
+                              CHK_SK_SUM, i))
+                    continue;
                 float4 v[SS];
 #pragma unroll
                 for (int s = 0; s < SS; ++s)

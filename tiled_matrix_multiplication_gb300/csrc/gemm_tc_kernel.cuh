@@ -371,8 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb =
                         PAIR ? map_to_cta(full_bar(stage), pair_leader) : full_bar(stage);
                     // rank-3 maps for batched operands (z = batch), 2-D otherwise
+                    // (checked builds: the box lies in the ring, x is 16-byte aligned)
                     auto load = [&](uint32_t dst, const CUtensorMap *map, bool batched, int x,
-                                    int y) {
+                                    int y, uint32_t bytes, int site) {
+                        if (!tg_check(p.status,
+                                      dst >= sA && dst + bytes <= sOut &&
+                                          tma_x_aligned(x, Cfg::ESIZE),
+                                      site, stage))
+                            return;
                         if constexpr (PAIR) {
                             if (batched)
                                 tma_load_3d_pair(dst, map, fb, x, y, wk.z);
@@ -391,19 +397,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
                         const uint32_t dst = sA + stage * Cfg::A_STAGE + q * (Cfg::A_STAGE / 2);
                         const int ya = row0 + q * (Cfg::CTA_M / 2);
-                        if (p.a_batched)
-                            tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
-                        else
-                            tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
+                        if (tg_check(p.status,
+                                     dst >= sA && dst + Cfg::A_STAGE / 2 <= sB &&
+                                         tma_x_aligned(kt * Cfg::BK, Cfg::ESIZE),
+                                     CHK_TC_LOAD_A, stage)) {
+                            if (p.a_batched)
+                                tma_load_3d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, wk.z, mask);
+                            else
+                                tma_load_2d_pair_mc(dst, &tmA, fb, kt * Cfg::BK, ya, mask);
+                        }
                     } else {
-                        load(sA + stage * Cfg::A_STAGE, &tmA, p.a_batched, kt * Cfg::BK, row0);
+                        load(sA + stage * Cfg::A_STAGE, &tmA, p.a_batched, kt * Cfg::BK, row0,
+                             Cfg::A_STAGE, CHK_TC_LOAD_A);
                     }
 #pragma unroll
                     for (int j = 0; j < Cfg::B_CHUNKS; ++j)
                         load(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmB, p.b_batched,
                              colb + (j / Cfg::CHUNKS_PER_MMA) * Cfg::MMA_N +
                                  (j % Cfg::CHUNKS_PER_MMA) * Cfg::CHUNK_N,
-                             kt * Cfg::BK);
+                             kt * Cfg::BK, Cfg::B_BOX, CHK_TC_LOAD_B);
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -455,8 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t a0 = sA + stage * Cfg::A_STAGE;
                     const uint32_t b0 = sB + stage * Cfg::B_STAGE;
+                    // (checked builds: the stage's operands lie in the ring; if not,
+                    // its MMAs are left out and the ring still advances)
+                    const int kk_end = tg_check(p.status,
+                                                a0 + Cfg::A_STAGE <= sB &&
+                                                    b0 + Cfg::N_MMAS * Cfg::B_MMA_STRIDE <= sOut,
+                                                CHK_TC_MMA, stage)
+                                           ? Cfg::BK / Cfg::UMMA_K
+                                           : 0;
 #pragma unroll
                     for (int kk = 0; kk < Cfg::BK / Cfg::UMMA_K; ++kk) {
+                        if (kk >= kk_end) break;
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
 #pragma unroll
                         for (int h = 0; h < Cfg::N_MMAS; ++h) {
@@ -518,13 +539,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) bulk_wait_group_read<kOutBufs - 1>();
                 __syncwarp();
             }
-            return my_boxes + (nbox % kOutBufs) * kOutBox;
+            const uint32_t box = my_boxes + (nbox % kOutBufs) * kOutBox;
+            // (checked builds: the box lies in the staging area; after a failed
+            // check the warp stages into the first box instead -- in bounds, the
+            // result is invalid and the status word says so)
+            if (!tg_check(p.status, box >= sOut && box + kOutBox <= sOut + kOutStaging,
+                          CHK_TC_STAGE, ew))
+                return sOut;
+            return box;
         };
         auto store_box = [&](uint32_t box, int x, int y, int z, bool in_range) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (in_range) {
+                // (checked builds: x 16-byte aligned, no negative coordinate)
+                if (in_range && tg_check(p.status,
+                                         tma_x_aligned(x, f32_out ? 4 : 2) && x >= 0 && y >= 0,
+                                         CHK_TC_STORE, quad)) {
                     if (p.batch > 1)
                         tma_store_3d(&tmC, box, x, y, z);
                     else
@@ -554,6 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c0 = cbeg; c0 < cend; c0 += 32) {
                 uint32_t r[32];
+                // (checked builds: the columns lie in this accumulator buffer)
+                if (!tg_check(p.status, c0 + 32 <= Cfg::ACC_STRIDE && buf < NACC, CHK_TC_TMEM, c0))
+                    break;
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;
                 if (!tma) {

@@ -299,6 +299,7 @@ const char *tg_status_string(tg_status s) {
     case TG_ERR_ARCH: return "TG_ERR_ARCH";
     case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT";
     case TG_ERR_NOT_IMPLEMENTED: return "TG_ERR_NOT_IMPLEMENTED";
+    case TG_ERR_BOUNDS: return "TG_ERR_BOUNDS";
     default: return "TG_ERR_UNKNOWN";
     }
 }
@@ -453,6 +454,28 @@ tg_status tg_selftest_timeout(int32_t timeout_ms, void *stream) {
     if (st != TG_OK) return st;
     return cuda_status(tg::launch_selftest_timeout(
         dev->status, static_cast<uint64_t>(timeout_ms) * 1000000ull, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t tg_checked_build(void) {
+#ifdef TG_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+tg_status tg_selftest_bounds(int32_t index, void *stream) {
+    if (index < 0 || index > 1024) return TG_ERR_INVALID_VALUE;
+#ifdef TG_CHECKED
+    DeviceState *dev = nullptr;
+    const tg_status st = device_state(&dev);
+    if (st != TG_OK) return st;
+    return cuda_status(tg::launch_selftest_bounds(dev->status, index,
+                                                  static_cast<cudaStream_t>(stream)));
+#else
+    (void)stream;
+    return TG_ERR_NOT_IMPLEMENTED;
+#endif
 }
 
 tg_status tg_last_device_error(void *stream) {

@@ -139,6 +139,9 @@ cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t
 // One CTA waits, bounded by timeout_ns, on an mbarrier that nothing arrives
 // on, and records TG_ERR_TIMEOUT in `status` the way the GEMM kernels do.
 cudaError_t launch_selftest_timeout(int *status, uint64_t timeout_ns, cudaStream_t stream);
+#ifdef TG_CHECKED
+cudaError_t launch_selftest_bounds(int *status, int index, cudaStream_t stream);
+#endif
 // C = the sum of the `splits` partial planes, through the epilogue `epi`
 // (splits == 0: the empty sum, i.e. the epilogue of zero).
 // 3xTF32 operand splitting (x = hi + lo with both parts TF32 values):

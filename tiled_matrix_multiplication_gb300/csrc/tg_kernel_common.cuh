@@ -13,6 +13,36 @@ __device__ __forceinline__ void record_failure(int *status, int code, int where)
     if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, where);
 }
 
+// Checked builds (compiled with -DTG_CHECKED, libtg_gemm_checked.so): device-side
+// bounds and alignment checks in front of the kernels' shared-memory, tensor-
+// memory, TMA and remote accesses.  A failed check records TG_ERR_BOUNDS (8)
+// and the site in the status word and the caller skips the access (the kernel
+// then ends through its bounded waits); nothing traps.  In the normal build
+// tg_check is `true` and its condition is never evaluated at run time.
+#ifdef TG_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr int kErrBounds = 8;
+// check sites (high half of the recorded `where`; the low half is a detail)
+enum CheckSite : int {
+    CHK_TC_LOAD_A = 1, CHK_TC_LOAD_B = 2, CHK_TC_MMA = 3, CHK_TC_TMEM = 4, CHK_TC_STAGE = 5,
+    CHK_TC_STORE = 6, CHK_SK_LOAD = 7, CHK_SK_TMEM = 8, CHK_SK_PUSH = 9, CHK_SK_SUM = 10,
+    CHK_SELFTEST = 15
+};
+__device__ __forceinline__ bool tg_check(int *status, bool ok, int site, int detail) {
+    if constexpr (kChecked) {
+        if (!ok) {
+            record_failure(status, kErrBounds, (site << 16) | (detail & 0xffff));
+            return false;
+        }
+    }
+    return true;
+}
+// a TMA tile coordinate along the innermost dimension starts on a 16-byte boundary
+__device__ __forceinline__ bool tma_x_aligned(int x, int esize) { return ((x * esize) & 15) == 0; }
+
 // Load 32 accumulator columns of this thread's row and wait for them in one
 // statement, so no use of r[] can be scheduled ahead of the wait.
 __device__ __forceinline__ void tmem_load_32cols_sync(uint32_t taddr, uint32_t (&r)[32]) {
