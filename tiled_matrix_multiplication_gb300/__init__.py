@@ -45,16 +45,45 @@ __all__ = [
 ]
 
 
+_TORCH_CODES = None
+
+
 def dtype_code(dtype) -> int:
     """torch dtype (or 'f16'/'bf16'/'f32') -> tg_dtype code."""
+    global _TORCH_CODES
     if isinstance(dtype, str):
         return DTYPE_CODES[dtype]
-    import torch
-    table = {torch.float16: TG_F16, torch.bfloat16: TG_BF16, torch.float32: TG_F32,
-             torch.float8_e4m3fn: TG_E4M3, torch.float8_e5m2: TG_E5M2}
-    if dtype not in table:
+    if _TORCH_CODES is None:
+        import torch
+        _TORCH_CODES = {torch.float16: TG_F16, torch.bfloat16: TG_BF16, torch.float32: TG_F32,
+                        torch.float8_e4m3fn: TG_E4M3, torch.float8_e5m2: TG_E5M2}
+    code = _TORCH_CODES.get(dtype)
+    if code is None:
         raise TgError(TG_ERR_UNSUPPORTED, f"dtype {dtype}")
-    return table[dtype]
+    return code
+
+
+class _OnDevice:
+    """Makes `device` current for the call, touching the current device only
+    when it differs (entering torch's device context on every call costs more
+    than a small GEMM on the GPU)."""
+    __slots__ = ("index", "prev")
+
+    def __init__(self, device):
+        self.index = device.index
+
+    def __enter__(self):
+        import torch
+        cur = torch.cuda.current_device()
+        self.prev = cur if cur != self.index else None
+        if self.prev is not None:
+            torch.cuda.set_device(self.index)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            import torch
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _stream_handle(stream) -> int:
@@ -94,7 +123,7 @@ def gemm(a, b, out_dtype=None, out=None, stream=None, **options):
     ldb = b.stride(0) if K > 1 else max(N, 1)
     ldc = out.stride(0) if M > 1 else max(N, 1)
     opt = make_options(**options) if options else None
-    with torch.cuda.device(a.device):
+    with _OnDevice(a.device):
         st = tg_gemm_ex(M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
                         dtype_code(a.dtype), dtype_code(out_dtype), _stream_handle(stream), opt)
     if st != TG_OK:
@@ -146,7 +175,7 @@ def gemm_fused(a, b, out_dtype=None, out=None, stream=None, alpha=1.0, scale=Non
                        residual=residual.data_ptr() if residual is not None else 0, ldr=ldr,
                        activation=activation)
     opt = make_options(**options) if options else None
-    with torch.cuda.device(a.device):
+    with _OnDevice(a.device):
         st = tg_gemm_fused(M, N, K, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
                            dtype_code(a.dtype), dtype_code(out_dtype), ep,
                            _stream_handle(stream), opt)
@@ -204,7 +233,7 @@ def bmm(a, b, out_dtype=None, out=None, stream=None, **options):
     import torch
     batch, M, N, K, lda, sa, ldb, sb, ldc, sc, out_dtype, out = _bmm_args(a, b, out_dtype, out)
     opt = make_options(**options) if options else None
-    with torch.cuda.device(a.device):
+    with _OnDevice(a.device):
         st = tg_gemm_strided_batched(batch, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(), ldb, sb,
                                      out.data_ptr(), ldc, sc, dtype_code(a.dtype),
                                      dtype_code(out_dtype), _stream_handle(stream), opt)
@@ -243,7 +272,7 @@ def bmm_fused(a, b, out_dtype=None, out=None, stream=None, alpha=1.0, scale=None
                        residual=residual.data_ptr() if residual is not None else 0, ldr=ldr,
                        activation=activation)
     opt = make_options(**options) if options else None
-    with torch.cuda.device(a.device):
+    with _OnDevice(a.device):
         st = tg_gemm_strided_batched_fused(batch, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(),
                                            ldb, sb, out.data_ptr(), ldc, sc, dtype_code(a.dtype),
                                            dtype_code(out_dtype), ep, sr,
