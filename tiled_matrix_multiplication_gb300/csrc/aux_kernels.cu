@@ -33,17 +33,34 @@
 namespace tg {
 namespace {
 
+// grid.x over groups of V = 16 / sizeof(T) columns (one group per thread),
+// grid.y over rows (each block loops over rows gridDim.y apart).  The
+// destination's base and pitch are 16-byte aligned, so a thread gathers its V
+// elements with plain loads (the source is the unaligned one) and writes them
+// with one 16-byte store.
 template <typename T>
-__global__ void pack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst,
-                                 int64_t ld_dst, int64_t rows, int64_t cols) {
+__global__ void __launch_bounds__(256) pack_rows_kernel(const T *__restrict__ src, int64_t ld_src,
+                                                        T *__restrict__ dst, int64_t ld_dst,
+                                                        int64_t rows, int64_t cols) {
     grid_dependency_wait();
     grid_launch_dependents();
-    const int64_t total = rows * cols;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / cols;
-        const int64_t c = i - r * cols;
-        dst[r * ld_dst + c] = src[r * ld_src + c];
+    constexpr int V = 16 / static_cast<int>(sizeof(T));
+    const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * V;
+    if (c >= cols) return;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const T *s = src + r * ld_src + c;
+        T *d = dst + r * ld_dst + c;
+        if (c + V <= cols) {
+            union {
+                T e[V];
+                uint4 u;
+            } w;
+#pragma unroll
+            for (int e = 0; e < V; ++e) w.e[e] = s[e];
+            *reinterpret_cast<uint4 *>(d) = w.u;
+        } else {
+            for (int e = 0; c + e < cols; ++e) d[e] = s[e];
+        }
     }
 }
 
@@ -242,18 +259,24 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream
 cudaError_t launch_pack_rows(const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                              int64_t rows, int64_t cols, int esize, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (esize != 1 && esize != 2 && esize != 4) return cudaErrorInvalidValue;
     const int threads = 256;
-    const int blocks = grid_for(rows * cols, threads);
+    const int64_t per_block = static_cast<int64_t>(threads) * (16 / esize);   // columns
+    const int bx = static_cast<int>((cols + per_block - 1) / per_block);
+    const int total = grid_for(static_cast<int64_t>(bx) * rows * threads, threads);
+    const int by = static_cast<int>(std::min<int64_t>(std::min<int64_t>(rows, 65535),
+                                                       std::max<int64_t>(1, total / bx)));
+    const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(by));
     if (esize == 1)
-        return launch_pdl(pack_rows_kernel<uint8_t>, dim3(blocks), dim3(threads), stream,
+        return launch_pdl(pack_rows_kernel<uint8_t>, grid, dim3(threads), stream,
                           static_cast<const uint8_t *>(src), ld_src, static_cast<uint8_t *>(dst),
                           ld_dst, rows, cols);
     if (esize == 2)
-        return launch_pdl(pack_rows_kernel<uint16_t>, dim3(blocks), dim3(threads), stream,
+        return launch_pdl(pack_rows_kernel<uint16_t>, grid, dim3(threads), stream,
                           static_cast<const uint16_t *>(src), ld_src,
                           static_cast<uint16_t *>(dst), ld_dst, rows, cols);
     if (esize == 4)
-        return launch_pdl(pack_rows_kernel<uint32_t>, dim3(blocks), dim3(threads), stream,
+        return launch_pdl(pack_rows_kernel<uint32_t>, grid, dim3(threads), stream,
                           static_cast<const uint32_t *>(src), ld_src,
                           static_cast<uint32_t *>(dst), ld_dst, rows, cols);
     return cudaErrorInvalidValue;

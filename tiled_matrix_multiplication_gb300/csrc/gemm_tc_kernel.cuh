@@ -264,6 +264,49 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int split, int ro
     }
 }
 
+// Store a warp's 32 rows x 32 columns chunk (this lane's row `row` in r[])
+// through the warp's staging area `stg` (32 x 32 words, 16-byte aligned): each
+// lane writes its row with 16-byte stores, then the warp writes one row at a
+// time with lanes on consecutive columns, so a store instruction covers 32
+// consecutive columns of one row instead of one column of 32 rows.  Row i of
+// the chunk takes 128 bytes with its 16-byte pieces swizzled (piece p at
+// p ^ (i & 7)), so neither pass has bank conflicts.  For C whose base or row
+// pitch rules out wide stores, and split-K partials whose row length is not a
+// multiple of 4.  Called by all 32 lanes with the same wrow0 (the warp's
+// first row) and col < N.
+__device__ __forceinline__ void store_chunk_rows(const TcParams &p, int split, int wrow0, int col,
+                                                 int lane, uint32_t (&r)[32], float *stg,
+                                                 int z = 0) {
+    const int ncols = min(32, p.N - col);
+    const int row = wrow0 + lane;
+    if (p.splits == 1 && p.epi.on && row < p.M) epi_chunk32(p.epi, p.out_kind, row, col, ncols, r, z);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4 *>(stg + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+    __syncwarp();
+    const int rows = min(32, p.M - wrow0);
+    const int piece = lane >> 2, word = lane & 3;
+#pragma unroll 1
+    for (int i = 0; i < rows; ++i) {
+        const float v = stg[i * 32 + ((piece ^ (i & 7)) << 2) + word];
+        if (lane >= ncols) continue;
+        if (p.splits > 1) {
+            p.partial[(static_cast<int64_t>(split) * p.M + wrow0 + i) * p.N + col + lane] = v;
+            continue;
+        }
+        const int64_t off = static_cast<int64_t>(z) * p.stride_c +
+                            static_cast<int64_t>(wrow0 + i) * p.ldc + col + lane;
+        if (p.out_kind == OUT_F32)
+            static_cast<float *>(p.c)[off] = v;
+        else if (p.out_kind == OUT_F16)
+            static_cast<__half *>(p.c)[off] = __float2half_rn(v);
+        else
+            static_cast<__nv_bfloat16 *>(p.c)[off] = __float2bfloat16_rn(v);
+    }
+    __syncwarp();   // the staging area is free for the next chunk
+}
+
 // Writes 16 bytes (four 32-bit words) as chunk `chunk` (0..3) of this lane's
 // 64-byte row of an output staging box, with the 64-byte swizzle a TMA store
 // of that box expects (16-byte chunk index XOR address bits 7..8).  Eight
@@ -533,6 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rewritten only after the TMA store issued kOutBufs boxes earlier has
         // finished reading it
         const uint32_t my_boxes = sOut + static_cast<uint32_t>(ew * kOutBufs * kOutBox);
+        // the same 4 KB as 32 x 32 words, for C written without TMA stores
+        float *my_stg = reinterpret_cast<float *>(gbase + (my_boxes - base));
+        static_assert(kOutBufs * kOutBox >= 32 * 32 * 4, "a warp's staging holds a 32 x 32 chunk");
         uint32_t nbox = 0;
         auto next_box = [&]() {
             if (nbox >= kOutBufs) {
@@ -591,7 +637,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_load_32cols_sync(taddr + c0, r);
                 const int col = wk.tn * BN + c0;
                 if (!tma) {
-                    if (row < p.M && col < p.N) store_chunk(p, wk.split, row, col, r, wk.z);
+                    if (col < p.N) {
+                        // wide per-row stores where C (or the partials) allow
+                        // them, else one row at a time through the staging area
+                        const bool wide = (p.splits > 1 ? (p.N & 3) == 0 : p.c_vector != 0) &&
+                                          col + 32 <= p.N;
+                        if (wide) {
+                            if (row < p.M) store_chunk(p, wk.split, row, col, r, wk.z);
+                        } else if (wrow0 < p.M) {
+                            store_chunk_rows(p, wk.split, wrow0, col, lane, r, my_stg, wk.z);
+                        }
+                    }
                     continue;
                 }
                 const bool in_range = wrow0 < p.M && col < p.N;   // the box holds valid C
