@@ -46,6 +46,8 @@ CASES = [
     (128, 8192, 2048, "f16", "f16", dict(path=SK)),          # split of 2, one CTA per SM
     (128, 1300, 1000, "f16", "f32", dict(path=SK, block_n=256, splits=4)),
     (100, 2048, 1024, "e4m3", "bf16", dict(path=SK)),
+    (1000, 1999, 777, "f32", "f32", {}),                    # TF32, packed, C row by row
+    (2048, 4096, 1024, "f16", "f16", {}),                   # the planner's pairs sharing A, many tiles
 ]
 
 
