@@ -76,10 +76,10 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, 
 // `batch` > 1: that many products with 16-byte aligned operands (no packing,
 // no K split across kernels) in one launch; the batch index is the slowest
 // dimension of the work list.
-void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
-               int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
-               const tg_options *opt, Plan *pl, int pair_slots, int quad_slots,
-               int64_t batch) {
+static void make_plan_uncached(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda,
+                               const void *b, int64_t ldb, const void *c, int64_t ldc,
+                               tg_dtype din, tg_dtype dout, int num_sms, const tg_options *opt,
+                               Plan *pl, int pair_slots, int quad_slots, int64_t batch) {
     tg_plan &p = pl->pub;
     std::memset(&p, 0, sizeof(p));
     const int ei = esize_of(din), eo = esize_of(dout);
@@ -284,6 +284,60 @@ void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, cons
     p.kernels = (p.pack_a ? 1 : 0) + (p.pack_b ? 1 : 0) + 1 + (global_partials ? 1 : 0);
     const int tmo = (opt && opt->timeout_ms) ? opt->timeout_ms : kDefaultTimeoutMs;
     pl->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
+}
+
+// The plans of recent calls.  make_plan_uncached is a pure function of its
+// arguments -- of the operand pointers only whether each is 16-byte aligned --
+// and tries every kernel variant and split count (about 1 us of host time for
+// a small product, a fifth of a call's), so a repeated shape takes its plan
+// from here.  16 entries, replaced round-robin, under a lock.
+namespace {
+struct PlanKey {
+    int64_t M, N, K, lda, ldb, ldc, stride_c, batch;
+    int32_t din, dout, num_sms, pair_slots, quad_slots, align, has_opt, pad;
+    tg_options opt;
+};
+struct PlanCache {
+    std::mutex mu;
+    PlanKey key[16];
+    Plan plan[16];
+    int used = 0, next = 0;
+};
+PlanCache &plan_cache() {
+    static PlanCache cache;
+    return cache;
+}
+}  // namespace
+
+void make_plan(int64_t M, int64_t N, int64_t K, const void *a, int64_t lda, const void *b,
+               int64_t ldb, const void *c, int64_t ldc, tg_dtype din, tg_dtype dout, int num_sms,
+               const tg_options *opt, Plan *pl, int pair_slots, int quad_slots,
+               int64_t batch) {
+    PlanKey k;
+    std::memset(&k, 0, sizeof(k));   // padding included: keys compare bytewise
+    k.M = M, k.N = N, k.K = K, k.lda = lda, k.ldb = ldb, k.ldc = ldc;
+    k.stride_c = pl->stride_c, k.batch = batch;
+    k.din = din, k.dout = dout, k.num_sms = num_sms;
+    k.pair_slots = pair_slots, k.quad_slots = quad_slots;
+    k.align = (aligned16(a) ? 1 : 0) | (aligned16(b) ? 2 : 0) | (aligned16(c) ? 4 : 0);
+    k.has_opt = opt != nullptr;
+    if (opt) k.opt = *opt;
+    PlanCache &cache = plan_cache();
+    {
+        std::lock_guard<std::mutex> lock(cache.mu);
+        for (int i = 0; i < cache.used; ++i) {
+            if (std::memcmp(&cache.key[i], &k, sizeof(k)) == 0) {
+                *pl = cache.plan[i];
+                return;
+            }
+        }
+    }
+    make_plan_uncached(M, N, K, a, lda, b, ldb, c, ldc, din, dout, num_sms, opt, pl, pair_slots,
+                       quad_slots, batch);
+    std::lock_guard<std::mutex> lock(cache.mu);
+    const int i = cache.used < 16 ? cache.used++ : (cache.next++ & 15);
+    cache.key[i] = k;
+    cache.plan[i] = *pl;
 }
 
 // Argument rules of tg_gemm_strided_batched on top of those of one product.
