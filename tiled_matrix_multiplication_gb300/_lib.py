@@ -88,6 +88,8 @@ _lib = None
 def load(path: str | None = None):
     """Load the library (raises if it is missing -- build it with ``build()``)."""
     global _lib
+    if _lib is not None and path is None:   # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
